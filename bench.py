@@ -1,0 +1,341 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused Hyper-Connection step (hc_post -> hc_mixes -> split/Sinkhorn -> hc_pre ->
+RMSNorm) on GB300: one step = one hc_post_then_pre over the prefill batch B=4, T=4096 (16,384
+tokens, hc=4, d=5120) of seeded synthetic inputs already resident in HBM.
+
+Prints one JSON line. `value` is tokens/s over all ranks; `roofline` rates the fused kernel
+against the measured HBM copy bandwidth; `e2e` repeats the step through the same C-ABI call with
+the inputs copied from pinned host memory and the results copied back inside the timed region;
+`cpu_baseline` times the CPU oracle (double precision) on this host's cores on a sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun every rank runs its own batch (weak scaling, no data-path collective).
+`--impl reference` times the CPU oracle itself as the reference arm.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "HC step tokens/s and achieved HBM GB/s vs peak, prefill B=4 T=4096"
+WORKLOAD = "prefill_b4_t4096"
+BYTES_PER_TOKEN = 102592      # read X 40960 + delta 10240 + post 16 + comb 64 + pre_mix 16;
+                              # write X' 40960 + y_normed 10240 + pre/post/comb 96
+PARAM_BYTES = 1986668         # hc_fn fp32 1966080 + norm_w 20480 + hc_base 96 + hc_scale 12
+FUSED_SOURCES = ["hyper_connection_residual_hc_gb300/csrc/hc_fused.cu", "hyper_connection_residual_hc_gb300/csrc/hc_ptx.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "hc_fused_prefill_b4_t4096_traffic.json")
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _source_hash():
+    h = hashlib.sha256()
+    for rel in FUSED_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_per_launch(n_tokens):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary, scaled to this
+    launch's token count; None when absent or taken on another version of the kernel."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    if t.get("source_sha256_16") != _source_hash():
+        return None
+    return float(t["dram_bytes_per_launch"]) * n_tokens / float(t["tokens"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _oracle_sample_rate(w, tokens, threads):
+    """Oracle hc_post_then_pre on the first `tokens` tokens of the workload: tokens/s."""
+    import oracle as orc
+    from hyper_connection_residual_hc_gb300 import synth
+    from hyper_connection_residual_hc_gb300.synth import T_COMB, T_DELTA, T_POST, T_PREMIX, T_X
+    prm = synth.params(w, 0)
+    args = (synth.tokens(w, T_DELTA, 0, 0, tokens), synth.tokens(w, T_X, 0, 0, tokens),
+            synth.tokens(w, T_POST, 0, 0, tokens), synth.tokens(w, T_COMB, 0, 0, tokens),
+            synth.tokens(w, T_PREMIX, 0, 0, tokens))
+    t0 = time.perf_counter()
+    orc.hc_post_then_pre(*args, prm["hc_fn"], prm["hc_scale"], prm["hc_base"], prm["norm_w"], w.iters, w.hc_eps,
+                         w.norm_eps, threads=threads)
+    return tokens / (time.perf_counter() - t0)
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle as it stands, on this host's cores, a bounded sample per step."""
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    import oracle as orc
+    from hyper_connection_residual_hc_gb300 import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    threads = orc.hardware_threads()
+    # size each step so that warmup + steps take about two minutes at most
+    rate = _oracle_sample_rate(w, 2 * threads, threads)
+    per_step = max(threads, min(w.n, int(rate * 120.0 / max(1, args.steps + args.warmup))))
+    for _ in range(args.warmup):
+        _oracle_sample_rate(w, per_step, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_sample_rate(w, per_step, threads)
+    el = time.perf_counter() - t0
+    value = per_step * args.steps / el
+    sample = "first %d of the %d tokens of %s per step (hc_post_then_pre, float64 oracle)" % (per_step, w.n, WORKLOAD)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens": w.n, "hc": w.hc, "d": w.d, "sinkhorn_iters": w.iters},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import hyper_connection_residual_hc_gb300 as hc
+    from hyper_connection_residual_hc_gb300 import synth
+    from hyper_connection_residual_hc_gb300.synth import T_COMB, T_DELTA, T_POST, T_PREMIX, T_X
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    hc.load()
+
+    w0 = synth.WORKLOADS[WORKLOAD]
+    import dataclasses
+    w = dataclasses.replace(w0, seed=w0.seed + 17 * rank) if rank else w0  # each rank its own batch
+    n, d = w.n, w.d
+    prm = synth.params(w, 0)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    def f32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+
+    host = dict(delta=bf(synth.tokens(w, T_DELTA, 0)), X=bf(synth.tokens(w, T_X, 0)),
+                post=f32(synth.tokens(w, T_POST, 0)), comb=f32(synth.tokens(w, T_COMB, 0)),
+                pre_mix=f32(synth.tokens(w, T_PREMIX, 0)))
+    dev = {k: v.cuda() for k, v in host.items()}
+    hc_fn = f32(prm["hc_fn"]).cuda()
+    planes = torch.empty(hc.hc_prepare_params_size(4, d) // 2, dtype=torch.bfloat16, device="cuda")
+    hc.hc_prepare_params(hc_fn, 4, d, planes)
+    scale, base, nw = f32(prm["hc_scale"]).cuda(), f32(prm["hc_base"]).cuda(), f32(prm["norm_w"]).cuda()
+    P = hc.params(planes, scale, base, nw)
+    s = hc.shape(d=d, sinkhorn_iters=w.iters, hc_eps=w.hc_eps, norm_eps=w.norm_eps)
+    out = dict(X_out=torch.empty((n, 4, d), dtype=torch.bfloat16, device="cuda"),
+               y_normed=torch.empty((n, d), dtype=torch.bfloat16, device="cuda"),
+               pre=torch.empty((n, 4), dtype=torch.float32, device="cuda"),
+               post=torch.empty((n, 4), dtype=torch.float32, device="cuda"),
+               comb=torch.empty((n, 4, 4), dtype=torch.float32, device="cuda"))
+    stream = torch.cuda.current_stream()
+
+    def step():
+        hc.hc_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, n, s, out["X_out"],
+                            out["y_normed"], out["pre"], out["post"], out["comb"], stream)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    barrier()
+    werr = hc.hc_device_error(clear=True)
+
+    # timed region: one fused launch per step, CUDA events on the launching stream around each launch
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    el_ms = t_start.elapsed_time(t_end)
+    kern_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    if dist is not None:
+        t = torch.tensor([el_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        el_ms = float(t.item())
+    derr = hc.hc_device_error(clear=True)
+
+    # end to end through the C ABI: pinned host inputs in, results out, every step
+    pin_in = {k: v.pin_memory() for k, v in host.items()}
+    pin_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
+    e2e_steps = max(3, min(20, args.steps))
+    h2d = sum(v.numel() * v.element_size() for v in pin_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in pin_out.values())
+
+    def e2e_step():
+        for k in dev:
+            dev[k].copy_(pin_in[k], non_blocking=True)
+        step()
+        for k in out:
+            pin_out[k].copy_(out[k], non_blocking=True)
+        stream.synchronize()
+
+    e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    barrier()
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    tokens_total = n * world
+    value = tokens_total * args.steps / (el_ms / 1e3)
+    peak, peak_kind = _peaks()
+    alg_bytes = n * BYTES_PER_TOKEN + PARAM_BYTES
+    achieved = alg_bytes / (kern_ms / 1e3) / 1e9
+    clusters = hc.hc_fused_clusters()
+    tile_m, tiles = hc.hc_plan_tiles(n, clusters)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle as orc
+        threads = orc.hardware_threads()
+        r0 = _oracle_sample_rate(w, 2 * threads, threads)
+        sample_tokens = int(max(threads, min(n, r0 * 15.0)))  # about 15 s of wall time at most
+        rate = _oracle_sample_rate(w, sample_tokens, threads)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": "hc_post_then_pre on the first %d of the %d tokens of %s, float64 oracle, %d threads"
+                         % (sample_tokens, n, WORKLOAD, threads)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": el_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens_per_gpu": n, "B": w.B, "T": w.T, "hc": w.hc, "d": d,
+                       "sinkhorn_iters": w.iters, "hc_eps": w.hc_eps, "norm_eps": w.norm_eps,
+                       "stream_dtype": "bf16", "coefficient_dtype": "f32",
+                       "l2": "no flush: every step reads 839 MB of inputs and writes 839 MB, far above the 129 MB L2",
+                       "tile_tokens": tile_m, "tiles": tiles, "clusters_of_8": clusters,
+                       "hbm_gb_per_s": alg_bytes * args.steps / (el_ms / 1e3) / 1e9},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": _traffic_per_launch(n), "algorithmic_bytes": alg_bytes,
+                         "kernel": "hc_fused_kernel<true>", "kernel_ms": kern_ms},
+            "cpu_baseline": cpu,
+            "e2e": {"value": tokens_total * e2e_steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                       "samples": clk["samples"]},
+            "gpu_launches": args.steps,
+            "device_error": werr | derr,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

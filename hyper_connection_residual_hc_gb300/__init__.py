@@ -1,0 +1,168 @@
+"""GB300 (sm_103a) Hyper-Connection stream step: Python binding of the C-ABI library libhc.so.
+
+Every function here has the name and the argument order of the C entry point it wraps
+(``include/hc.h``); the binding only turns tensors into raw device pointers, picks the current
+CUDA stream when none is given and raises :class:`HCError` on a nonzero status. All arithmetic
+runs in the library's CUDA kernels. There is no fallback: if libhc.so is missing or cannot be
+loaded, :func:`load` raises.
+
+Device buffers are torch tensors (or integer device addresses); the caller allocates and owns
+them, and must keep them alive until the stream has finished with them.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libhc.so")
+
+HC_OK = 0
+HC_ERR_NULL = -1
+HC_ERR_SHAPE = -2
+HC_ERR_UNSUPPORTED = -3
+HC_ERR_ALIGN = -4
+HC_ERR_ALIAS = -5
+HC_ERR_ARG = -6
+HC_ERR_CUDA = -7
+HC_ERR_DEVICE = -8
+
+# every symbol include/hc.h declares
+SYMBOLS = (
+    "hc_prepare_params_size", "hc_prepare_params", "hc_pre_step", "hc_post_then_pre", "hc_post",
+    "hc_debug_mixes", "hc_plan_tiles", "hc_fused_clusters", "hc_device_error", "hc_status_string",
+)
+
+
+class HCError(RuntimeError):
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__("%s failed: %s (status %d)" % (fn, message, status))
+        self.status = status
+
+
+class hc_shape_t(ctypes.Structure):
+    _fields_ = [("hc", ctypes.c_int), ("d", ctypes.c_int), ("sinkhorn_iters", ctypes.c_int),
+                ("hc_eps", ctypes.c_float), ("norm_eps", ctypes.c_float)]
+
+
+class hc_params_t(ctypes.Structure):
+    _fields_ = [("hc_fn_planes", ctypes.c_void_p), ("hc_scale", ctypes.c_void_p), ("hc_base", ctypes.c_void_p),
+                ("norm_w", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libhc.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError("libhc.so not found at %s: build it with hyper_connection_residual_hc_gb300.build.build()"
+                           % path)
+    lib = ctypes.CDLL(path)
+    P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.hc_prepare_params_size.argtypes = [I, I, ctypes.POINTER(ctypes.c_size_t)]
+    lib.hc_prepare_params.argtypes = [P, I, I, P, P]
+    lib.hc_pre_step.argtypes = [P, P, hc_params_t, I64, hc_shape_t, P, P, P, P, P]
+    lib.hc_post_then_pre.argtypes = [P, P, P, P, P, hc_params_t, I64, hc_shape_t, P, P, P, P, P, P]
+    lib.hc_post.argtypes = [P, P, P, P, I64, hc_shape_t, P, P]
+    lib.hc_debug_mixes.argtypes = [P, hc_params_t, I64, hc_shape_t, P, P]
+    lib.hc_plan_tiles.argtypes = [I64, I, ctypes.POINTER(I), ctypes.POINTER(I64)]
+    lib.hc_fused_clusters.argtypes = [ctypes.POINTER(I)]
+    lib.hc_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), I, P]
+    lib.hc_status_string.argtypes = [I]
+    lib.hc_status_string.restype = ctypes.c_char_p
+    for name in SYMBOLS:
+        if name != "hc_status_string":
+            getattr(lib, name).restype = I
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(fn: str, status: int):
+    if status != HC_OK:
+        raise HCError(fn, status, load().hc_status_string(status).decode())
+
+
+def shape(d: int = 5120, sinkhorn_iters: int = 20, hc_eps: float = 1e-6, norm_eps: float = 1e-6, hc: int = 4):
+    return hc_shape_t(hc, d, sinkhorn_iters, hc_eps, norm_eps)
+
+
+def params(hc_fn_planes, hc_scale, hc_base, norm_w) -> hc_params_t:
+    """An hc_params_t of device pointers (the tensors must outlive its use)."""
+    return hc_params_t(_ptr(hc_fn_planes), _ptr(hc_scale), _ptr(hc_base), _ptr(norm_w))
+
+
+def hc_status_string(status: int) -> str:
+    return load().hc_status_string(status).decode()
+
+
+def hc_prepare_params_size(hc: int, d: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("hc_prepare_params_size", load().hc_prepare_params_size(hc, d, ctypes.byref(out)))
+    return out.value
+
+
+def hc_prepare_params(hc_fn, hc: int, d: int, planes, stream=None) -> None:
+    _check("hc_prepare_params", load().hc_prepare_params(_ptr(hc_fn), hc, d, _ptr(planes), _stream(stream)))
+
+
+def hc_pre_step(X, pre_mix, p: hc_params_t, n: int, s: hc_shape_t, y_normed, pre, post, comb, stream=None) -> None:
+    _check("hc_pre_step", load().hc_pre_step(_ptr(X), _ptr(pre_mix), p, n, s, _ptr(y_normed), _ptr(pre), _ptr(post),
+                                             _ptr(comb), _stream(stream)))
+
+
+def hc_post_then_pre(delta, X, post, comb, pre_mix, nxt: hc_params_t, n: int, s: hc_shape_t, X_out, y_normed,
+                     pre_out, post_out, comb_out, stream=None) -> None:
+    _check("hc_post_then_pre", load().hc_post_then_pre(
+        _ptr(delta), _ptr(X), _ptr(post), _ptr(comb), _ptr(pre_mix), nxt, n, s, _ptr(X_out), _ptr(y_normed),
+        _ptr(pre_out), _ptr(post_out), _ptr(comb_out), _stream(stream)))
+
+
+def hc_post(delta, X, post, comb, n: int, s: hc_shape_t, X_out, stream=None) -> None:
+    _check("hc_post", load().hc_post(_ptr(delta), _ptr(X), _ptr(post), _ptr(comb), n, s, _ptr(X_out),
+                                     _stream(stream)))
+
+
+def hc_debug_mixes(X, p: hc_params_t, n: int, s: hc_shape_t, mixes, stream=None) -> None:
+    _check("hc_debug_mixes", load().hc_debug_mixes(_ptr(X), p, n, s, _ptr(mixes), _stream(stream)))
+
+
+def hc_plan_tiles(n: int, clusters: int):
+    tm = ctypes.c_int(0)
+    nt = ctypes.c_int64(0)
+    _check("hc_plan_tiles", load().hc_plan_tiles(n, clusters, ctypes.byref(tm), ctypes.byref(nt)))
+    return tm.value, nt.value
+
+
+def hc_fused_clusters() -> int:
+    c = ctypes.c_int(0)
+    _check("hc_fused_clusters", load().hc_fused_clusters(ctypes.byref(c)))
+    return c.value
+
+
+def hc_device_error(clear: bool = True, stream=None) -> int:
+    w = ctypes.c_uint(0)
+    _check("hc_device_error", load().hc_device_error(ctypes.byref(w), 1 if clear else 0, _stream(stream)))
+    return w.value

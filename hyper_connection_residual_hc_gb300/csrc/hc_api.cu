@@ -1,0 +1,339 @@
+// C ABI of libhc.so (declared in include/hc.h): host-side argument validation, the two
+// elementwise kernels (standalone writing half, weight splitting) and dispatch to the fused
+// reading-half kernel.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/hc.h"
+#include "hc_internal.h"
+
+namespace hc {
+namespace {
+
+constexpr int kHC = 4;
+constexpr int kMix = (2 + kHC) * kHC;
+
+// ---- writing half: X' = bf16(post_k * delta + sum_j comb[j,k] X_j) ---------------------------
+// "Write the streams" page, formula for X'_{n,k}; "Source layer, pairs pooled" page, Block.hc_post
+// excerpt. One thread per (token, 8 columns); all four streams of those columns, so X_out may be X.
+
+__device__ __forceinline__ float lo16(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float hi16(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pk(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(256) hc_post_kernel(const uint4* __restrict__ X, const uint4* __restrict__ delta,
+                                                      const float4* __restrict__ post, const float4* __restrict__ comb,
+                                                      uint4* X_out, long long n, int dv) {
+    const long long total = n * dv;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+        const long long t = idx / dv;
+        const long long i = idx - t * dv;
+        const float4 pst = __ldg(post + t);
+        float c[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 v = __ldg(comb + t * 4 + j);
+            c[4 * j] = v.x; c[4 * j + 1] = v.y; c[4 * j + 2] = v.z; c[4 * j + 3] = v.w;
+        }
+        const float pv[4] = {pst.x, pst.y, pst.z, pst.w};
+        float x[4][8], dl[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 v = __ldcs(X + (t * 4 + j) * dv + i);
+            x[j][0] = lo16(v.x); x[j][1] = hi16(v.x); x[j][2] = lo16(v.y); x[j][3] = hi16(v.y);
+            x[j][4] = lo16(v.z); x[j][5] = hi16(v.z); x[j][6] = lo16(v.w); x[j][7] = hi16(v.w);
+        }
+        {
+            const uint4 v = __ldcs(delta + t * dv + i);
+            dl[0] = lo16(v.x); dl[1] = hi16(v.x); dl[2] = lo16(v.y); dl[3] = hi16(v.y);
+            dl[4] = lo16(v.z); dl[5] = hi16(v.z); dl[6] = lo16(v.w); dl[7] = hi16(v.w);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float s = pv[k] * dl[e];
+                s = fmaf(c[0 * 4 + k], x[0][e], s);
+                s = fmaf(c[1 * 4 + k], x[1][e], s);
+                s = fmaf(c[2 * 4 + k], x[2][e], s);
+                s = fmaf(c[3 * 4 + k], x[3][e], s);
+                o[e] = s;
+            }
+            __stcs(X_out + (t * 4 + k) * dv + i, make_uint4(pk(o[0], o[1]), pk(o[2], o[3]), pk(o[4], o[5]), pk(o[6], o[7])));
+        }
+    }
+}
+
+// ---- weight split: hc_fn = hi + mid + lo, three bf16 planes ----------------------------------
+// Plane rows are grouped for the fused kernel's accumulator drain: row 36*h + 12*p + i holds
+// plane p (0 hi, 1 mid, 2 lo) of mix 12*h + i.
+__global__ void __launch_bounds__(256) hc_prepare_kernel(const float* __restrict__ fn, __nv_bfloat16* planes,
+                                                         long long D) {
+    const long long total = static_cast<long long>(kMix) * D;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+        const long long m = idx / D;
+        const long long c = idx - m * D;
+        const float w = fn[idx];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+        const float r1 = w - __bfloat162float(hi);  // exact (Sterbenz)
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const float r2 = r1 - __bfloat162float(mid);  // exact; at most 8 significant bits remain
+        const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+        const long long hh = m / 12, i = m % 12;
+        planes[(36 * hh + 0 + i) * D + c] = hi;
+        planes[(36 * hh + 12 + i) * D + c] = mid;
+        planes[(36 * hh + 24 + i) * D + c] = lo;
+    }
+}
+
+int grid_for(long long work, int per_block) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    long long blocks = (work + per_block - 1) / per_block;
+    const long long cap = static_cast<long long>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return static_cast<int>(blocks);
+}
+
+// ---- validation ---------------------------------------------------------------------------------
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na && nb && x < y + nb && y < x + na;
+}
+
+int check_shape_fused(int64_t n, const hc_shape_t& s) {
+    if (n < 0) return HC_ERR_SHAPE;
+    if (s.hc < 1 || s.d < 1) return HC_ERR_SHAPE;
+    if (s.d % 256 != 0) return HC_ERR_SHAPE;
+    if (n > 0x7FFFFFFFLL) return HC_ERR_SHAPE;
+    if (s.hc != kHC) return HC_ERR_UNSUPPORTED;
+    if (s.d > 5120) return HC_ERR_UNSUPPORTED;
+    if (s.sinkhorn_iters < 1) return HC_ERR_ARG;
+    if (!std::isfinite(s.hc_eps) || s.hc_eps < 0.f || !std::isfinite(s.norm_eps) || s.norm_eps < 0.f)
+        return HC_ERR_ARG;
+    return HC_OK;
+}
+
+int check_params(const hc_params_t& p) {
+    if (!p.hc_fn_planes || !p.hc_scale || !p.hc_base || !p.norm_w) return HC_ERR_NULL;
+    if (!aligned16(p.hc_fn_planes) || !aligned16(p.hc_scale) || !aligned16(p.hc_base) || !aligned16(p.norm_w))
+        return HC_ERR_ALIGN;
+    return HC_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? HC_OK : HC_ERR_CUDA; }
+
+}  // namespace
+}  // namespace hc
+
+using namespace hc;
+
+extern "C" {
+
+const char* hc_status_string(int status) {
+    switch (status) {
+        case HC_OK: return "ok";
+        case HC_ERR_NULL: return "a required pointer is NULL";
+        case HC_ERR_SHAPE: return "invalid shape (n < 0, or d not a positive multiple of the required granule)";
+        case HC_ERR_UNSUPPORTED: return "configuration not implemented by the GPU path (hc != 4 or d > 5120)";
+        case HC_ERR_ALIGN: return "a device pointer is not 16-byte aligned";
+        case HC_ERR_ALIAS: return "an output overlaps an input or another output";
+        case HC_ERR_ARG: return "invalid scalar argument (sinkhorn_iters < 1, or an eps negative or not finite)";
+        case HC_ERR_CUDA: return "a CUDA call or kernel launch failed";
+        case HC_ERR_DEVICE: return "a kernel gave up a bounded wait";
+        default: return "unknown status";
+    }
+}
+
+int hc_prepare_params_size(int hc, int d, size_t* bytes) {
+    if (!bytes) return HC_ERR_NULL;
+    if (hc < 1 || d < 1) return HC_ERR_SHAPE;
+    *bytes = static_cast<size_t>(3) * static_cast<size_t>((2 + hc) * hc) * static_cast<size_t>(hc) *
+             static_cast<size_t>(d) * 2u;
+    return HC_OK;
+}
+
+int hc_prepare_params(const float* hc_fn, int hc, int d, void* planes, hc_stream_t stream) {
+    if (!hc_fn || !planes) return HC_ERR_NULL;
+    if (hc < 1 || d < 1 || d % 8 != 0) return HC_ERR_SHAPE;
+    if (hc != kHC) return HC_ERR_UNSUPPORTED;
+    if (!aligned16(hc_fn) || !aligned16(planes)) return HC_ERR_ALIGN;
+    const long long D = static_cast<long long>(hc) * d;
+    if (overlap(hc_fn, static_cast<size_t>(kMix * D) * 4, planes, static_cast<size_t>(3 * kMix * D) * 2))
+        return HC_ERR_ALIAS;
+    const long long work = kMix * D;
+    hc_prepare_kernel<<<grid_for(work, 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        hc_fn, static_cast<__nv_bfloat16*>(planes), D);
+    return cuda_status(cudaGetLastError());
+}
+
+int hc_post(const void* delta, const void* X, const float* post, const float* comb, int64_t n, hc_shape_t s,
+            void* X_out, hc_stream_t stream) {
+    if (!delta || !X || !post || !comb || !X_out) return HC_ERR_NULL;
+    if (n < 0 || s.hc < 1 || s.d < 1 || s.d % 8 != 0 || n > (1LL << 40)) return HC_ERR_SHAPE;
+    if (s.hc != kHC) return HC_ERR_UNSUPPORTED;
+    if (!aligned16(delta) || !aligned16(X) || !aligned16(post) || !aligned16(comb) || !aligned16(X_out))
+        return HC_ERR_ALIGN;
+    const size_t xb = static_cast<size_t>(n) * kHC * s.d * 2, db = static_cast<size_t>(n) * s.d * 2;
+    if ((X_out != X && overlap(X_out, xb, X, xb)) || overlap(X_out, xb, delta, db) ||
+        overlap(X_out, xb, post, static_cast<size_t>(n) * 16) || overlap(X_out, xb, comb, static_cast<size_t>(n) * 64))
+        return HC_ERR_ALIAS;
+    if (n == 0) return HC_OK;
+    const int dv = s.d / 8;
+    hc_post_kernel<<<grid_for(n * dv, 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(X), static_cast<const uint4*>(delta), reinterpret_cast<const float4*>(post),
+        reinterpret_cast<const float4*>(comb), static_cast<uint4*>(X_out), n, dv);
+    return cuda_status(cudaGetLastError());
+}
+
+int hc_pre_step(const void* X, const float* pre_mix, hc_params_t p, int64_t n, hc_shape_t s, void* y_normed,
+                float* pre, float* post, float* comb, hc_stream_t stream) {
+    if (!X || !pre_mix || !y_normed || !pre || !post || !comb) return HC_ERR_NULL;
+    int st = check_params(p);
+    if (st != HC_OK) return st;
+    st = check_shape_fused(n, s);
+    if (st != HC_OK) return st;
+    if (!aligned16(X) || !aligned16(pre_mix) || !aligned16(y_normed) || !aligned16(pre) || !aligned16(post) ||
+        !aligned16(comb))
+        return HC_ERR_ALIGN;
+    const size_t N = static_cast<size_t>(n);
+    const size_t xb = N * kHC * s.d * 2, yb = N * s.d * 2, cb = N * 16, kb = N * 64;
+    const void* outs[4] = {y_normed, pre, post, comb};
+    const size_t osz[4] = {yb, cb, cb, kb};
+    const void* ins[2] = {X, pre_mix};
+    const size_t isz[2] = {xb, cb};
+    for (int i = 0; i < 4; ++i) {
+        for (int j = 0; j < 2; ++j)
+            if (overlap(outs[i], osz[i], ins[j], isz[j])) return HC_ERR_ALIAS;
+        for (int j = i + 1; j < 4; ++j)
+            if (overlap(outs[i], osz[i], outs[j], osz[j])) return HC_ERR_ALIAS;
+    }
+    if (n == 0) return HC_OK;
+    FusedArgs a = {};
+    a.post_mode = false;
+    a.X = X;
+    a.pre_mix = pre_mix;
+    a.planes = p.hc_fn_planes;
+    a.hc_scale = p.hc_scale;
+    a.hc_base = p.hc_base;
+    a.norm_w = p.norm_w;
+    a.y_normed = y_normed;
+    a.pre_out = pre;
+    a.post_out = post;
+    a.comb_out = comb;
+    a.n = n;
+    a.d = s.d;
+    a.iters = s.sinkhorn_iters;
+    a.hc_eps = s.hc_eps;
+    a.norm_eps = s.norm_eps;
+    return launch_fused(a, reinterpret_cast<cudaStream_t>(stream)) == 0 ? HC_OK : HC_ERR_CUDA;
+}
+
+int hc_post_then_pre(const void* delta, const void* X, const float* post, const float* comb, const float* pre_mix,
+                     hc_params_t next, int64_t n, hc_shape_t s, void* X_out, void* y_normed, float* pre_out,
+                     float* post_out, float* comb_out, hc_stream_t stream) {
+    if (!delta || !X || !post || !comb || !pre_mix || !X_out || !y_normed || !pre_out || !post_out || !comb_out)
+        return HC_ERR_NULL;
+    int st = check_params(next);
+    if (st != HC_OK) return st;
+    st = check_shape_fused(n, s);
+    if (st != HC_OK) return st;
+    const void* ptrs[10] = {delta, X, post, comb, pre_mix, X_out, y_normed, pre_out, post_out, comb_out};
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return HC_ERR_ALIGN;
+    const size_t N = static_cast<size_t>(n);
+    const size_t xb = N * kHC * s.d * 2, yb = N * s.d * 2, cb = N * 16, kb = N * 64;
+    const void* ins[5] = {delta, X, post, comb, pre_mix};
+    const size_t isz[5] = {yb, xb, cb, kb, cb};
+    const void* outs[5] = {X_out, y_normed, pre_out, post_out, comb_out};
+    const size_t osz[5] = {xb, yb, cb, cb, kb};
+    for (int i = 0; i < 5; ++i) {
+        for (int j = 0; j < 5; ++j)
+            if (overlap(outs[i], osz[i], ins[j], isz[j])) return HC_ERR_ALIAS;
+        for (int j = i + 1; j < 5; ++j)
+            if (overlap(outs[i], osz[i], outs[j], osz[j])) return HC_ERR_ALIAS;
+    }
+    if (n == 0) return HC_OK;
+    FusedArgs a = {};
+    a.post_mode = true;
+    a.X = X;
+    a.delta = delta;
+    a.post = post;
+    a.comb = comb;
+    a.pre_mix = pre_mix;
+    a.planes = next.hc_fn_planes;
+    a.hc_scale = next.hc_scale;
+    a.hc_base = next.hc_base;
+    a.norm_w = next.norm_w;
+    a.X_out = X_out;
+    a.y_normed = y_normed;
+    a.pre_out = pre_out;
+    a.post_out = post_out;
+    a.comb_out = comb_out;
+    a.n = n;
+    a.d = s.d;
+    a.iters = s.sinkhorn_iters;
+    a.hc_eps = s.hc_eps;
+    a.norm_eps = s.norm_eps;
+    return launch_fused(a, reinterpret_cast<cudaStream_t>(stream)) == 0 ? HC_OK : HC_ERR_CUDA;
+}
+
+int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float* mixes, hc_stream_t stream) {
+    if (!X || !mixes || !p.hc_fn_planes) return HC_ERR_NULL;
+    hc_shape_t s2 = s;
+    if (s2.sinkhorn_iters < 1) s2.sinkhorn_iters = 1;
+    int st = check_shape_fused(n, s2);
+    if (st != HC_OK) return st;
+    if (!aligned16(X) || !aligned16(mixes) || !aligned16(p.hc_fn_planes)) return HC_ERR_ALIGN;
+    const size_t N = static_cast<size_t>(n);
+    if (overlap(mixes, N * kMix * 4, X, N * kHC * s.d * 2)) return HC_ERR_ALIAS;
+    if (n == 0) return HC_OK;
+    // the kernel reads scale/base/norm_w unconditionally: point them at the planes (never used)
+    FusedArgs a = {};
+    a.post_mode = false;
+    a.X = X;
+    a.planes = p.hc_fn_planes;
+    a.hc_scale = static_cast<const float*>(p.hc_fn_planes);
+    a.hc_base = static_cast<const float*>(p.hc_fn_planes);
+    a.norm_w = static_cast<const float*>(p.hc_fn_planes);
+    a.mixes_out = mixes;
+    a.n = n;
+    a.d = s.d;
+    a.iters = s2.sinkhorn_iters;
+    a.hc_eps = s2.hc_eps;
+    a.norm_eps = s2.norm_eps;
+    return launch_fused(a, reinterpret_cast<cudaStream_t>(stream)) == 0 ? HC_OK : HC_ERR_CUDA;
+}
+
+int hc_plan_tiles(int64_t n, int clusters, int* tile_m, int64_t* num_tiles) {
+    if (!tile_m || !num_tiles) return HC_ERR_NULL;
+    if (n < 0 || clusters < 1) return HC_ERR_SHAPE;
+    plan_tiles(n, clusters, tile_m, num_tiles);
+    return HC_OK;
+}
+
+int hc_fused_clusters(int* clusters) {
+    if (!clusters) return HC_ERR_NULL;
+    return fused_active_clusters(clusters) == 0 ? HC_OK : HC_ERR_CUDA;
+}
+
+int hc_device_error(unsigned int* word, int clear, hc_stream_t stream) {
+    if (!word) return HC_ERR_NULL;
+    return read_device_error(word, clear, reinterpret_cast<cudaStream_t>(stream)) == 0 ? HC_OK : HC_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,835 @@
+// Fused Hyper-Connection stream step for GB300 (sm_103a).
+//
+// One launch computes, per token (DeepSeek V4.1 model-atlas pages):
+//   [post mode] X' = bf16(post_k * Delta + sum_j comb[j,k] * X_j)      "Write the streams" page,
+//                                                                      formula for X'_{n,k}
+//   r     = 1/sqrt(mean(X'^2 over all 4*d values) + norm_eps)         "Source layer, pairs pooled"
+//   mixes = r * (X'_flat . hc_fn^T)        (24 numbers)                page, Block.hc_mixes excerpt
+//   pre / post / comb from mixes: sigmoid, 2*sigmoid, softmax rows     "Reading weights" page,
+//            + eps then Sinkhorn column/row normalisation             hc_split_sinkhorn excerpt
+//   y        = bf16(sum_j pre_mix_j * X'_j)                            Block.hc_pre excerpt
+//   y_normed = bf16(norm_w * y / sqrt(mean(y^2) + norm_eps))           "Final RMSNorm" page,
+//                                                                      RMSNorm excerpt
+// In pre-step mode X' is the input X itself and nothing is written back to the streams.
+//
+// Decomposition. A cluster of 8 CTAs owns a tile of up to 128 tokens; CTA `rank` owns the
+// d-slice [rank*d/8, (rank+1)*d/8) of every stream. Per 32-column stage a CTA:
+//   - TMA-loads the four X tiles [tokens x 32 cols], the Delta tile and the four matching
+//     slices of the split projection weights (bf16 planes hi/mid/lo, 72 rows) into shared
+//     memory, 64-byte swizzled;
+//   - computes X' in place (thread = token: 8 compute warps, two per TMEM lane quadrant, each
+//     warp owning 16 of the 32 columns), accumulates sum(X'^2), forms y, rounds it, accumulates
+//     sum(y^2) and parks the bf16 y row-slice in tensor memory;
+//   - lets one thread issue 8 tcgen05.mma (M=128 tokens, N=80 >= 72 plane rows, K=16) that
+//     project the bf16 X' tile on the three planes; the products are exact in fp32, so the
+//     split projection has fp32-FFMA accuracy;
+//   - TMA-stores the X' tile (written once) from the same shared-memory buffer;
+//   - drains the stage's accumulator from TMEM into 12 per-thread fp32 sums (the three planes
+//     added back together); the two TMEM accumulators alternate so the MMA of stage s+1 runs
+//     while stage s drains.
+// At the end of a tile the CTAs exchange their 28 partial sums per token through distributed
+// shared memory: every CTA finishes RMSNorm for its slice of y (read back from TMEM, TMA-stored),
+// and CTA `rank` runs the split and Sinkhorn for the tokens t with t % 8 == rank.
+//
+// Every wait on an mbarrier is bounded in time; on expiry the kernel records an error in a
+// device word, stops waiting everywhere, finishes its loops without hanging, frees its tensor
+// memory and returns.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include "hc_internal.h"
+#include "hc_ptx.cuh"
+
+namespace hc {
+
+constexpr int kMix = 24;
+constexpr int kBRows = 72;        // 3 planes x 24 mixes
+constexpr int kUmmaM = 128;
+constexpr int kUmmaN = 80;        // smallest legal N >= 72 at M = 128
+constexpr int kCluster = 8;
+constexpr int kTileMax = 128;
+constexpr int kChunk = 32;        // columns per stage: 64-byte rows
+constexpr int kStages = 3;
+constexpr int kComputeWarps = 8;
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
+constexpr int kWarpStore = 10;
+constexpr int kWarpSplit = 11;
+constexpr int kThreads = 12 * 32;
+constexpr int kMaxDSlice = 640;   // d <= 5120
+
+// shared memory layout, offsets from a 1024-byte aligned base
+constexpr int kXTileBytes = kTileMax * kChunk * 2;            // 8192: 128 rows x 64 B
+constexpr int kBTileBytes = kBRows * kChunk * 2;              // 4608: 72 rows x 64 B (the MMA reads
+                                                              // 80 rows; rows 72..79 are ignored)
+constexpr int kOffX = 0;
+constexpr int kOffD = 4 * kXTileBytes;
+constexpr int kOffB = kOffD + kXTileBytes;
+constexpr int kStageBytes = kOffB + 4 * kBTileBytes;          // 59392
+constexpr int kOffYStage = kStages * kStageBytes;
+constexpr int kYStageBytes = 32 * 16 * 2;                     // 32 rows x 32 B
+constexpr int kOffPart = kOffYStage + kComputeWarps * 2 * kYStageBytes;
+constexpr int kPartRows = 28;  // 24 mixes, sum x^2 (two halves), sum y^2 (two halves)
+constexpr int kPartBytes = kPartRows * kTileMax * 4;
+constexpr int kOffNormW = kOffPart + 2 * kPartBytes;
+constexpr int kOffBar = kOffNormW + kMaxDSlice * 4;
+constexpr int kBarFull = 0, kBarXReady = 3, kBarEmpty = 6, kBarAccFull = 9, kBarAccEmpty = 11, kBarMmaDone = 13;
+constexpr int kNumBars = 14;
+constexpr int kOffTmemPtr = kOffBar + kNumBars * 8;
+constexpr int kOffAbort = kOffTmemPtr + 4;
+constexpr int kSmemUsed = kOffAbort + 4;
+constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
+
+static_assert(kWarpSplit == kThreads / 32 - 1, "the split warp is the last one");
+static_assert(kStageBytes % 1024 == 0, "stage buffers keep 1024-byte alignment");
+static_assert(kOffB % 512 == 0 && kBTileBytes % 512 == 0, "B tiles start on 512-byte swizzle atoms");
+static_assert(kOffYStage % 256 == 0, "32-byte swizzle staging needs 256-byte alignment");
+static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in shared memory of one CTA");
+// the MMA of the last B tile of the last stage reads 8 rows (512 B) past it: still inside the CTA
+static_assert(kOffB + 3 * kBTileBytes + kUmmaN * 64 + (kStages - 1) * kStageBytes <= kSmemUsed, "B overrun");
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol0 = 0, kAccCol1 = 96, kYCol = 192;  // y slice: up to 320 columns
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+// device error word: bit set = which wait gave up
+__device__ unsigned int g_hc_error = 0;
+enum : unsigned int {
+    kErrProducer = 1u, kErrMma = 2u, kErrComputeFull = 4u, kErrComputeAcc = 8u, kErrStore = 16u, kErrDrain = 32u
+};
+
+struct FusedParams {
+    const float* post;
+    const float* comb;
+    const float* pre_mix;
+    const float* hc_scale;
+    const float* hc_base;
+    const float* norm_w;
+    float* pre_out;
+    float* post_out;
+    float* comb_out;
+    float* mixes_out;
+    long long n;
+    long long num_tiles;
+    int write_y;
+    int d;
+    int d_slice;
+    int stages_per_tile;
+    int tile_m;
+    int iters;
+    float hc_eps;
+    float norm_eps;
+};
+
+// ---- small helpers ------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // a -> low half
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+    f[0] = bf_lo(v.x); f[1] = bf_hi(v.x); f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
+    f[4] = bf_lo(v.z); f[5] = bf_hi(v.z); f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
+}
+
+// Bounded mbarrier wait shared by all roles of one CTA.
+struct Waiter {
+    volatile uint32_t* abort;
+    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, unsigned int code) const {
+        if (mbar_test(bar, parity)) return true;
+        const uint64_t t0 = global_timer_ns();
+        while (true) {
+            for (int i = 0; i < 32; ++i)
+                if (mbar_test(bar, parity)) return true;
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort = 1u;
+                atomicOr(&g_hc_error, code);
+                return false;
+            }
+        }
+    }
+    // Same, but ignores an abort raised elsewhere: used at exit to let copies in flight land.
+    __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) const {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_test(bar, parity)) {
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                atomicOr(&g_hc_error, kErrDrain);
+                return;
+            }
+        }
+    }
+};
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
+
+// "Reading weights" page, hc_split_sinkhorn kernel excerpt and the formula for p, in fp32.
+__device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const float (&sc)[3], const float (&b)[kMix],
+                                               int iters, float eps, float (&pre)[4], float (&post)[4],
+                                               float (&C)[16]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pre[j] = sigmoidf_(m[j] * sc[0] + b[j]) + eps;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) post[j] = 2.0f * sigmoidf_(m[4 + j] * sc[1] + b[4 + j]);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) C[q] = m[8 + q] * sc[2] + b[8 + q];
+    // softmax over each row (max subtracted), then + eps
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float mx = fmaxf(fmaxf(C[4 * j], C[4 * j + 1]), fmaxf(C[4 * j + 2], C[4 * j + 3]));
+        float e0 = expf(C[4 * j] - mx), e1 = expf(C[4 * j + 1] - mx);
+        float e2 = expf(C[4 * j + 2] - mx), e3 = expf(C[4 * j + 3] - mx);
+        float inv = __frcp_rn((e0 + e1) + (e2 + e3));
+        C[4 * j] = e0 * inv + eps;
+        C[4 * j + 1] = e1 * inv + eps;
+        C[4 * j + 2] = e2 * inv + eps;
+        C[4 * j + 3] = e3 * inv + eps;
+    }
+    auto col_norm = [&]() {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float inv = __frcp_rn(((C[k] + C[4 + k]) + (C[8 + k] + C[12 + k])) + eps);
+            C[k] *= inv;
+            C[4 + k] *= inv;
+            C[8 + k] *= inv;
+            C[12 + k] *= inv;
+        }
+    };
+    auto row_norm = [&]() {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float inv = __frcp_rn(((C[4 * j] + C[4 * j + 1]) + (C[4 * j + 2] + C[4 * j + 3])) + eps);
+            C[4 * j] *= inv;
+            C[4 * j + 1] *= inv;
+            C[4 * j + 2] *= inv;
+            C[4 * j + 3] *= inv;
+        }
+    };
+    col_norm();
+    for (int it = 1; it < iters; ++it) {
+        row_norm();
+        col_norm();
+    }
+}
+
+// ---- the kernel ---------------------------------------------------------------------------------
+
+template <bool kPost>
+__global__ void __launch_bounds__(kThreads, 1)
+    hc_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmD,
+                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmXo,
+                    const __grid_constant__ CUtensorMap tmY, const FusedParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t cid = cluster_id_x();
+    const uint32_t ncl = num_clusters_x();
+    const int d0 = static_cast<int>(rank) * p.d_slice;
+    const int S = p.stages_per_tile;
+
+    auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
+    const Waiter W{abort_flag};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(kBarFull + s), 1);
+            mbar_init(bar(kBarXReady + s), kComputeWarps);
+            mbar_init(bar(kBarEmpty + s), 2);  // MMA completion + X' store done reading
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar(kBarAccFull + a), 1);
+            mbar_init(bar(kBarAccEmpty + a), kComputeWarps);
+        }
+        mbar_init(bar(kBarMmaDone), 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == kWarpProducer && lane == 0) {
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmB);
+        if (kPost) tma_prefetch_desc(&tmD);
+    }
+    {
+        float* nw = reinterpret_cast<float*>(smem + kOffNormW);
+        for (int i = threadIdx.x; i < p.d_slice; i += kThreads) nw[i] = p.norm_w[d0 + i];
+    }
+    if (warp == 0) {
+        tmem_alloc(sbase + kOffTmemPtr, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemPtr);
+
+    const long long my_tiles =
+        (static_cast<long long>(cid) < p.num_tiles) ? (p.num_tiles - 1 - cid) / ncl + 1 : 0;
+
+    if (warp < kComputeWarps) {
+        // ================= compute warps: X', sums, y, accumulator drain, epilogue ============
+        const int q = warp & 3;             // TMEM lane quadrant = token rows 32q..32q+31
+        const int h = warp >> 2;            // column half of each 32-column stage
+        const int row = 32 * q + lane;      // token row inside the tile
+        const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        const float* nw = reinterpret_cast<const float*>(smem + kOffNormW);
+        long long g = 0;        // global stage counter (same sequence in every role)
+        uint32_t ycount = 0;    // y_normed staging buffers used by this warp
+        for (long long it = 0; it < my_tiles; ++it) {
+            const long long tile = cid + it * ncl;
+            const long long t0 = tile * p.tile_m;
+            const long long tok = t0 + row;
+            const bool valid = (row < p.tile_m) && (tok < p.n);
+            float cpost[4] = {0.f, 0.f, 0.f, 0.f}, ccomb[16], pm[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ccomb[i] = 0.f;
+            if (valid) {
+                if (p.pre_mix) {
+                    float4 v = __ldg(reinterpret_cast<const float4*>(p.pre_mix) + tok);
+                    pm[0] = v.x; pm[1] = v.y; pm[2] = v.z; pm[3] = v.w;
+                }
+                if (kPost) {
+                    float4 v = __ldg(reinterpret_cast<const float4*>(p.post) + tok);
+                    cpost[0] = v.x; cpost[1] = v.y; cpost[2] = v.z; cpost[3] = v.w;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float4 c = __ldg(reinterpret_cast<const float4*>(p.comb) + tok * 4 + j);
+                        ccomb[4 * j] = c.x; ccomb[4 * j + 1] = c.y; ccomb[4 * j + 2] = c.z; ccomb[4 * j + 3] = c.w;
+                    }
+                }
+            }
+            float acc[12];
+#pragma unroll
+            for (int i = 0; i < 12; ++i) acc[i] = 0.f;
+            float sx[4] = {0.f, 0.f, 0.f, 0.f};
+            float sy[2] = {0.f, 0.f};
+
+            auto drain = [&](long long gd) {
+                const uint32_t a = static_cast<uint32_t>(gd & 1);
+                const uint32_t par = static_cast<uint32_t>((gd >> 1) & 1);
+                W.wait(bar(kBarAccFull + a), par, kErrComputeAcc);
+                tc_fence_after();
+                uint32_t v[36];
+                const uint32_t col = (a ? kAccCol1 : kAccCol0) + 36u * h;
+                tmem_ld36_wait(tl + col, tl + col + 32u, v);
+#pragma unroll
+                for (int i = 0; i < 12; ++i)
+                    acc[i] += (__uint_as_float(v[i]) + __uint_as_float(v[12 + i])) + __uint_as_float(v[24 + i]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarAccEmpty + a));
+            };
+
+            for (int s = 0; s < S; ++s, ++g) {
+                const int slot = static_cast<int>(g % kStages);
+                const uint32_t par = static_cast<uint32_t>((g / kStages) & 1);
+                W.wait(bar(kBarFull + slot), par, kErrComputeFull);
+                const uint32_t sb = sbase + slot * kStageBytes;
+                uint32_t yb[8];
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = 2 * h + cc;
+                    const uint32_t off = static_cast<uint32_t>(row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
+                    float xr[4][8];
+                    uint4 xv[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) xv[j] = ld_smem_v4(sb + kOffX + j * kXTileBytes + off);
+                    if (kPost) {
+                        float dl[8], xf[4][8];
+                        unpack8(ld_smem_v4(sb + kOffD + off), dl);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) unpack8(xv[j], xf[j]);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            float o[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                float t = cpost[k] * dl[e];
+                                t = fmaf(ccomb[0 * 4 + k], xf[0][e], t);
+                                t = fmaf(ccomb[1 * 4 + k], xf[1][e], t);
+                                t = fmaf(ccomb[2 * 4 + k], xf[2][e], t);
+                                t = fmaf(ccomb[3 * 4 + k], xf[3][e], t);
+                                o[e] = t;
+                            }
+                            uint4 ov;
+                            ov.x = pack_bf16(o[0], o[1]);
+                            ov.y = pack_bf16(o[2], o[3]);
+                            ov.z = pack_bf16(o[4], o[5]);
+                            ov.w = pack_bf16(o[6], o[7]);
+                            st_smem_v4(sb + kOffX + k * kXTileBytes + off, ov);
+                            unpack8(ov, xr[k]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) unpack8(xv[j], xr[j]);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) sx[k] = fmaf(xr[k][e], xr[k][e], sx[k]);
+                    float yv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        float t = pm[0] * xr[0][e];
+                        t = fmaf(pm[1], xr[1][e], t);
+                        t = fmaf(pm[2], xr[2][e], t);
+                        t = fmaf(pm[3], xr[3][e], t);
+                        yv[e] = t;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t u = pack_bf16(yv[2 * e], yv[2 * e + 1]);
+                        yb[cc * 4 + e] = u;
+                        const float a0 = bf_lo(u), a1 = bf_hi(u);
+                        sy[cc] = fmaf(a0, a0, sy[cc]);
+                        sy[cc] = fmaf(a1, a1, sy[cc]);
+                    }
+                }
+                tmem_st8(tl + kYCol + static_cast<uint32_t>(s * 16 + h * 8), yb);
+                if (kPost) fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarXReady + slot));
+                if (s > 0) drain(g - 1);
+            }
+            drain(g - 1);
+
+            // partial sums of this CTA's slice -> shared memory for the cluster exchange
+            float* P = reinterpret_cast<float*>(smem + kOffPart + (it & 1) * kPartBytes);
+#pragma unroll
+            for (int i = 0; i < 12; ++i) P[(12 * h + i) * kTileMax + row] = acc[i];
+            P[(24 + h) * kTileMax + row] = (sx[0] + sx[1]) + (sx[2] + sx[3]);
+            P[(26 + h) * kTileMax + row] = sy[0] + sy[1];
+            tmem_st_wait();
+            cluster_arrive();
+            cluster_wait();
+
+            // RMSNorm of y: the statistic is the sum over all 8 slices
+            const uint32_t pa = sbase + kOffPart + static_cast<uint32_t>((it & 1) * kPartBytes);
+            float syt = 0.f;
+            for (uint32_t r = 0; r < kCluster; ++r) {
+                const uint32_t ra = dsmem_addr(pa, r);
+                syt += ld_dsmem_f32(ra + static_cast<uint32_t>((26 * kTileMax + row) * 4)) +
+                       ld_dsmem_f32(ra + static_cast<uint32_t>((27 * kTileMax + row) * 4));
+            }
+            const float ry = 1.0f / sqrtf(syt / static_cast<float>(p.d) + p.norm_eps);
+
+            if (p.write_y && 32 * q < p.tile_m) {
+                for (int s = 0; s < S; ++s) {
+                    uint32_t yv[8];
+                    tmem_ld8_wait(tl + kYCol + static_cast<uint32_t>(s * 16 + h * 8), yv);
+                    const float* w = nw + s * 32 + h * 16;
+                    uint32_t ov[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float a0 = w[2 * e] * (bf_lo(yv[e]) * ry);
+                        const float a1 = w[2 * e + 1] * (bf_hi(yv[e]) * ry);
+                        ov[e] = pack_bf16(a0, a1);
+                    }
+                    const uint32_t buf = ycount & 1u;
+                    ++ycount;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    const uint32_t st = sbase + kOffYStage + static_cast<uint32_t>((warp * 2 + buf) * kYStageBytes);
+                    const uint32_t sw = static_cast<uint32_t>((lane >> 2) & 1);
+                    st_smem_v4(st + lane * 32 + ((0u ^ sw) << 4), make_uint4(ov[0], ov[1], ov[2], ov[3]));
+                    st_smem_v4(st + lane * 32 + ((1u ^ sw) << 4), make_uint4(ov[4], ov[5], ov[6], ov[7]));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmY, st, d0 + s * 32 + h * 16, static_cast<int>(t0 + 32 * q));
+                        bulk_commit();
+                    }
+                }
+            }
+        }
+        if (lane == 0) bulk_wait<0>();
+    } else if (warp == kWarpProducer) {
+        // ================= TMA producer =========================================================
+        uint64_t pol_stream = 0, pol_keep = 0;
+        if (lane == 0) {
+            pol_stream = policy_evict_first();
+            pol_keep = policy_evict_last();
+        }
+        const uint32_t bytes = static_cast<uint32_t>(4 * p.tile_m * 64 + (kPost ? p.tile_m * 64 : 0) + 4 * kBTileBytes);
+        long long g = 0;
+        for (long long it = 0; it < my_tiles; ++it) {
+            const long long tile = cid + it * ncl;
+            const int t0 = static_cast<int>(tile * p.tile_m);
+            for (int s = 0; s < S; ++s, ++g) {
+                const int slot = static_cast<int>(g % kStages);
+                const long long round = g / kStages;
+                if (round > 0) W.wait(bar(kBarEmpty + slot), static_cast<uint32_t>((round - 1) & 1), kErrProducer);
+                if (lane == 0) {
+                    const uint32_t sb = sbase + slot * kStageBytes;
+                    const uint32_t fb = bar(kBarFull + slot);
+                    const int col = d0 + s * kChunk;
+                    mbar_arrive_expect_tx(fb, bytes);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) tma_load_3d(sb + kOffX + j * kXTileBytes, &tmX, fb, col, j, t0, pol_stream);
+                    if (kPost) tma_load_2d(sb + kOffD, &tmD, fb, col, t0, pol_stream);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) tma_load_2d(sb + kOffB + k * kBTileBytes, &tmB, fb, k * p.d + col, 0, pol_keep);
+                }
+                __syncwarp();
+            }
+            if (it > 0) cluster_wait();
+            cluster_arrive();
+        }
+        if (my_tiles > 0) cluster_wait();
+        // let every load issued land before the CTA can exit
+        const long long issued = g;
+        for (long long gg = (issued > kStages ? issued - kStages : 0); gg < issued; ++gg)
+            W.drain(bar(kBarFull + static_cast<int>(gg % kStages)), static_cast<uint32_t>((gg / kStages) & 1));
+    } else if (warp == kWarpMma) {
+        // ================= MMA issuer ===========================================================
+        constexpr uint32_t idesc = idesc_bf16_f32(kUmmaM, kUmmaN);
+        long long g = 0;
+        for (long long it = 0; it < my_tiles; ++it) {
+            for (int s = 0; s < S; ++s, ++g) {
+                const int slot = static_cast<int>(g % kStages);
+                const uint32_t a = static_cast<uint32_t>(g & 1);
+                const long long ra = g >> 1;
+                if (ra > 0) W.wait(bar(kBarAccEmpty + a), static_cast<uint32_t>((ra - 1) & 1), kErrMma);
+                W.wait(bar(kBarXReady + slot), static_cast<uint32_t>((g / kStages) & 1), kErrMma);
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sb = sbase + slot * kStageBytes;
+                    const uint32_t dcol = tmem + (a ? kAccCol1 : kAccCol0);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint64_t ad = sdesc_kmajor_sw64(sb + kOffX + k * kXTileBytes + kk * 32);
+                            const uint64_t bd = sdesc_kmajor_sw64(sb + kOffB + k * kBTileBytes + kk * 32);
+                            umma_bf16(dcol, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
+                        }
+                    }
+                    umma_commit(bar(kBarEmpty + slot));
+                    umma_commit(bar(kBarAccFull + a));
+                }
+                __syncwarp();
+            }
+            if (it > 0) cluster_wait();
+            cluster_arrive();
+        }
+        if (my_tiles > 0) cluster_wait();
+        if (lane == 0) {
+            umma_commit(bar(kBarMmaDone));
+            W.drain(bar(kBarMmaDone), 0);
+        }
+        __syncwarp();
+    } else if (warp == kWarpStore) {
+        // ================= X' writer (post mode) and slot release ================================
+        long long g = 0;
+        for (long long it = 0; it < my_tiles; ++it) {
+            const long long tile = cid + it * ncl;
+            const int t0 = static_cast<int>(tile * p.tile_m);
+            for (int s = 0; s < S; ++s, ++g) {
+                const int slot = static_cast<int>(g % kStages);
+                W.wait(bar(kBarXReady + slot), static_cast<uint32_t>((g / kStages) & 1), kErrStore);
+                if (kPost && lane == 0) {
+                    const uint32_t sb = sbase + slot * kStageBytes;
+                    const int col = d0 + s * kChunk;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) tma_store_3d(&tmXo, sb + kOffX + k * kXTileBytes, col, k, t0);
+                    bulk_commit();
+                    bulk_wait_read<0>();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarEmpty + slot));
+            }
+            if (it > 0) cluster_wait();
+            cluster_arrive();
+        }
+        if (my_tiles > 0) cluster_wait();
+        if (lane == 0) bulk_wait<0>();
+    } else {  // warp == kWarpSplit
+        // ================= split + Sinkhorn for this CTA's share of each tile ===================
+        float sc[3], bs[kMix];
+#pragma unroll
+        for (int i = 0; i < 3; ++i) sc[i] = __ldg(p.hc_scale + i);
+#pragma unroll
+        for (int i = 0; i < kMix; ++i) bs[i] = __ldg(p.hc_base + i);
+        for (long long it = 0; it < my_tiles; ++it) {
+            cluster_arrive();
+            cluster_wait();
+            const long long tile = cid + it * ncl;
+            const long long t0 = tile * p.tile_m;
+            const int r_tok = static_cast<int>(rank) + kCluster * lane;
+            if (lane < kTileMax / kCluster && r_tok < p.tile_m && t0 + r_tok < p.n) {
+                const long long tok = t0 + r_tok;
+                const uint32_t pa = sbase + kOffPart + static_cast<uint32_t>((it & 1) * kPartBytes);
+                float m[kMix];
+#pragma unroll
+                for (int i = 0; i < kMix; ++i) m[i] = 0.f;
+                float sxt = 0.f;
+                for (uint32_t r = 0; r < kCluster; ++r) {
+                    const uint32_t ra = dsmem_addr(pa, r);
+#pragma unroll
+                    for (int i = 0; i < kMix; ++i)
+                        m[i] += ld_dsmem_f32(ra + static_cast<uint32_t>((i * kTileMax + r_tok) * 4));
+                    sxt += ld_dsmem_f32(ra + static_cast<uint32_t>((24 * kTileMax + r_tok) * 4)) +
+                           ld_dsmem_f32(ra + static_cast<uint32_t>((25 * kTileMax + r_tok) * 4));
+                }
+                const float rr = 1.0f / sqrtf(sxt / static_cast<float>(4 * p.d) + p.norm_eps);
+#pragma unroll
+                for (int i = 0; i < kMix; ++i) m[i] *= rr;
+                if (p.mixes_out) {
+                    float4* mo = reinterpret_cast<float4*>(p.mixes_out + tok * kMix);
+#pragma unroll
+                    for (int i = 0; i < kMix / 4; ++i) mo[i] = make_float4(m[4 * i], m[4 * i + 1], m[4 * i + 2], m[4 * i + 3]);
+                }
+                if (p.pre_out) {
+                    float pre[4], post[4], C[16];
+                    split_sinkhorn(m, sc, bs, p.iters, p.hc_eps, pre, post, C);
+                    reinterpret_cast<float4*>(p.pre_out)[tok] = make_float4(pre[0], pre[1], pre[2], pre[3]);
+                    reinterpret_cast<float4*>(p.post_out)[tok] = make_float4(post[0], post[1], post[2], post[3]);
+                    float4* co = reinterpret_cast<float4*>(p.comb_out) + tok * 4;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) co[j] = make_float4(C[4 * j], C[4 * j + 1], C[4 * j + 2], C[4 * j + 3]);
+                }
+            }
+            __syncwarp();
+        }
+    }
+
+    // nobody may read this CTA's shared memory after it exits
+    cluster_arrive();
+    cluster_wait();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---- host side ----------------------------------------------------------------------------------
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+            const uint32_t* box, CUtensorMapSwizzle sw) {
+    auto fn = get_encode();
+    if (!fn) return false;
+    uint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
+                    reinterpret_cast<const cuuint64_t*>(dims), reinterpret_cast<const cuuint64_t*>(strides_bytes),
+                    reinterpret_cast<const cuuint32_t*>(box), reinterpret_cast<const cuuint32_t*>(estr),
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct DeviceState {
+    bool ready = false;
+    int clusters = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int prepare_device(int* clusters) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -7;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        const void* kernels[2] = {reinterpret_cast<const void*>(&hc_fused_kernel<false>),
+                                  reinterpret_cast<const void*>(&hc_fused_kernel<true>)};
+        for (const void* k : kernels)
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+                return -7;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kCluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(kCluster, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, reinterpret_cast<const void*>(&hc_fused_kernel<true>), &cfg) !=
+                cudaSuccess ||
+            nc < 1)
+            return -7;
+        st.clusters = nc;
+        st.ready = true;
+    }
+    *clusters = st.clusters;
+    return 0;
+}
+
+}  // namespace
+
+void plan_tiles(int64_t n, int clusters, int* tile_m, int64_t* num_tiles) {
+    if (n <= 0) {
+        *tile_m = kTileMax;
+        *num_tiles = 0;
+        return;
+    }
+    if (clusters < 1) clusters = 1;
+    if (n <= kTileMax) {
+        // one tile per cluster at most; spread small batches over clusters in 32-token tiles
+        int64_t best_tiles = 1;
+        int best_m = static_cast<int>(n);
+        for (int m = 32; m < n && m <= kTileMax; m += 32) {
+            const int64_t tiles = (n + m - 1) / m;
+            if (tiles <= clusters) {
+                best_m = m;
+                best_tiles = tiles;
+                break;
+            }
+        }
+        *tile_m = best_m;
+        *num_tiles = best_tiles;
+        return;
+    }
+    // cost of a choice: waves x (tokens per tile + fixed per-tile overhead in token-equivalents)
+    const int64_t overhead = 32;
+    int64_t best_cost = -1;
+    int best_m = kTileMax;
+    for (int m = kTileMax; m >= 32; m -= 32) {
+        const int64_t tiles = (n + m - 1) / m;
+        const int64_t waves = (tiles + clusters - 1) / clusters;
+        const int64_t cost = waves * (m + overhead);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best_m = m;
+        }
+    }
+    *tile_m = best_m;
+    *num_tiles = (n + best_m - 1) / best_m;
+}
+
+int fused_active_clusters(int* clusters) { return prepare_device(clusters); }
+
+int launch_fused(const FusedArgs& a, cudaStream_t stream) {
+    int clusters = 0;
+    if (prepare_device(&clusters) != 0) return -7;
+    int tile_m = 0;
+    int64_t num_tiles = 0;
+    plan_tiles(a.n, clusters, &tile_m, &num_tiles);
+    if (num_tiles == 0) return 0;
+
+    const uint64_t n = static_cast<uint64_t>(a.n), d = static_cast<uint64_t>(a.d);
+    CUtensorMap tmX, tmD, tmB, tmXo, tmY;
+    {
+        const uint64_t dims[3] = {d, 4, n};
+        const uint64_t str[2] = {d * 2, 4 * d * 2};
+        const uint32_t box[3] = {kChunk, 1, static_cast<uint32_t>(tile_m)};
+        if (!encode(&tmX, a.X, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+        if (!encode(&tmXo, a.post_mode ? a.X_out : a.X, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+    }
+    {
+        const uint64_t dims[2] = {d, n};
+        const uint64_t str[1] = {d * 2};
+        const uint32_t box[2] = {kChunk, static_cast<uint32_t>(tile_m)};
+        if (!encode(&tmD, a.post_mode ? a.delta : a.X, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+        const uint32_t boxy[2] = {16, 32};
+        if (!encode(&tmY, a.y_normed ? a.y_normed : a.X, 2, dims, str, boxy, CU_TENSOR_MAP_SWIZZLE_32B)) return -7;
+    }
+    {
+        const uint64_t dims[2] = {4 * d, static_cast<uint64_t>(kBRows)};
+        const uint64_t str[1] = {4 * d * 2};
+        const uint32_t box[2] = {kChunk, static_cast<uint32_t>(kBRows)};
+        if (!encode(&tmB, a.planes, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+    }
+
+    FusedParams p;
+    p.post = a.post;
+    p.comb = a.comb;
+    p.pre_mix = a.pre_mix;
+    p.hc_scale = a.hc_scale;
+    p.hc_base = a.hc_base;
+    p.norm_w = a.norm_w;
+    p.pre_out = a.pre_out;
+    p.post_out = a.post_out;
+    p.comb_out = a.comb_out;
+    p.mixes_out = a.mixes_out;
+    p.n = a.n;
+    p.num_tiles = num_tiles;
+    p.write_y = a.y_normed != nullptr;
+    p.d = a.d;
+    p.d_slice = a.d / kCluster;
+    p.stages_per_tile = p.d_slice / kChunk;
+    p.tile_m = tile_m;
+    p.iters = a.iters;
+    p.hc_eps = a.hc_eps;
+    p.norm_eps = a.norm_eps;
+
+    const int64_t grid_clusters = std::min<int64_t>(num_tiles, clusters);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_clusters * kCluster), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (a.post_mode)
+        e = cudaLaunchKernelEx(&cfg, hc_fused_kernel<true>, tmX, tmD, tmB, tmXo, tmY, p);
+    else
+        e = cudaLaunchKernelEx(&cfg, hc_fused_kernel<false>, tmX, tmD, tmB, tmXo, tmY, p);
+    return e == cudaSuccess ? 0 : -7;
+}
+
+int read_device_error(unsigned int* word, int clear, cudaStream_t stream) {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_hc_error, sizeof(v), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return -7;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return -7;
+    if (clear) {
+        const unsigned int z = 0;
+        if (cudaMemcpyToSymbolAsync(g_hc_error, &z, sizeof(z), 0, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return -7;
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return -7;
+    }
+    *word = v;
+    return 0;
+}
+
+}  // namespace hc

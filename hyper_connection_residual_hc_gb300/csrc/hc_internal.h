@@ -1,0 +1,48 @@
+// Host-side declarations shared by the library's translation units (not part of the C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace hc {
+
+// Everything one fused launch needs. Device pointers; optional ones may be null.
+struct FusedArgs {
+    bool post_mode;          // true: hc_post_then_pre; false: hc_pre_step (X used as is)
+    const void* X;           // bf16 [n, 4, d]
+    const void* delta;       // bf16 [n, d]            (post mode)
+    const float* post;       // fp32 [n, 4]            (post mode)
+    const float* comb;       // fp32 [n, 4, 4]         (post mode)
+    const float* pre_mix;    // fp32 [n, 4]            (null: zeros; diagnostic use only)
+    const void* planes;      // bf16 [72, 4d]
+    const float* hc_scale;   // fp32 [3]
+    const float* hc_base;    // fp32 [24]
+    const float* norm_w;     // fp32 [d]
+    void* X_out;             // bf16 [n, 4, d]         (post mode)
+    void* y_normed;          // bf16 [n, d]            (null: not written)
+    float* pre_out;          // fp32 [n, 4]            (null: not written)
+    float* post_out;         // fp32 [n, 4]
+    float* comb_out;         // fp32 [n, 4, 4]
+    float* mixes_out;        // fp32 [n, 24]           (null: not written)
+    int64_t n;
+    int d;
+    int iters;
+    float hc_eps;
+    float norm_eps;
+};
+
+// Tile plan of the fused kernel: tokens per tile and number of tiles for n tokens when
+// `clusters` thread-block clusters run concurrently.
+void plan_tiles(int64_t n, int clusters, int* tile_m, int64_t* num_tiles);
+
+// Launches the fused kernel; returns an HC_* status.
+int launch_fused(const FusedArgs& a, cudaStream_t stream);
+
+// Reads (and optionally clears) the device error word of the current device.
+int read_device_error(unsigned int* word, int clear, cudaStream_t stream);
+
+// Co-resident clusters of the fused kernel on the current device (cached per device).
+int fused_active_clusters(int* clusters);
+
+}  // namespace hc

@@ -1,0 +1,157 @@
+/*
+ * hc.h -- C ABI of the GB300 (sm_103a) Hyper-Connection stream-step library (libhc.so).
+ *
+ * The Hyper-Connection residual keeps hc parallel copies ("streams") of the hidden state.
+ * Around every sublayer the model (DeepSeek V4.1 model-atlas pages) does, per token:
+ *   writing half  ("Write the streams" page, formula for X'_{n,k}; "Source layer, pairs pooled"
+ *                  page, Block.hc_post excerpt):
+ *       X'_k = post_k * Delta + sum_j comb[j,k] * X_j            (fp32 math, cast to bf16)
+ *   reading half  (same page, Block.hc_mixes and Block.hc_pre excerpts; "Reading weights" page,
+ *                  hc_split_sinkhorn kernel excerpt and the formula for p; "Final RMSNorm" page,
+ *                  RMSNorm excerpt):
+ *       r      = 1 / sqrt(mean over all hc*d values of X'^2 + norm_eps)
+ *       mixes  = r * (X'_flat . hc_fn^T)                      24 numbers at hc = 4
+ *       pre    = sigmoid(s0*mixes[0:hc] + base) + hc_eps
+ *       post   = 2*sigmoid(s1*mixes[hc:2hc] + base)
+ *       comb   = Sinkhorn(softmax_rows(s2*mixes[2hc:] + base) + hc_eps), sinkhorn_iters rounds
+ *       y      = bf16(sum_j pre_mix_j * X'_j)                 pre_mix = the INCOMING reading mix
+ *       y_normed = bf16(norm_w * y / sqrt(mean(y^2) + norm_eps))
+ * Block.forward ("Source layer, pairs pooled" page) hands the (pre, post, comb) computed by one
+ * sublayer to the next: the returned pre is the next call's pre_mix, post/comb are the next
+ * call's post/comb.
+ *
+ * Conventions for every entry point
+ *   - Pointers marked [device] are CUDA device pointers in the current device's context; the
+ *     caller allocates and owns every buffer. The library never allocates or frees device memory
+ *     and never synchronises the stream, except hc_device_error (documented there).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *   - All arrays are contiguous row-major; tokens are flattened, n = batch * positions.
+ *   - bf16 is IEEE bfloat16 (16-bit storage); fp32 is IEEE binary32.
+ *   - Layouts: X, X_out [n, hc, d] bf16; delta, y_normed [n, d] bf16; pre_mix, pre, post [n, hc]
+ *     fp32; comb [n, hc, hc] fp32 with comb[t, j, k]: j = source stream (summed over in the
+ *     writing half), k = destination stream. mixes order: [pre hc | post hc | comb hc*hc, row j
+ *     then column k].
+ *   - Every device pointer must be 16-byte aligned (HC_ERR_ALIGN otherwise).
+ *   - n == 0 is a no-op that returns HC_OK. n < 0 returns HC_ERR_SHAPE.
+ *   - Arguments are validated on the host before anything is launched; a failed check returns a
+ *     negative status and leaves every output untouched. No exception crosses the ABI.
+ *   - Floating-point specials (NaN, Inf) in the data propagate; they are never trapped.
+ */
+#ifndef HC_GB300_H
+#define HC_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* hc_stream_t; /* identical to cudaStream_t */
+
+/* Status codes. */
+enum {
+    HC_OK = 0,
+    HC_ERR_NULL = -1,        /* a required pointer is NULL */
+    HC_ERR_SHAPE = -2,       /* n < 0, or d not a positive multiple of the supported granule */
+    HC_ERR_UNSUPPORTED = -3, /* a valid configuration this GPU path does not implement (hc != 4, d > 5120) */
+    HC_ERR_ALIGN = -4,       /* a device pointer is not 16-byte aligned */
+    HC_ERR_ALIAS = -5,       /* an output overlaps an input or another output (see each call) */
+    HC_ERR_ARG = -6,         /* sinkhorn_iters < 1, or an eps negative or not finite */
+    HC_ERR_CUDA = -7,        /* a CUDA runtime/driver call or kernel launch failed */
+    HC_ERR_DEVICE = -8       /* a kernel gave up a bounded wait (see hc_device_error) */
+};
+
+/* Problem shape and scalar constants. The model's values ("Router" page, config.json excerpt):
+ * hc = 4 (hc_mult), d = 5120 (dim), sinkhorn_iters = 20, hc_eps = 1e-6, norm_eps = 1e-20. */
+typedef struct {
+    int hc;             /* streams; the GPU path implements hc == 4 */
+    int d;              /* width of one stream: a multiple of 256, at most 5120, for the fused calls;
+                           a multiple of 8 for hc_post */
+    int sinkhorn_iters; /* >= 1: one softmax + column normalisation, then iters-1 row+column rounds */
+    float hc_eps;       /* >= 0, finite: the eps of pre and of the Sinkhorn normalisations */
+    float norm_eps;     /* >= 0, finite: used by both the mixes statistic and the sublayer RMSNorm */
+} hc_shape_t;
+
+/* One sublayer's HC parameters ("Source layer, pairs pooled" page, Block.__init__ excerpt:
+ * hc_fn [mix_hc, hc*d], hc_base [mix_hc], hc_scale [3], mix_hc = (2+hc)*hc; the sublayer's
+ * RMSNorm weight [d]). All [device]. */
+typedef struct {
+    const void* hc_fn_planes; /* bf16 [3*mix_hc, hc*d]: hc_fn split by hc_prepare_params. Required. */
+    const float* hc_scale;    /* fp32 [3] */
+    const float* hc_base;     /* fp32 [mix_hc] */
+    const float* norm_w;      /* fp32 [d] */
+} hc_params_t;
+
+/* Size in bytes of the buffer hc_prepare_params fills: 3 * (2+hc)*hc * hc*d * 2.
+ * Returns HC_ERR_NULL / HC_ERR_SHAPE on bad arguments. Host-only, no CUDA call. */
+int hc_prepare_params_size(int hc, int d, size_t* bytes);
+
+/* Split an fp32 hc_fn [(2+hc)*hc, hc*d] [device] into three bf16 planes hi + mid + lo whose sum
+ * equals every fp32 weight exactly, laid out for the fused kernels' tensor-core projection,
+ * into `planes` [device] (hc_prepare_params_size bytes, 16-byte aligned). Run it once per
+ * parameter set (weights are static); the planes stay valid while hc_fn is unchanged.
+ * No counterpart on the pages: it is this library's weight packing. hc must be 4. */
+int hc_prepare_params(const float* hc_fn, int hc, int d, void* planes, hc_stream_t stream);
+
+/* Reading half of one sublayer ("Source layer, pairs pooled" page, Block.forward excerpt, the
+ * lines up to the sublayer's norm): hc_mixes of X with `p`, hc_pre of X with pre_mix, RMSNorm.
+ *   X        [device] bf16 [n, hc, d]      the incoming streams
+ *   pre_mix  [device] fp32 [n, hc]         the reading mix handed over by the previous sublayer
+ *   p        this sublayer's parameters
+ *   y_normed [device] bf16 [n, d]          out: the sublayer's input
+ *   pre, post [device] fp32 [n, hc]; comb [device] fp32 [n, hc, hc]   out: this sublayer's
+ *            coefficients (pre goes to the next sublayer, post/comb to this one's hc_post)
+ * Outputs must not overlap each other or any input (HC_ERR_ALIAS). */
+int hc_pre_step(const void* X, const float* pre_mix, hc_params_t p, int64_t n, hc_shape_t s,
+                void* y_normed, float* pre, float* post, float* comb, hc_stream_t stream);
+
+/* Writing half of a sublayer, then the reading half of the next one, fused in one pass:
+ *   X_out = hc_post(delta, X, post, comb)   ("Write the streams" page, formula for X')
+ *   (y_normed, pre_out, post_out, comb_out) = hc_pre_step(X_out, pre_mix, next)
+ *   delta [device] bf16 [n, d]      the sublayer's output
+ *   X     [device] bf16 [n, hc, d]  the streams the sublayer read (its residual)
+ *   post, comb [device] fp32        this sublayer's writing coefficients
+ *   pre_mix [device] fp32 [n, hc]   the reading mix for the next sublayer (the pre returned by
+ *                                   the call that produced post/comb)
+ *   next                            the next sublayer's parameters
+ * X_out is written once. Outputs must not overlap each other or any input (HC_ERR_ALIAS). */
+int hc_post_then_pre(const void* delta, const void* X, const float* post, const float* comb,
+                     const float* pre_mix, hc_params_t next, int64_t n, hc_shape_t s, void* X_out,
+                     void* y_normed, float* pre_out, float* post_out, float* comb_out,
+                     hc_stream_t stream);
+
+/* Writing half alone ("Write the streams" page): X_out = bf16(post_k*delta + sum_j comb[j,k]*X_j).
+ * For the last sublayer of a stack and for boundaries where another module edits the streams
+ * before the next reading half. s.sinkhorn_iters and the eps fields are ignored; d is a multiple
+ * of 8. X_out may be exactly X (in place); any other overlap with X or delta is HC_ERR_ALIAS. */
+int hc_post(const void* delta, const void* X, const float* post, const float* comb, int64_t n,
+            hc_shape_t s, void* X_out, hc_stream_t stream);
+
+/* Diagnostic: the 24 mix numbers r * (X_flat . hc_fn^T) [device] fp32 [n, (2+hc)*hc] exactly as the
+ * fused reading half computes them (same kernel, same tensor-core projection), for checking the
+ * projection on its own. p.hc_scale, p.hc_base and p.norm_w are not read. */
+int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float* mixes,
+                   hc_stream_t stream);
+
+/* Tile plan of the fused calls for n tokens when `clusters` 8-CTA clusters run at once: tokens per
+ * tile (a multiple of 32 unless one tile holds all n <= 128 tokens) and the number of tiles.
+ * Host-only, no CUDA call. Returns HC_ERR_NULL / HC_ERR_SHAPE on bad arguments. */
+int hc_plan_tiles(int64_t n, int clusters, int* tile_m, int64_t* num_tiles);
+
+/* How many 8-CTA clusters of the fused kernel fit on the current device at once. */
+int hc_fused_clusters(int* clusters);
+
+/* Read the device-side error word of the current device: nonzero when a kernel gave up a
+ * bounded wait (it then returned early and its outputs are not valid). Synchronises `stream`.
+ * If `clear` is nonzero the word is reset to 0. Returns HC_OK, HC_ERR_NULL or HC_ERR_CUDA. */
+int hc_device_error(unsigned int* word, int clear, hc_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char* hc_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HC_GB300_H */

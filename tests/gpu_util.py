@@ -1,0 +1,171 @@
+"""Helpers for the GPU parity tests: device buffers, calls through the C ABI, comparisons with
+the oracle and the tolerances they use.
+
+Tolerances (stated once, used everywhere):
+  bf16 outputs (X', y_normed): at most 1 bf16 ulp from the oracle given the same inputs. The GPU
+    rounds an fp32 value, the oracle an exact one; they differ only near rounding ties.
+  mixes: |gpu - oracle| <= max(1e-5 |m|, 1e-6) + 2 u S, with u = 2^-24 and S = r sum_c |x_c w_mc|:
+    a 20,480-term dot product accumulated in fp32 is off by a few u S whatever the order.
+  pre/post/comb given the GPU's own mixes (stage isolated): rel 1e-5 or abs 1e-6.
+  pre/post/comb end to end: the same, plus the mixes bound pushed through the split: pre and post
+    through the sigmoid's slope, comb through the oracle split's sensitivities (central differences).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import hyper_connection_residual_hc_gb300 as hc
+import oracle as orc
+
+U = 2.0 ** -24
+
+
+def dev_bf16(a_u16: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a_u16).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def dev_f32(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def host_u16(t: torch.Tensor) -> np.ndarray:
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def host_f32(t: torch.Tensor) -> np.ndarray:
+    return t.cpu().numpy().astype(np.float64)
+
+
+class DevParams:
+    """One sublayer's parameters on the device, with hc_fn split by hc_prepare_params."""
+
+    def __init__(self, prm: dict, d: int):
+        self.hc_fn = dev_f32(prm["hc_fn"])
+        self.hc_scale = dev_f32(prm["hc_scale"])
+        self.hc_base = dev_f32(prm["hc_base"])
+        self.norm_w = dev_f32(prm["norm_w"])
+        nbytes = hc.hc_prepare_params_size(4, d)
+        self.planes = torch.empty(nbytes // 2, dtype=torch.bfloat16, device="cuda")
+        hc.hc_prepare_params(self.hc_fn, 4, d, self.planes)
+        self.c = hc.params(self.planes, self.hc_scale, self.hc_base, self.norm_w)
+
+
+def alloc_outputs(n: int, d: int, post_mode: bool):
+    o = dict(y_normed=torch.empty((n, d), dtype=torch.bfloat16, device="cuda"),
+             pre=torch.empty((n, 4), dtype=torch.float32, device="cuda"),
+             post=torch.empty((n, 4), dtype=torch.float32, device="cuda"),
+             comb=torch.empty((n, 4, 4), dtype=torch.float32, device="cuda"))
+    if post_mode:
+        o["X_out"] = torch.empty((n, 4, d), dtype=torch.bfloat16, device="cuda")
+    return o
+
+
+def run_pre_step(X, pre_mix, P: DevParams, s, n):
+    o = alloc_outputs(n, s.d, False)
+    hc.hc_pre_step(X, pre_mix, P.c, n, s, o["y_normed"], o["pre"], o["post"], o["comb"])
+    return o
+
+
+def run_post_then_pre(delta, X, post, comb, pre_mix, P: DevParams, s, n):
+    o = alloc_outputs(n, s.d, True)
+    hc.hc_post_then_pre(delta, X, post, comb, pre_mix, P.c, n, s, o["X_out"], o["y_normed"], o["pre"], o["post"],
+                        o["comb"])
+    return o
+
+
+def debug_mixes(X, P: DevParams, s, n):
+    m = torch.empty((n, 24), dtype=torch.float32, device="cuda")
+    hc.hc_debug_mixes(X, P.c, n, s, m)
+    return m
+
+
+def device_error_clear():
+    w = hc.hc_device_error(clear=True)
+    assert w == 0, "a kernel gave up a bounded wait (word 0x%x)" % w
+
+
+# ---- comparisons --------------------------------------------------------------------------------
+
+def bf16_key(b: np.ndarray) -> np.ndarray:
+    b = b.astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def ulp_diff(a_u16: np.ndarray, b_u16: np.ndarray) -> np.ndarray:
+    return np.abs(bf16_key(a_u16) - bf16_key(b_u16))
+
+
+def assert_bf16_close(gpu_u16, ref_u16, what, max_ulp=1):
+    gpu_u16 = np.asarray(gpu_u16)
+    ref_u16 = np.asarray(ref_u16)
+    nan_g = (gpu_u16 & 0x7F80) == 0x7F80
+    nan_r = (ref_u16 & 0x7F80) == 0x7F80
+    assert np.array_equal(nan_g, nan_r), "%s: non-finite values differ" % what
+    dd = ulp_diff(gpu_u16[~nan_g], ref_u16[~nan_r])
+    worst = int(dd.max()) if dd.size else 0
+    assert worst <= max_ulp, "%s: %d values beyond %d ulp (worst %d ulp)" % (what, int((dd > max_ulp).sum()), max_ulp, worst)
+    return float((dd == 0).mean()) if dd.size else 1.0
+
+
+def mixes_tol(m_ref, S):
+    return np.maximum(1e-5 * np.abs(m_ref), 1e-6) + 2 * U * S
+
+
+def assert_mixes_close(m_gpu, m_ref, S, what="mixes"):
+    err = np.abs(m_gpu - m_ref)
+    tol = mixes_tol(m_ref, S)
+    bad = err > tol
+    assert not bad.any(), "%s: %d beyond tolerance, worst err/tol %.3g" % (what, int(bad.sum()), float((err / tol).max()))
+    return float((err / (U * S)).max())
+
+
+def assert_coef_close(gpu, ref, what, extra=None):
+    tol = np.maximum(1e-5 * np.abs(ref), 1e-6)
+    if extra is not None:
+        tol = tol + extra
+    err = np.abs(gpu - ref)
+    bad = err > tol
+    assert not bad.any(), "%s: %d beyond tolerance, worst err %.3g (tol %.3g)" % (
+        what, int(bad.sum()), float(err[bad].max()), float(tol[bad][np.argmax(err[bad])]))
+
+
+def split_sensitivity_bound(m_ref, S, hc_scale, hc_base, iters, eps):
+    """Bound on |d(pre, post, comb)| from mixes errors up to E = 2 u S + 1e-5|m| + 1e-6, pushed through
+    the oracle split: analytic for pre/post, central differences for comb."""
+    n = m_ref.shape[0]
+    E = 2 * U * S + 1e-5 * np.abs(m_ref) + 1e-6
+    pre0, post0, comb0 = orc.split_sinkhorn(m_ref, hc_scale, hc_base, 4, iters, eps)
+    s0, s1 = float(hc_scale[0]), float(hc_scale[1])
+    sg = pre0 - eps
+    b_pre = abs(s0) * sg * (1 - sg) * E[:, 0:4]
+    sp = post0 / 2
+    b_post = 2 * abs(s1) * sp * (1 - sp) * E[:, 4:8]
+    b_comb = np.zeros((n, 4, 4))
+    for k in range(8, 24):
+        h = np.maximum(E[:, k], 1e-9)
+        mp = m_ref.copy()
+        mm = m_ref.copy()
+        mp[:, k] += h
+        mm[:, k] -= h
+        _, _, cp = orc.split_sinkhorn(mp, hc_scale, hc_base, 4, iters, eps)
+        _, _, cm = orc.split_sinkhorn(mm, hc_scale, hc_base, 4, iters, eps)
+        b_comb += np.abs(cp - cm) / 2
+    return b_pre, b_post, b_comb
+
+
+def check_step(out, ref, m_gpu, m_ref, S, prm, iters, eps, label):
+    """Compare one reading half (pre_step outputs) with the oracle's, both ways:
+    stage-isolated (oracle split on the GPU's mixes) and end to end."""
+    pre_g, post_g, comb_g = host_f32(out["pre"]), host_f32(out["post"]), host_f32(out["comb"])
+    assert_mixes_close(m_gpu, m_ref, S, label + " mixes")
+    pre_i, post_i, comb_i = orc.split_sinkhorn(m_gpu, prm["hc_scale"], prm["hc_base"], 4, iters, eps)
+    assert_coef_close(pre_g, pre_i, label + " pre (isolated)")
+    assert_coef_close(post_g, post_i, label + " post (isolated)")
+    assert_coef_close(comb_g, comb_i, label + " comb (isolated)")
+    bp, bq, bc = split_sensitivity_bound(m_ref, S, prm["hc_scale"], prm["hc_base"], iters, eps)
+    assert_coef_close(pre_g, ref["pre"], label + " pre", bp)
+    assert_coef_close(post_g, ref["post"], label + " post", bq)
+    assert_coef_close(comb_g, ref["comb"], label + " comb", bc)

@@ -1,0 +1,143 @@
+"""Host-side checks of the C-ABI library that need no GPU: it builds for sm_103a, loads, exports
+every entry point include/hc.h declares, validates arguments before touching the device, and
+plans tiles sensibly. Pointers here are fake device addresses that are never dereferenced:
+every call below returns from host-side validation (or is a no-op) before any CUDA call."""
+
+import os
+import re
+import subprocess
+
+import pytest
+
+import hyper_connection_residual_hc_gb300 as hc
+from hyper_connection_residual_hc_gb300 import build as hcbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    hcbuild.build()
+    return hc.load()
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "hc.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(hc_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert _declared_functions() == sorted(hc.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", hc.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (hc_\w+)", out))
+    missing = [s for s in _declared_functions() if s not in exported]
+    assert not missing, missing
+    for s in _declared_functions():
+        assert hasattr(lib, s)
+
+
+def test_status_strings(lib):
+    for code in range(0, -9, -1):
+        assert hc.hc_status_string(code)
+    assert hc.hc_status_string(-100) == "unknown status"
+
+
+def test_prepare_params_size(lib):
+    assert hc.hc_prepare_params_size(4, 5120) == 3 * 24 * 20480 * 2
+    with pytest.raises(hc.HCError) as e:
+        hc.hc_prepare_params_size(4, 0)
+    assert e.value.status == hc.HC_ERR_SHAPE
+
+
+# fake, 256-byte aligned device addresses far apart (never dereferenced)
+A = [0x7F0000000000 + i * (1 << 36) for i in range(16)]
+
+
+def _p():
+    return hc.params(A[10], A[11], A[12], A[13])
+
+
+def _expect(status, fn, *args):
+    with pytest.raises(hc.HCError) as e:
+        fn(*args)
+    assert e.value.status == status, (e.value.status, status)
+
+
+def test_pre_step_validation(lib):
+    s = hc.shape()
+    st = 0
+    _expect(hc.HC_ERR_NULL, hc.hc_pre_step, None, A[1], _p(), 8, s, A[2], A[3], A[4], A[5], st)
+    _expect(hc.HC_ERR_NULL, hc.hc_pre_step, A[0], A[1], hc.params(None, A[11], A[12], A[13]), 8, s, A[2], A[3], A[4], A[5], st)
+    _expect(hc.HC_ERR_SHAPE, hc.hc_pre_step, A[0], A[1], _p(), -1, s, A[2], A[3], A[4], A[5], st)
+    _expect(hc.HC_ERR_SHAPE, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(d=5000), A[2], A[3], A[4], A[5], st)
+    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(hc=2), A[2], A[3], A[4], A[5], st)
+    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(d=5376), A[2], A[3], A[4], A[5], st)
+    _expect(hc.HC_ERR_ARG, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(sinkhorn_iters=0), A[2], A[3], A[4], A[5], st)
+    _expect(hc.HC_ERR_ARG, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(hc_eps=float("nan")), A[2], A[3], A[4], A[5], st)
+    _expect(hc.HC_ERR_ARG, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(norm_eps=-1.0), A[2], A[3], A[4], A[5], st)
+    _expect(hc.HC_ERR_ALIGN, hc.hc_pre_step, A[0] + 8, A[1], _p(), 8, s, A[2], A[3], A[4], A[5], st)
+    _expect(hc.HC_ERR_ALIGN, hc.hc_pre_step, A[0], A[1], hc.params(A[10] + 4, A[11], A[12], A[13]), 8, s, A[2], A[3], A[4], A[5], st)
+    # y_normed overlapping X, pre overlapping post
+    _expect(hc.HC_ERR_ALIAS, hc.hc_pre_step, A[0], A[1], _p(), 8, s, A[0] + 1024, A[3], A[4], A[5], st)
+    _expect(hc.HC_ERR_ALIAS, hc.hc_pre_step, A[0], A[1], _p(), 8, s, A[2], A[3], A[3] + 64, A[5], st)
+    # n == 0 is a no-op
+    hc.hc_pre_step(A[0], A[1], _p(), 0, s, A[2], A[3], A[4], A[5], st)
+
+
+def test_post_then_pre_validation(lib):
+    s = hc.shape()
+    st = 0
+    args = [A[0], A[1], A[2], A[3], A[4], _p(), 8, s, A[5], A[6], A[7], A[8], A[9], st]
+    for i in (0, 1, 2, 3, 4, 8, 9, 10, 11, 12):
+        bad = list(args)
+        bad[i] = None
+        _expect(hc.HC_ERR_NULL, hc.hc_post_then_pre, *bad)
+    bad = list(args)
+    bad[8] = A[1] + 4096  # X_out inside X
+    _expect(hc.HC_ERR_ALIAS, hc.hc_post_then_pre, *bad)
+    bad = list(args)
+    bad[8] = A[1]  # exactly in place is not allowed for the fused call
+    _expect(hc.HC_ERR_ALIAS, hc.hc_post_then_pre, *bad)
+    bad = list(args)
+    bad[9] = A[0]  # y_normed on delta
+    _expect(hc.HC_ERR_ALIAS, hc.hc_post_then_pre, *bad)
+    bad = list(args)
+    bad[2] = A[2] + 12
+    _expect(hc.HC_ERR_ALIGN, hc.hc_post_then_pre, *bad)
+    bad = list(args)
+    bad[6] = 1 << 31
+    _expect(hc.HC_ERR_SHAPE, hc.hc_post_then_pre, *bad)
+    bad = list(args)
+    bad[6] = 0
+    hc.hc_post_then_pre(*bad)
+
+
+def test_post_validation(lib):
+    s = hc.shape(d=24)  # hc_post only needs d % 8 == 0
+    _expect(hc.HC_ERR_SHAPE, hc.hc_post, A[0], A[1], A[2], A[3], 4, hc.shape(d=20), A[4], 0)
+    _expect(hc.HC_ERR_ALIAS, hc.hc_post, A[0], A[1], A[2], A[3], 4, s, A[1] + 16, 0)
+    _expect(hc.HC_ERR_ALIAS, hc.hc_post, A[0], A[1], A[2], A[3], 4, s, A[0], 0)
+    hc.hc_post(A[0], A[1], A[2], A[3], 0, s, A[1], 0)  # exactly in place is allowed; n == 0 no-op
+
+
+def test_plan_tiles(lib):
+    for clusters in (1, 7, 16, 18, 19):
+        for n in [1, 2, 31, 32, 33, 64, 100, 127, 128, 129, 255, 256, 1000, 4096, 16384, 16385, 65536, 100003]:
+            tm, nt = hc.hc_plan_tiles(n, clusters)
+            assert 1 <= tm <= 128
+            assert nt * tm >= n and (nt - 1) * tm < n
+            if nt > 1:
+                assert tm % 32 == 0
+    # the prefill batch spreads evenly enough: waves * tile within 10% of the ideal per-cluster share
+    tm, nt = hc.hc_plan_tiles(16384, 19)
+    waves = -(-nt // 19)
+    assert waves * tm <= 1.1 * 16384 / 19
+    # decode batches use small tiles so that many clusters work
+    tm, nt = hc.hc_plan_tiles(256, 19)
+    assert tm == 32 and nt == 8
+    assert hc.hc_plan_tiles(0, 19) == (128, 0)

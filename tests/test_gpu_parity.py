@@ -1,0 +1,340 @@
+"""CUDA path against the CPU oracle, element by element, through the C ABI.
+
+Small cases run every output of every token through the oracle; they span several tiles and a
+ragged last tile (n = 1, 3, 127, 129, 300) and several stream widths (d = 256 ... 5120). The
+full-size workloads are checked on sampled tokens (tokens are independent, so a sample is exact)
+and the chained workloads step by step, teacher-forced: each step's oracle takes the GPU's own
+inputs for that step. Tolerances are defined in gpu_util.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import hyper_connection_residual_hc_gb300 as hc
+import oracle as orc
+from hyper_connection_residual_hc_gb300 import synth
+from hyper_connection_residual_hc_gb300.synth import T_COMB, T_DELTA, T_POST, T_PREMIX, T_X
+
+import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    hc.load()
+    gu.device_error_clear()
+    yield
+    gu.device_error_clear()
+
+
+def _inputs(w, step=0, lo=0, hi=None):
+    hi = w.n if hi is None else hi
+    return dict(X=synth.tokens(w, T_X, step, lo, hi), delta=synth.tokens(w, T_DELTA, step, lo, hi),
+                post=synth.tokens(w, T_POST, step, lo, hi), comb=synth.tokens(w, T_COMB, step, lo, hi),
+                pre_mix=synth.tokens(w, T_PREMIX, step, lo, hi))
+
+
+def _shape(w):
+    return hc.shape(d=w.d, sinkhorn_iters=w.iters, hc_eps=w.hc_eps, norm_eps=w.norm_eps)
+
+
+# ---- pieces ----------------------------------------------------------------------------------------
+
+def test_prepare_params_split_is_exact():
+    w = synth.WORKLOADS["prefill_b4_t4096"]
+    prm = synth.params(w, 0)
+    P = gu.DevParams(prm, w.d)
+    planes = gu.host_u16(P.planes).reshape(72, 4 * w.d)
+    vals = orc.bf16_to_double(planes)
+    rec = np.zeros((24, 4 * w.d))
+    for h in range(2):
+        for p in range(3):
+            rec[12 * h:12 * h + 12] += vals[36 * h + 12 * p:36 * h + 12 * p + 12]
+    assert np.array_equal(rec, prm["hc_fn"].astype(np.float64))
+    # the hi plane is the nearest bf16 of each weight
+    hi = np.concatenate([planes[0:12], planes[36:48]])
+    assert np.array_equal(hi, orc.double_to_bf16(prm["hc_fn"].astype(np.float64)))
+
+
+@pytest.mark.parametrize("n,d", [(1, 5120), (3, 5120), (127, 5120), (300, 5120), (129, 1024), (40, 256)])
+def test_debug_mixes_match_oracle(n, d):
+    w = synth.small("step_b1_t64", 1, n, d, seed=100 + n)
+    x = synth.tokens(w, T_X, 0)
+    prm = synth.params(w, 0)
+    P = gu.DevParams(prm, d)
+    s = _shape(w)
+    m_gpu = gu.host_f32(gu.debug_mixes(gu.dev_bf16(x), P, s, n))
+    m_ref, r_ref, S = orc.hc_mixes(x, prm["hc_fn"], w.norm_eps)
+    worst = gu.assert_mixes_close(m_gpu, m_ref, S)
+    print("n=%d d=%d worst |err|/(uS) = %.3f" % (n, d, worst))
+    gu.device_error_clear()
+
+
+@pytest.mark.parametrize("n,d", [(1, 5120), (3, 5120), (127, 5120), (300, 5120), (129, 512), (33, 256)])
+def test_pre_step_matches_oracle(n, d):
+    w = synth.small("step_b1_t64", 1, n, d, seed=200 + n)
+    inp = _inputs(w)
+    prm = synth.params(w, 0)
+    P = gu.DevParams(prm, d)
+    s = _shape(w)
+    X = gu.dev_bf16(inp["X"])
+    out = gu.run_pre_step(X, gu.dev_f32(inp["pre_mix"]), P, s, n)
+    m_gpu = gu.host_f32(gu.debug_mixes(X, P, s, n))
+    ref = orc.hc_pre_step(inp["X"], inp["pre_mix"], prm["hc_fn"], prm["hc_scale"], prm["hc_base"], prm["norm_w"],
+                          w.iters, w.hc_eps, w.norm_eps)
+    exact = gu.assert_bf16_close(gu.host_u16(out["y_normed"]), ref["y_normed"], "y_normed")
+    gu.check_step(out, ref, m_gpu, ref["mixes"], ref["S"], prm, w.iters, w.hc_eps, "pre_step")
+    print("n=%d d=%d y_normed bit-exact %.5f" % (n, d, exact))
+    gu.device_error_clear()
+
+
+@pytest.mark.parametrize("n,d", [(1, 5120), (3, 5120), (127, 5120), (300, 5120), (129, 1024), (65, 256)])
+def test_post_then_pre_matches_oracle(n, d):
+    w = synth.small("step_b1_t64", 1, n, d, seed=300 + n)
+    inp = _inputs(w)
+    prm = synth.params(w, 0)
+    P = gu.DevParams(prm, d)
+    s = _shape(w)
+    out = gu.run_post_then_pre(gu.dev_bf16(inp["delta"]), gu.dev_bf16(inp["X"]), gu.dev_f32(inp["post"]),
+                               gu.dev_f32(inp["comb"]), gu.dev_f32(inp["pre_mix"]), P, s, n)
+    xo = gu.host_u16(out["X_out"])
+    xo_ref = orc.hc_post(inp["X"], inp["delta"], inp["post"], inp["comb"])
+    ex_x = gu.assert_bf16_close(xo, xo_ref, "X_out")
+    # reading half teacher-forced on the GPU's X'
+    ref = orc.hc_pre_step(xo, inp["pre_mix"], prm["hc_fn"], prm["hc_scale"], prm["hc_base"], prm["norm_w"],
+                          w.iters, w.hc_eps, w.norm_eps)
+    ex_y = gu.assert_bf16_close(gu.host_u16(out["y_normed"]), ref["y_normed"], "y_normed")
+    m_gpu = gu.host_f32(gu.debug_mixes(out["X_out"], P, s, n))
+    gu.check_step(out, ref, m_gpu, ref["mixes"], ref["S"], prm, w.iters, w.hc_eps, "post_then_pre")
+    # and free running: the oracle's own X' all the way (reported; bf16 ties may differ by 1 ulp)
+    free = orc.hc_post_then_pre(inp["delta"], inp["X"], inp["post"], inp["comb"], inp["pre_mix"], prm["hc_fn"],
+                                prm["hc_scale"], prm["hc_base"], prm["norm_w"], w.iters, w.hc_eps, w.norm_eps)
+    dd = gu.ulp_diff(gu.host_u16(out["y_normed"]), free["y_normed"])
+    print("n=%d d=%d X' bit-exact %.5f, y_normed bit-exact %.5f, free-running y_normed max ulp %d"
+          % (n, d, ex_x, ex_y, int(dd.max())))
+    gu.device_error_clear()
+
+
+@pytest.mark.parametrize("n,d", [(1, 5120), (5, 24), (300, 5120), (77, 1024)])
+def test_hc_post_matches_oracle(n, d):
+    w = synth.small("step_b1_t64", 1, n, d, seed=400 + n)
+    inp = _inputs(w)
+    s = hc.shape(d=d)
+    X = gu.dev_bf16(inp["X"])
+    out = torch.empty_like(X)
+    hc.hc_post(gu.dev_bf16(inp["delta"]), X, gu.dev_f32(inp["post"]), gu.dev_f32(inp["comb"]), n, s, out)
+    ref = orc.hc_post(inp["X"], inp["delta"], inp["post"], inp["comb"])
+    gu.assert_bf16_close(gu.host_u16(out), ref, "hc_post")
+    # in place gives the same bits
+    hc.hc_post(gu.dev_bf16(inp["delta"]), X, gu.dev_f32(inp["post"]), gu.dev_f32(inp["comb"]), n, s, X)
+    assert np.array_equal(gu.host_u16(X), gu.host_u16(out))
+
+
+# ---- special cases with closed forms ------------------------------------------------------------
+
+def test_identity_comb_returns_streams_bit_exact():
+    n, d = 130, 5120
+    w = synth.small("step_b1_t64", 1, n, d, seed=7)
+    inp = _inputs(w)
+    prm = synth.params(w, 0)
+    P = gu.DevParams(prm, d)
+    post = np.zeros((n, 4), np.float32)
+    comb = np.tile(np.eye(4, dtype=np.float32), (n, 1, 1))
+    out = gu.run_post_then_pre(gu.dev_bf16(inp["delta"]), gu.dev_bf16(inp["X"]), gu.dev_f32(post), gu.dev_f32(comb),
+                               gu.dev_f32(inp["pre_mix"]), P, _shape(w), n)
+    assert np.array_equal(gu.host_u16(out["X_out"]), inp["X"])
+
+
+def test_uniform_logits_closed_form_on_gpu():
+    """hc_fn = 0 and base = 0 give mixes = 0: pre = 1/2 + eps, post = 1, comb = the scalar recurrence
+    v <- v / (4 v + eps) from 1/4 + eps (one column step, then a row and a column step per round)."""
+    n, d = 70, 5120
+    w = synth.small("step_b1_t64", 1, n, d, seed=8)
+    inp = _inputs(w)
+    prm = synth.params(w, 0)
+    prm["hc_fn"][:] = 0
+    prm["hc_base"][:] = 0
+    P = gu.DevParams(prm, d)
+    for iters, eps in [(20, 1e-6), (50, 1e-6), (3, 0.25)]:
+        s = hc.shape(d=d, sinkhorn_iters=iters, hc_eps=eps)
+        out = gu.run_pre_step(gu.dev_bf16(inp["X"]), gu.dev_f32(inp["pre_mix"]), P, s, n)
+        v = 0.25 + eps
+        v = v / (4 * v + eps)
+        for _ in range(iters - 1):
+            v = v / (4 * v + eps)
+            v = v / (4 * v + eps)
+        assert np.allclose(gu.host_f32(out["pre"]), 0.5 + np.float32(eps), rtol=1e-6)
+        assert np.array_equal(gu.host_f32(out["post"]), np.ones((n, 4)))
+        assert np.allclose(gu.host_f32(out["comb"]), v, rtol=1e-5), (gu.host_f32(out["comb"])[0, 0, 0], v)
+
+
+def test_one_hot_pre_mix_reads_one_stream():
+    n, d = 64, 5120
+    w = synth.small("step_b1_t64", 1, n, d, seed=9)
+    inp = _inputs(w)
+    prm = synth.params(w, 0)
+    P = gu.DevParams(prm, d)
+    for j in range(4):
+        pm = np.zeros((n, 4), np.float32)
+        pm[:, j] = 1.0
+        out = gu.run_pre_step(gu.dev_bf16(inp["X"]), gu.dev_f32(pm), P, _shape(w), n)
+        want, _ = orc.rmsnorm(inp["X"][:, j], prm["norm_w"], w.norm_eps)
+        gu.assert_bf16_close(gu.host_u16(out["y_normed"]), want, "one-hot y_normed stream %d" % j)
+
+
+def test_model_norm_eps_1e20():
+    """The model's own norm_eps (1e-20) instead of the workloads' 1e-6."""
+    n, d = 129, 5120
+    w = synth.small("step_b1_t64", 1, n, d, seed=10, norm_eps=1e-20)
+    inp = _inputs(w)
+    prm = synth.params(w, 0)
+    P = gu.DevParams(prm, d)
+    s = _shape(w)
+    X = gu.dev_bf16(inp["X"])
+    out = gu.run_pre_step(X, gu.dev_f32(inp["pre_mix"]), P, s, n)
+    ref = orc.hc_pre_step(inp["X"], inp["pre_mix"], prm["hc_fn"], prm["hc_scale"], prm["hc_base"], prm["norm_w"],
+                          w.iters, w.hc_eps, w.norm_eps)
+    gu.assert_bf16_close(gu.host_u16(out["y_normed"]), ref["y_normed"], "y_normed")
+    gu.check_step(out, ref, gu.host_f32(gu.debug_mixes(X, P, s, n)), ref["mixes"], ref["S"], prm, w.iters, w.hc_eps,
+                  "eps1e-20")
+
+
+def test_zero_tokens_is_a_noop():
+    d = 5120
+    w = synth.small("step_b1_t64", 1, 4, d, seed=11)
+    P = gu.DevParams(synth.params(w, 0), d)
+    o = gu.alloc_outputs(4, d, True)
+    o["y_normed"].fill_(3.0)
+    X = torch.zeros((4, 4, d), dtype=torch.bfloat16, device="cuda")
+    hc.hc_pre_step(X, o["pre"], P.c, 0, hc.shape(), o["y_normed"], o["X_out"], o["post"], o["comb"])
+    torch.cuda.synchronize()
+    assert bool((o["y_normed"] == 3.0).all())
+
+
+# ---- the five workloads ------------------------------------------------------------------------------
+
+def _sample(n, k, rng, tile=128):
+    idx = set(range(min(n, 8))) | set(range(max(0, n - 8), n))
+    for b in range(0, n, tile * 16):
+        idx.update([b, min(n - 1, b + tile - 1), min(n - 1, b + tile)])
+    idx.update(rng.choice(n, size=min(k, n), replace=False).tolist())
+    return np.array(sorted(idx), dtype=np.int64)
+
+
+def _check_sampled(w, step, dev_in, out, prm, idx, post_mode, label):
+    """Oracle on the sampled tokens of one step, fed that step's device inputs (teacher-forced)."""
+    X = gu.host_u16(dev_in["X"][idx])
+    pm = gu.host_f32(dev_in["pre_mix"][idx]).astype(np.float32)
+    if post_mode:
+        delta = gu.host_u16(dev_in["delta"][idx])
+        post = gu.host_f32(dev_in["post"][idx]).astype(np.float32)
+        comb = gu.host_f32(dev_in["comb"][idx]).astype(np.float32)
+        xo = gu.host_u16(out["X_out"][idx])
+        gu.assert_bf16_close(xo, orc.hc_post(X, delta, post, comb), label + " X_out")
+        X = xo
+    ref = orc.hc_pre_step(X, pm, prm["hc_fn"], prm["hc_scale"], prm["hc_base"], prm["norm_w"], w.iters, w.hc_eps,
+                          w.norm_eps)
+    gu.assert_bf16_close(gu.host_u16(out["y_normed"][idx]), ref["y_normed"], label + " y_normed")
+    sub = {k: out[k][idx] for k in ("pre", "post", "comb")}
+    P = gu.DevParams(prm, w.d)
+    m_gpu = gu.host_f32(gu.debug_mixes(gu.dev_bf16(X), P, _shape(w), len(idx)))
+    gu.check_step(sub, ref, m_gpu, ref["mixes"], ref["S"], prm, w.iters, w.hc_eps, label)
+
+
+def test_workload_step_b1_t64():
+    w = synth.WORKLOADS["step_b1_t64"]
+    inp = _inputs(w)
+    prm = synth.params(w, 0)
+    P = gu.DevParams(prm, w.d)
+    dev = {k: (gu.dev_bf16(v) if v.dtype == np.uint16 else gu.dev_f32(v)) for k, v in inp.items()}
+    out = gu.run_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, _shape(w), w.n)
+    _check_sampled(w, 0, dev, out, prm, np.arange(w.n), True, "step_b1_t64")
+    gu.device_error_clear()
+
+
+def test_workload_prefill_b4_t4096():
+    w = synth.WORKLOADS["prefill_b4_t4096"]
+    inp = _inputs(w)
+    prm = synth.params(w, 0)
+    P = gu.DevParams(prm, w.d)
+    dev = {k: (gu.dev_bf16(v) if v.dtype == np.uint16 else gu.dev_f32(v)) for k, v in inp.items()}
+    out = gu.run_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, _shape(w), w.n)
+    idx = _sample(w.n, 384, np.random.default_rng(0))
+    _check_sampled(w, 0, dev, out, prm, idx, True, "prefill_b4_t4096")
+    # properties on every token: X_out differs from X, y_normed finite, comb columns sum to 1
+    comb = out["comb"]
+    assert torch.isfinite(out["y_normed"].float()).all()
+    assert float((comb.sum(dim=1) - 1).abs().max()) < 1e-4
+    pre = out["pre"]
+    assert float(pre.min()) >= 1e-6 * 0.999 and float(pre.max()) <= 1 + 2e-6
+    gu.device_error_clear()
+
+
+def _run_chain(w, sample_k, first_pre_step, fresh_delta):
+    """Steps: [hc_pre_step], then hc_post_then_pre ... ; every step checked teacher-forced on a sample."""
+    rng = np.random.default_rng(w.seed)
+    s = _shape(w)
+    n = w.n
+    X = gu.dev_bf16(synth.tokens(w, T_X, 0))
+    pre_mix = gu.dev_f32(synth.tokens(w, T_PREMIX, 0))
+    steps = w.steps
+    worst = 0
+    if first_pre_step:
+        prm = synth.params(w, 0)
+        P = gu.DevParams(prm, w.d)
+        out = gu.run_pre_step(X, pre_mix, P, s, n)
+        idx = _sample(n, sample_k, rng)
+        _check_sampled(w, 0, dict(X=X, pre_mix=pre_mix), out, prm, idx, False, "%s step 0" % w.name)
+        state = dict(X=X, post=out["post"], comb=out["comb"], pre_mix=out["pre"], y=out["y_normed"])
+        start = 1
+        wd = prm["w_diag"]
+    else:
+        state = dict(X=X, post=gu.dev_f32(synth.tokens(w, T_POST, 0)), comb=gu.dev_f32(synth.tokens(w, T_COMB, 0)),
+                     pre_mix=pre_mix, y=None)
+        start = 0
+        wd = None
+    for l in range(start, steps):
+        if fresh_delta:
+            delta = gu.dev_bf16(synth.tokens(w, T_DELTA, l))
+        else:
+            delta = (state["y"].float() * gu.dev_f32(wd)).to(torch.bfloat16)  # stand-in sublayer
+        prm = synth.params(w, l)
+        P = gu.DevParams(prm, w.d)
+        out = gu.run_post_then_pre(delta, state["X"], state["post"], state["comb"], state["pre_mix"], P, s, n)
+        idx = _sample(n, sample_k, rng)
+        dev_in = dict(X=state["X"], delta=delta, post=state["post"], comb=state["comb"], pre_mix=state["pre_mix"])
+        _check_sampled(w, l, dev_in, out, prm, idx, True, "%s step %d" % (w.name, l))
+        state = dict(X=out["X_out"], post=out["post"], comb=out["comb"], pre_mix=out["pre"], y=out["y_normed"])
+        wd = prm["w_diag"]
+        worst = max(worst, float(state["X"].float().abs().max()))
+    gu.device_error_clear()
+    return state, worst
+
+
+def test_workload_decode_chain_b256_80steps():
+    w = synth.WORKLOADS["decode_chain_b256_80steps"]
+    state, worst = _run_chain(w, 256, first_pre_step=True, fresh_delta=False)
+    # the chain's tail: the last writing half alone
+    delta = gu.dev_bf16(synth.tokens(w, T_DELTA, w.steps))
+    Xf = torch.empty_like(state["X"])
+    hc.hc_post(delta, state["X"], state["post"], state["comb"], w.n, _shape(w), Xf)
+    ref = orc.hc_post(gu.host_u16(state["X"]), gu.host_u16(delta), gu.host_f32(state["post"]).astype(np.float32),
+                      gu.host_f32(state["comb"]).astype(np.float32))
+    gu.assert_bf16_close(gu.host_u16(Xf), ref, "decode chain tail")
+    print("decode chain: max |X| after 80 steps %.3g" % worst)
+
+
+@pytest.mark.slow
+def test_workload_long_prefill_b1_t65536_4steps():
+    w = synth.WORKLOADS["long_prefill_b1_t65536_4steps"]
+    _run_chain(w, 256, first_pre_step=False, fresh_delta=True)
+
+
+@pytest.mark.slow
+def test_workload_stress_b2_t8192_80steps():
+    w = synth.WORKLOADS["stress_b2_t8192_80steps"]
+    _run_chain(w, 48, first_pre_step=True, fresh_delta=True)
