@@ -56,7 +56,8 @@ def _declare(lib):
     lib.oracle_hc_post.argtypes = [_I64, _I, _I, _P, _P, _P, _P, _P, _I]
     lib.oracle_hc_mixes.argtypes = [_I64, _I, _I, _P, _P, _D, _P, _P, _P, _I]
     lib.oracle_split_sinkhorn.argtypes = [_I64, _I, _P, _P, _P, _I, _D, _P, _P, _P, _I]
-    lib.oracle_hc_pre.argtypes = [_I64, _I, _I, _P, _P, _P, _P, _I]
+    lib.oracle_hc_pre.argtypes = [_I64, _I, _I, _P, _P, _P, _P, _P, _I]
+    lib.oracle_hc_post_detail.argtypes = [_I64, _I, _I, _P, _P, _P, _P, _P, _P, _P, _I]
     lib.oracle_rmsnorm.argtypes = [_I64, _I, _P, _P, _D, _P, _P, _I]
     lib.oracle_hc_pre_step.argtypes = [_I64, _I, _I, _P, _P, _P, _P, _P, _P, _I, _D, _D,
                                        _P, _P, _P, _P, _P, _P, _P, _P, _I]
@@ -148,16 +149,30 @@ def split_sinkhorn(mixes, hc_scale, hc_base, hc, iters, eps, threads=0, lib=None
     return pre, post, comb
 
 
-def hc_pre(X, pre_mix, threads=0, lib=None):
-    """Returns (y bf16 bits [n,d], y before rounding float64 [n,d])."""
+def hc_post_detail(X, delta, post, comb, threads=0, lib=None):
+    """hc_post plus, per element, the value before rounding and the sum of |terms| (float64)."""
+    lib = lib or load()
+    X = _c(X, np.uint16)
+    n, hc, d = X.shape
+    delta, post, comb = _c(delta, np.uint16), _c(post, np.float32), _c(comb, np.float32)
+    out = np.empty_like(X)
+    exact = np.empty(X.shape, np.float64)
+    mag = np.empty(X.shape, np.float64)
+    lib.oracle_hc_post_detail(n, hc, d, _p(X), _p(delta), _p(post), _p(comb), _p(out), _p(exact), _p(mag), threads)
+    return out, exact, mag
+
+
+def hc_pre(X, pre_mix, threads=0, lib=None, with_abssum=False):
+    """Returns (y bf16 bits [n,d], y before rounding float64 [n,d][, sum of |terms| [n,d]])."""
     lib = lib or load()
     X = _c(X, np.uint16)
     n, hc, d = X.shape
     pre_mix = _c(pre_mix, np.float32)
     y = np.empty((n, d), np.uint16)
     ye = np.empty((n, d), np.float64)
-    lib.oracle_hc_pre(n, hc, d, _p(X), _p(pre_mix), _p(y), _p(ye), threads)
-    return y, ye
+    ya = np.empty((n, d), np.float64)
+    lib.oracle_hc_pre(n, hc, d, _p(X), _p(pre_mix), _p(y), _p(ye), _p(ya), threads)
+    return (y, ye, ya) if with_abssum else (y, ye)
 
 
 def rmsnorm(x, w, eps, threads=0, lib=None):

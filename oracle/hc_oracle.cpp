@@ -99,14 +99,22 @@ void parallel_for(int64_t n, int threads, F&& body) {
 // [WS] formula X'_{n,k} = u_k * Delta + sum_j C_jk X_{n,j}; [SL] hc_post excerpt: the sum runs over
 // the comb index that multiplies the residual's stream (dim 2 of comb), the result is cast to the
 // stream dtype.
+// Optionally also returns the value before rounding and the sum of the terms' magnitudes (the
+// scale of any fp32 evaluation's rounding error, used by tolerances).
 void post_token(int hc, int d, const uint16_t* X, const uint16_t* delta, const float* post,
-                const float* comb, uint16_t* X_out) {
+                const float* comb, uint16_t* X_out, double* exact, double* abssum) {
     for (int k = 0; k < hc; ++k) {
         for (int i = 0; i < d; ++i) {
             double acc = static_cast<double>(post[k]) * bf16_to_double(delta[i]);
-            for (int j = 0; j < hc; ++j)
-                acc += static_cast<double>(comb[j * hc + k]) * bf16_to_double(X[j * d + i]);
+            double mag = std::fabs(acc);
+            for (int j = 0; j < hc; ++j) {
+                double term = static_cast<double>(comb[j * hc + k]) * bf16_to_double(X[j * d + i]);
+                acc += term;
+                mag += std::fabs(term);
+            }
             X_out[k * d + i] = double_to_bf16(acc);
+            if (exact) exact[k * d + i] = acc;
+            if (abssum) abssum[k * d + i] = mag;
         }
     }
 }
@@ -192,11 +200,17 @@ void split_token(int hc, const double* m, const float* hc_scale, const float* hc
 }
 
 // [SL] hc_pre excerpt: y = sum_j pre_mix_j * X_j in float, cast back to the stream dtype.
-void pre_token(int hc, int d, const uint16_t* X, const float* pre_mix, uint16_t* y, double* y_exact) {
+void pre_token(int hc, int d, const uint16_t* X, const float* pre_mix, uint16_t* y, double* y_exact,
+               double* y_abssum) {
     for (int i = 0; i < d; ++i) {
-        double acc = 0.0;
-        for (int j = 0; j < hc; ++j) acc += static_cast<double>(pre_mix[j]) * bf16_to_double(X[j * d + i]);
+        double acc = 0.0, mag = 0.0;
+        for (int j = 0; j < hc; ++j) {
+            double term = static_cast<double>(pre_mix[j]) * bf16_to_double(X[j * d + i]);
+            acc += term;
+            mag += std::fabs(term);
+        }
         if (y_exact) y_exact[i] = acc;
+        if (y_abssum) y_abssum[i] = mag;
         y[i] = double_to_bf16(acc);
     }
 }
@@ -231,7 +245,16 @@ void oracle_round_bf16(int64_t count, const double* x, uint16_t* out) {
 void oracle_hc_post(int64_t n, int hc, int d, const uint16_t* X, const uint16_t* delta, const float* post,
                     const float* comb, uint16_t* X_out, int threads) {
     parallel_for(n, threads, [&](int64_t t) {
-        post_token(hc, d, X + t * hc * d, delta + t * d, post + t * hc, comb + t * hc * hc, X_out + t * hc * d);
+        post_token(hc, d, X + t * hc * d, delta + t * d, post + t * hc, comb + t * hc * hc, X_out + t * hc * d,
+                   nullptr, nullptr);
+    });
+}
+
+void oracle_hc_post_detail(int64_t n, int hc, int d, const uint16_t* X, const uint16_t* delta, const float* post,
+                           const float* comb, uint16_t* X_out, double* exact, double* abssum, int threads) {
+    parallel_for(n, threads, [&](int64_t t) {
+        post_token(hc, d, X + t * hc * d, delta + t * d, post + t * hc, comb + t * hc * hc, X_out + t * hc * d,
+                   exact + t * hc * d, abssum + t * hc * d);
     });
 }
 
@@ -254,9 +277,10 @@ void oracle_split_sinkhorn(int64_t n, int hc, const double* mixes, const float* 
 }
 
 void oracle_hc_pre(int64_t n, int hc, int d, const uint16_t* X, const float* pre_mix, uint16_t* y,
-                   double* y_exact, int threads) {
+                   double* y_exact, double* y_abssum, int threads) {
     parallel_for(n, threads, [&](int64_t t) {
-        pre_token(hc, d, X + t * hc * d, pre_mix + t * hc, y + t * d, y_exact ? y_exact + t * d : nullptr);
+        pre_token(hc, d, X + t * hc * d, pre_mix + t * hc, y + t * d, y_exact ? y_exact + t * d : nullptr,
+                  y_abssum ? y_abssum + t * d : nullptr);
     });
 }
 
@@ -286,7 +310,7 @@ void oracle_hc_pre_step(int64_t n, int hc, int d, const uint16_t* X, const float
         split_token(hc, m.data(), hc_scale, hc_base, iters, hc_eps, pre + t * hc, post + t * hc,
                     comb + t * hc * hc);
         std::vector<uint16_t> y(d);
-        pre_token(hc, d, Xt, pre_mix + t * hc, y.data(), nullptr);
+        pre_token(hc, d, Xt, pre_mix + t * hc, y.data(), nullptr, nullptr);
         rmsnorm_token(d, y.data(), norm_w, norm_eps, y_normed + t * d, nullptr);
         if (mixes_out) std::copy(m.begin(), m.end(), mixes_out + t * M);
         if (S_out) std::copy(S.begin(), S.end(), S_out + t * M);

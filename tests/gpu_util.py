@@ -2,8 +2,14 @@
 the oracle and the tolerances they use.
 
 Tolerances (stated once, used everywhere):
-  bf16 outputs (X', y_normed): at most 1 bf16 ulp from the oracle given the same inputs. The GPU
-    rounds an fp32 value, the oracle an exact one; they differ only near rounding ties.
+  bf16 outputs (X', y_normed): 1 bf16 ulp after fp32 accumulation. The model evaluates hc_post and
+    hc_pre on float32 tensors and then casts; an fp32 evaluation of a k-term sum is off from the exact
+    value by at most k u A (A = sum of |terms|, u = 2^-24). So X' must lie within 1 bf16 ulp of an
+    fp32 evaluation: |gpu - exact| <= ulp_bf16(exact) + 6 u A. Away from cancellation this is the
+    plain "at most 1 ulp from the oracle's rounded value"; only where the terms nearly cancel does the
+    fp32 bound (several ulps of the tiny result) take over. y_normed likewise, with y's admissible
+    bf16 values pushed through the norm. Both checks also report the plain ulp histogram and require
+    99.9% of the values within 1 ulp of the oracle's rounding.
   mixes: |gpu - oracle| <= max(1e-5 |m|, 1e-6) + 2 u S, with u = 2^-24 and S = r sum_c |x_c w_mc|:
     a 20,480-term dot product accumulated in fp32 is off by a few u S whatever the order.
   pre/post/comb given the GPU's own mixes (stage isolated): rel 1e-5 or abs 1e-6.
@@ -108,6 +114,48 @@ def assert_bf16_close(gpu_u16, ref_u16, what, max_ulp=1):
     worst = int(dd.max()) if dd.size else 0
     assert worst <= max_ulp, "%s: %d values beyond %d ulp (worst %d ulp)" % (what, int((dd > max_ulp).sum()), max_ulp, worst)
     return float((dd == 0).mean()) if dd.size else 1.0
+
+
+def bf16_spacing(v):
+    """Distance between consecutive bf16 values around |v| (float64 array)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -133)))
+    return np.where(a < 2.0 ** -126, 2.0 ** -133, 2.0 ** (e - 7))
+
+
+def check_xprime(gpu_u16, X, delta, post, comb, what="X_out"):
+    """hc_post output against the oracle: within 1 bf16 ulp of an fp32 evaluation."""
+    ref, exact, mag = orc.hc_post_detail(X, delta, post, comb)
+    g = orc.bf16_to_double(gpu_u16)
+    tol = bf16_spacing(exact) + 6 * U * mag
+    bad = np.abs(g - exact) > tol
+    assert not bad.any(), "%s: %d values beyond 1 ulp + fp32 bound" % (what, int(bad.sum()))
+    dd = ulp_diff(np.asarray(gpu_u16), ref)
+    assert (dd <= 1).mean() >= 0.999, "%s: only %.5f within 1 ulp" % (what, float((dd <= 1).mean()))
+    return float((dd == 0).mean()), int(dd.max())
+
+
+def check_y_normed(gpu_u16, Xp, pre_mix, norm_w, norm_eps, what="y_normed"):
+    """y_normed against the oracle fed the same X': y may be any bf16 value an fp32 evaluation of
+    sum_j pre_mix_j X'_j can round to; the norm of each must be within 1 bf16 ulp."""
+    y_ref, y_exact, y_abs = orc.hc_pre(Xp, pre_mix, with_abssum=True)
+    yn_ref, _ = orc.rmsnorm(y_ref, norm_w, norm_eps)
+    yr = orc.bf16_to_double(y_ref)
+    r = 1.0 / np.sqrt((yr ** 2).mean(axis=1, keepdims=True) + norm_eps)
+    Ey = 5 * U * y_abs
+    y_lo = orc.bf16_to_double(orc.double_to_bf16(y_exact - Ey))
+    y_hi = orc.bf16_to_double(orc.double_to_bf16(y_exact + Ey))
+    w = np.asarray(norm_w, dtype=np.float64)[None, :]
+    a, b = w * y_lo * r, w * y_hi * r
+    lo, hi = np.minimum(a, b), np.maximum(a, b)
+    lo = lo - bf16_spacing(lo) - 4 * U * np.abs(lo)
+    hi = hi + bf16_spacing(hi) + 4 * U * np.abs(hi)
+    g = orc.bf16_to_double(gpu_u16)
+    bad = (g < lo) | (g > hi)
+    assert not bad.any(), "%s: %d values outside the admissible range" % (what, int(bad.sum()))
+    dd = ulp_diff(np.asarray(gpu_u16), yn_ref)
+    assert (dd <= 1).mean() >= 0.999, "%s: only %.5f within 1 ulp" % (what, float((dd <= 1).mean()))
+    return float((dd == 0).mean()), int(dd.max())
 
 
 def mixes_tol(m_ref, S):

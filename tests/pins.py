@@ -313,6 +313,11 @@ def pin_hc_post_dyadic_closed_form(lib):
             0.125 * 0.75 + (0.125 * 1 + 0.0 * -0.5 + 0.25 * 0.25 + 0.5 * 2)]
     for k in range(hc):
         assert np.all(out[k] == want[k]), (k, out[k, 0], want[k])
+    # the detailed form returns the same bits, the exact values and the sums of |terms|
+    o2, exact, mag = orc.hc_post_detail(X, delta, post, comb, lib=lib)
+    assert np.array_equal(o2, orc.hc_post(X, delta, post, comb, lib=lib))
+    mag_want = np.abs(post[0, :, None] * 0.75) + np.abs(comb[0].astype(np.float64) * c[:, None]).sum(axis=0)[:, None]
+    assert np.allclose(exact[0], np.array(want)[:, None]) and np.allclose(mag[0], mag_want)
 
 
 # ---- hc_mixes -----------------------------------------------------------------------------------
@@ -403,9 +408,10 @@ def pin_hc_pre_dyadic(lib):
     c = np.array([1.0, -0.5, 0.25, 2.0])
     X = _bf(np.repeat(c[:, None], d, axis=1))[None]
     p = np.array([[0.5, 0.25, 0.125, 0.0625]], np.float32)
-    y, ye = orc.hc_pre(X, p, lib=lib)
+    y, ye, ya = orc.hc_pre(X, p, lib=lib, with_abssum=True)
     want = 0.5 * 1 + 0.25 * -0.5 + 0.125 * 0.25 + 0.0625 * 2
     assert np.all(ye == want) and np.all(orc.bf16_to_double(y) == want)
+    assert np.all(ya == 0.5 * 1 + 0.25 * 0.5 + 0.125 * 0.25 + 0.0625 * 2)
 
 
 def pin_rmsnorm_constant(lib):

@@ -15,8 +15,8 @@ import oracle
 import pins
 
 MUTANTS = {
-    "hc_post_comb_transposed": ("comb[j * hc + k]) * bf16_to_double(X[j * d + i])",
-                                "comb[k * hc + j]) * bf16_to_double(X[j * d + i])"),
+    "hc_post_comb_transposed": ("comb[j * hc + k]) * bf16_to_double(X[j * d + i]);",
+                                "comb[k * hc + j]) * bf16_to_double(X[j * d + i]);"),
     "hc_post_drops_delta": ("double acc = static_cast<double>(post[k]) * bf16_to_double(delta[i]);",
                             "double acc = 0.0;"),
     "hc_post_wrong_post_index": ("static_cast<double>(post[k]) * bf16_to_double(delta[i])",
@@ -47,15 +47,15 @@ MUTANTS = {
     "sinkhorn_one_iteration_short": ("for (int it = 0; it < iters - 1; ++it)", "for (int it = 0; it < iters - 2; ++it)"),
     "sinkhorn_colsum_eps_dropped": ("C[j * hc + k] = C[j * hc + k] / (cs[k] + eps);",
                                     "C[j * hc + k] = C[j * hc + k] / cs[k];"),
-    "hc_pre_wrong_weight": ("acc += static_cast<double>(pre_mix[j]) * bf16_to_double(X[j * d + i]);",
-                            "acc += static_cast<double>(pre_mix[0]) * bf16_to_double(X[j * d + i]);"),
+    "hc_pre_wrong_weight": ("double term = static_cast<double>(pre_mix[j]) * bf16_to_double(X[j * d + i]);",
+                            "double term = static_cast<double>(pre_mix[0]) * bf16_to_double(X[j * d + i]);"),
     "rmsnorm_no_eps": ("double r = 1.0 / std::sqrt(ss / d + eps);", "double r = 1.0 / std::sqrt(ss / d);"),
     "rmsnorm_no_weight": ("double v = static_cast<double>(w[i]) * (bf16_to_double(x[i]) * r);",
                           "double v = bf16_to_double(x[i]) * r;"),
     "round_ties_away": ("(frac == 0.5 && std::fmod(r, 2.0) != 0.0)", "(frac == 0.5)"),
     "round_truncates": ("if (frac > 0.5 || (frac == 0.5 && std::fmod(r, 2.0) != 0.0)) r += 1.0;", ""),
     "pre_step_norms_unrounded_y": ("rmsnorm_token(d, y.data(), norm_w, norm_eps, y_normed + t * d, nullptr);",
-                                   "{ std::vector<double> ye(d); pre_token(hc, d, Xt, pre_mix + t * hc, y.data(), ye.data());"
+                                   "{ std::vector<double> ye(d); pre_token(hc, d, Xt, pre_mix + t * hc, y.data(), ye.data(), nullptr);"
                                    " double ss = 0; for (int i = 0; i < d; ++i) ss += ye[i] * ye[i];"
                                    " double rr = 1.0 / std::sqrt(ss / d + norm_eps);"
                                    " for (int i = 0; i < d; ++i) y_normed[t * d + i] = double_to_bf16(norm_w[i] * (ye[i] * rr)); }"),
