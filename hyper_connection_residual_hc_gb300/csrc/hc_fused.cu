@@ -101,6 +101,15 @@ constexpr uint32_t kAccCol0 = 0, kAccCol1 = 96, kYCol = 192;  // y slice: up to 
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
+// L2 handling of the streamed tiles (X, Delta): cache-hint policy of the loads (0 evict_normal,
+// 1 evict_first, 2 evict_last) and the L2 promotion of their tensor maps.
+#ifndef HC_STREAM_POLICY
+#define HC_STREAM_POLICY 0
+#endif
+#ifndef HC_STREAM_PROMOTION
+#define HC_STREAM_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+#endif
+
 // device error word: bit set = which wait gave up
 __device__ unsigned int g_hc_error = 0;
 enum : unsigned int {
@@ -467,7 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= TMA producer =========================================================
         uint64_t pol_stream = 0, pol_keep = 0;
         if (lane == 0) {
-            pol_stream = policy_evict_first();
+            pol_stream = HC_STREAM_POLICY == 1 ? policy_evict_first()
+                         : HC_STREAM_POLICY == 2 ? policy_evict_last() : policy_evict_normal();
             pol_keep = policy_evict_last();
         }
         const uint32_t bytes = static_cast<uint32_t>(4 * p.tile_m * 64 + (kPost ? p.tile_m * 64 : 0) + 4 * kBTileBytes);
@@ -643,14 +653,15 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-            const uint32_t* box, CUtensorMapSwizzle sw) {
+            const uint32_t* box, CUtensorMapSwizzle sw,
+            CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_128B) {
     auto fn = get_encode();
     if (!fn) return false;
     uint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
                     reinterpret_cast<const cuuint64_t*>(dims), reinterpret_cast<const cuuint64_t*>(strides_bytes),
                     reinterpret_cast<const cuuint32_t*>(box), reinterpret_cast<const cuuint32_t*>(estr),
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, promo,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -756,14 +767,16 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
         const uint64_t dims[3] = {d, 4, n};
         const uint64_t str[2] = {d * 2, 4 * d * 2};
         const uint32_t box[3] = {kChunk, 1, static_cast<uint32_t>(tile_m)};
-        if (!encode(&tmX, a.X, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+        if (!encode(&tmX, a.X, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B, HC_STREAM_PROMOTION)) return -7;
         if (!encode(&tmXo, a.post_mode ? a.X_out : a.X, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
     }
     {
         const uint64_t dims[2] = {d, n};
         const uint64_t str[1] = {d * 2};
         const uint32_t box[2] = {kChunk, static_cast<uint32_t>(tile_m)};
-        if (!encode(&tmD, a.post_mode ? a.delta : a.X, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+        if (!encode(&tmD, a.post_mode ? a.delta : a.X, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B,
+                    HC_STREAM_PROMOTION))
+            return -7;
         const uint32_t boxy[2] = {16, 32};
         if (!encode(&tmY, a.y_normed ? a.y_normed : a.X, 2, dims, str, boxy, CU_TENSOR_MAP_SWIZZLE_32B)) return -7;
     }
