@@ -209,10 +209,11 @@ def run_ours(args):
                post=torch.empty((n, 4), dtype=torch.float32, device="cuda"),
                comb=torch.empty((n, 4, 4), dtype=torch.float32, device="cuda"))
     stream = torch.cuda.current_stream()
+    ws = hc.new_workspace()
 
     def step():
         hc.hc_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, n, s, out["X_out"],
-                            out["y_normed"], out["pre"], out["post"], out["comb"], stream)
+                            out["y_normed"], out["pre"], out["post"], out["comb"], ws, stream)
 
     def barrier():
         torch.cuda.synchronize()
@@ -280,8 +281,8 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     alg_bytes = n * BYTES_PER_TOKEN + PARAM_BYTES
     achieved = alg_bytes / (kern_ms / 1e3) / 1e9
-    clusters = hc.hc_fused_clusters()
-    tile_m, tiles = hc.hc_plan_tiles(n, clusters)
+    groups = hc.hc_fused_groups()
+    tile_m, tiles = hc.hc_plan_tiles(n, groups)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -303,7 +304,7 @@ def run_ours(args):
                        "sinkhorn_iters": w.iters, "hc_eps": w.hc_eps, "norm_eps": w.norm_eps,
                        "stream_dtype": "bf16", "coefficient_dtype": "f32",
                        "l2": "no flush: every step reads 839 MB of inputs and writes 839 MB, far above the 129 MB L2",
-                       "tile_tokens": tile_m, "tiles": tiles, "clusters_of_8": clusters,
+                       "tile_tokens": tile_m, "tiles": tiles, "groups_of_8_ctas": groups,
                        "hbm_gb_per_s": alg_bytes * args.steps / (el_ms / 1e3) / 1e9},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,

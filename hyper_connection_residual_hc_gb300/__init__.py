@@ -30,8 +30,8 @@ HC_ERR_DEVICE = -8
 
 # every symbol include/hc.h declares
 SYMBOLS = (
-    "hc_prepare_params_size", "hc_prepare_params", "hc_pre_step", "hc_post_then_pre", "hc_post",
-    "hc_debug_mixes", "hc_plan_tiles", "hc_fused_clusters", "hc_device_error", "hc_status_string",
+    "hc_prepare_params_size", "hc_prepare_params", "hc_workspace_size", "hc_pre_step", "hc_post_then_pre",
+    "hc_post", "hc_debug_mixes", "hc_plan_tiles", "hc_fused_groups", "hc_device_error", "hc_status_string",
 )
 
 
@@ -66,12 +66,13 @@ def load(path: str = LIB_PATH):
     P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     lib.hc_prepare_params_size.argtypes = [I, I, ctypes.POINTER(ctypes.c_size_t)]
     lib.hc_prepare_params.argtypes = [P, I, I, P, P]
-    lib.hc_pre_step.argtypes = [P, P, hc_params_t, I64, hc_shape_t, P, P, P, P, P]
-    lib.hc_post_then_pre.argtypes = [P, P, P, P, P, hc_params_t, I64, hc_shape_t, P, P, P, P, P, P]
+    lib.hc_workspace_size.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
+    lib.hc_pre_step.argtypes = [P, P, hc_params_t, I64, hc_shape_t, P, P, P, P, P, P]
+    lib.hc_post_then_pre.argtypes = [P, P, P, P, P, hc_params_t, I64, hc_shape_t, P, P, P, P, P, P, P]
     lib.hc_post.argtypes = [P, P, P, P, I64, hc_shape_t, P, P]
-    lib.hc_debug_mixes.argtypes = [P, hc_params_t, I64, hc_shape_t, P, P]
+    lib.hc_debug_mixes.argtypes = [P, hc_params_t, I64, hc_shape_t, P, P, P]
     lib.hc_plan_tiles.argtypes = [I64, I, ctypes.POINTER(I), ctypes.POINTER(I64)]
-    lib.hc_fused_clusters.argtypes = [ctypes.POINTER(I)]
+    lib.hc_fused_groups.argtypes = [ctypes.POINTER(I)]
     lib.hc_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), I, P]
     lib.hc_status_string.argtypes = [I]
     lib.hc_status_string.restype = ctypes.c_char_p
@@ -128,16 +129,29 @@ def hc_prepare_params(hc_fn, hc: int, d: int, planes, stream=None) -> None:
     _check("hc_prepare_params", load().hc_prepare_params(_ptr(hc_fn), hc, d, _ptr(planes), _stream(stream)))
 
 
-def hc_pre_step(X, pre_mix, p: hc_params_t, n: int, s: hc_shape_t, y_normed, pre, post, comb, stream=None) -> None:
+def hc_workspace_size() -> int:
+    out = ctypes.c_size_t(0)
+    _check("hc_workspace_size", load().hc_workspace_size(ctypes.byref(out)))
+    return out.value
+
+
+def new_workspace(device=None):
+    """A zero-filled device workspace for the fused calls (torch uint8 tensor)."""
+    import torch
+    return torch.zeros(hc_workspace_size(), dtype=torch.uint8, device=device or "cuda")
+
+
+def hc_pre_step(X, pre_mix, p: hc_params_t, n: int, s: hc_shape_t, y_normed, pre, post, comb, workspace,
+                stream=None) -> None:
     _check("hc_pre_step", load().hc_pre_step(_ptr(X), _ptr(pre_mix), p, n, s, _ptr(y_normed), _ptr(pre), _ptr(post),
-                                             _ptr(comb), _stream(stream)))
+                                             _ptr(comb), _ptr(workspace), _stream(stream)))
 
 
 def hc_post_then_pre(delta, X, post, comb, pre_mix, nxt: hc_params_t, n: int, s: hc_shape_t, X_out, y_normed,
-                     pre_out, post_out, comb_out, stream=None) -> None:
+                     pre_out, post_out, comb_out, workspace, stream=None) -> None:
     _check("hc_post_then_pre", load().hc_post_then_pre(
         _ptr(delta), _ptr(X), _ptr(post), _ptr(comb), _ptr(pre_mix), nxt, n, s, _ptr(X_out), _ptr(y_normed),
-        _ptr(pre_out), _ptr(post_out), _ptr(comb_out), _stream(stream)))
+        _ptr(pre_out), _ptr(post_out), _ptr(comb_out), _ptr(workspace), _stream(stream)))
 
 
 def hc_post(delta, X, post, comb, n: int, s: hc_shape_t, X_out, stream=None) -> None:
@@ -145,20 +159,20 @@ def hc_post(delta, X, post, comb, n: int, s: hc_shape_t, X_out, stream=None) -> 
                                      _stream(stream)))
 
 
-def hc_debug_mixes(X, p: hc_params_t, n: int, s: hc_shape_t, mixes, stream=None) -> None:
-    _check("hc_debug_mixes", load().hc_debug_mixes(_ptr(X), p, n, s, _ptr(mixes), _stream(stream)))
+def hc_debug_mixes(X, p: hc_params_t, n: int, s: hc_shape_t, mixes, workspace, stream=None) -> None:
+    _check("hc_debug_mixes", load().hc_debug_mixes(_ptr(X), p, n, s, _ptr(mixes), _ptr(workspace), _stream(stream)))
 
 
-def hc_plan_tiles(n: int, clusters: int):
+def hc_plan_tiles(n: int, groups: int):
     tm = ctypes.c_int(0)
     nt = ctypes.c_int64(0)
-    _check("hc_plan_tiles", load().hc_plan_tiles(n, clusters, ctypes.byref(tm), ctypes.byref(nt)))
+    _check("hc_plan_tiles", load().hc_plan_tiles(n, groups, ctypes.byref(tm), ctypes.byref(nt)))
     return tm.value, nt.value
 
 
-def hc_fused_clusters() -> int:
+def hc_fused_groups() -> int:
     c = ctypes.c_int(0)
-    _check("hc_fused_clusters", load().hc_fused_clusters(ctypes.byref(c)))
+    _check("hc_fused_groups", load().hc_fused_groups(ctypes.byref(c)))
     return c.value
 
 

@@ -137,6 +137,8 @@ int check_params(const hc_params_t& p) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? HC_OK : HC_ERR_CUDA; }
 
+int launch_status(int internal) { return internal == 0 ? HC_OK : internal == -3 ? HC_ERR_UNSUPPORTED : HC_ERR_CUDA; }
+
 }  // namespace
 }  // namespace hc
 
@@ -200,26 +202,32 @@ int hc_post(const void* delta, const void* X, const float* post, const float* co
     return cuda_status(cudaGetLastError());
 }
 
+int hc_workspace_size(size_t* bytes) {
+    if (!bytes) return HC_ERR_NULL;
+    *bytes = workspace_bytes();
+    return HC_OK;
+}
+
 int hc_pre_step(const void* X, const float* pre_mix, hc_params_t p, int64_t n, hc_shape_t s, void* y_normed,
-                float* pre, float* post, float* comb, hc_stream_t stream) {
-    if (!X || !pre_mix || !y_normed || !pre || !post || !comb) return HC_ERR_NULL;
+                float* pre, float* post, float* comb, void* workspace, hc_stream_t stream) {
+    if (!X || !pre_mix || !y_normed || !pre || !post || !comb || !workspace) return HC_ERR_NULL;
     int st = check_params(p);
     if (st != HC_OK) return st;
     st = check_shape_fused(n, s);
     if (st != HC_OK) return st;
     if (!aligned16(X) || !aligned16(pre_mix) || !aligned16(y_normed) || !aligned16(pre) || !aligned16(post) ||
-        !aligned16(comb))
+        !aligned16(comb) || !aligned16(workspace))
         return HC_ERR_ALIGN;
     const size_t N = static_cast<size_t>(n);
     const size_t xb = N * kHC * s.d * 2, yb = N * s.d * 2, cb = N * 16, kb = N * 64;
-    const void* outs[4] = {y_normed, pre, post, comb};
-    const size_t osz[4] = {yb, cb, cb, kb};
+    const void* outs[5] = {y_normed, pre, post, comb, workspace};
+    const size_t osz[5] = {yb, cb, cb, kb, workspace_bytes()};
     const void* ins[2] = {X, pre_mix};
     const size_t isz[2] = {xb, cb};
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 5; ++i) {
         for (int j = 0; j < 2; ++j)
             if (overlap(outs[i], osz[i], ins[j], isz[j])) return HC_ERR_ALIAS;
-        for (int j = i + 1; j < 4; ++j)
+        for (int j = i + 1; j < 5; ++j)
             if (overlap(outs[i], osz[i], outs[j], osz[j])) return HC_ERR_ALIAS;
     }
     if (n == 0) return HC_OK;
@@ -235,36 +243,38 @@ int hc_pre_step(const void* X, const float* pre_mix, hc_params_t p, int64_t n, h
     a.pre_out = pre;
     a.post_out = post;
     a.comb_out = comb;
+    a.workspace = workspace;
     a.n = n;
     a.d = s.d;
     a.iters = s.sinkhorn_iters;
     a.hc_eps = s.hc_eps;
     a.norm_eps = s.norm_eps;
-    return launch_fused(a, reinterpret_cast<cudaStream_t>(stream)) == 0 ? HC_OK : HC_ERR_CUDA;
+    return launch_status(launch_fused(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int hc_post_then_pre(const void* delta, const void* X, const float* post, const float* comb, const float* pre_mix,
                      hc_params_t next, int64_t n, hc_shape_t s, void* X_out, void* y_normed, float* pre_out,
-                     float* post_out, float* comb_out, hc_stream_t stream) {
-    if (!delta || !X || !post || !comb || !pre_mix || !X_out || !y_normed || !pre_out || !post_out || !comb_out)
+                     float* post_out, float* comb_out, void* workspace, hc_stream_t stream) {
+    if (!delta || !X || !post || !comb || !pre_mix || !X_out || !y_normed || !pre_out || !post_out || !comb_out ||
+        !workspace)
         return HC_ERR_NULL;
     int st = check_params(next);
     if (st != HC_OK) return st;
     st = check_shape_fused(n, s);
     if (st != HC_OK) return st;
-    const void* ptrs[10] = {delta, X, post, comb, pre_mix, X_out, y_normed, pre_out, post_out, comb_out};
+    const void* ptrs[11] = {delta, X, post, comb, pre_mix, X_out, y_normed, pre_out, post_out, comb_out, workspace};
     for (const void* q : ptrs)
         if (!aligned16(q)) return HC_ERR_ALIGN;
     const size_t N = static_cast<size_t>(n);
     const size_t xb = N * kHC * s.d * 2, yb = N * s.d * 2, cb = N * 16, kb = N * 64;
     const void* ins[5] = {delta, X, post, comb, pre_mix};
     const size_t isz[5] = {yb, xb, cb, kb, cb};
-    const void* outs[5] = {X_out, y_normed, pre_out, post_out, comb_out};
-    const size_t osz[5] = {xb, yb, cb, cb, kb};
-    for (int i = 0; i < 5; ++i) {
+    const void* outs[6] = {X_out, y_normed, pre_out, post_out, comb_out, workspace};
+    const size_t osz[6] = {xb, yb, cb, cb, kb, workspace_bytes()};
+    for (int i = 0; i < 6; ++i) {
         for (int j = 0; j < 5; ++j)
             if (overlap(outs[i], osz[i], ins[j], isz[j])) return HC_ERR_ALIAS;
-        for (int j = i + 1; j < 5; ++j)
+        for (int j = i + 1; j < 6; ++j)
             if (overlap(outs[i], osz[i], outs[j], osz[j])) return HC_ERR_ALIAS;
     }
     if (n == 0) return HC_OK;
@@ -284,23 +294,29 @@ int hc_post_then_pre(const void* delta, const void* X, const float* post, const 
     a.pre_out = pre_out;
     a.post_out = post_out;
     a.comb_out = comb_out;
+    a.workspace = workspace;
     a.n = n;
     a.d = s.d;
     a.iters = s.sinkhorn_iters;
     a.hc_eps = s.hc_eps;
     a.norm_eps = s.norm_eps;
-    return launch_fused(a, reinterpret_cast<cudaStream_t>(stream)) == 0 ? HC_OK : HC_ERR_CUDA;
+    return launch_status(launch_fused(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float* mixes, hc_stream_t stream) {
-    if (!X || !mixes || !p.hc_fn_planes) return HC_ERR_NULL;
+int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float* mixes, void* workspace,
+                   hc_stream_t stream) {
+    if (!X || !mixes || !p.hc_fn_planes || !workspace) return HC_ERR_NULL;
     hc_shape_t s2 = s;
     if (s2.sinkhorn_iters < 1) s2.sinkhorn_iters = 1;
     int st = check_shape_fused(n, s2);
     if (st != HC_OK) return st;
-    if (!aligned16(X) || !aligned16(mixes) || !aligned16(p.hc_fn_planes)) return HC_ERR_ALIGN;
+    if (!aligned16(X) || !aligned16(mixes) || !aligned16(p.hc_fn_planes) || !aligned16(workspace))
+        return HC_ERR_ALIGN;
     const size_t N = static_cast<size_t>(n);
-    if (overlap(mixes, N * kMix * 4, X, N * kHC * s.d * 2)) return HC_ERR_ALIAS;
+    if (overlap(mixes, N * kMix * 4, X, N * kHC * s.d * 2) ||
+        overlap(workspace, workspace_bytes(), X, N * kHC * s.d * 2) ||
+        overlap(workspace, workspace_bytes(), mixes, N * kMix * 4))
+        return HC_ERR_ALIAS;
     if (n == 0) return HC_OK;
     // the kernel reads scale/base/norm_w unconditionally: point them at the planes (never used)
     FusedArgs a = {};
@@ -311,24 +327,25 @@ int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float*
     a.hc_base = static_cast<const float*>(p.hc_fn_planes);
     a.norm_w = static_cast<const float*>(p.hc_fn_planes);
     a.mixes_out = mixes;
+    a.workspace = workspace;
     a.n = n;
     a.d = s.d;
     a.iters = s2.sinkhorn_iters;
     a.hc_eps = s2.hc_eps;
     a.norm_eps = s2.norm_eps;
-    return launch_fused(a, reinterpret_cast<cudaStream_t>(stream)) == 0 ? HC_OK : HC_ERR_CUDA;
+    return launch_status(launch_fused(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int hc_plan_tiles(int64_t n, int clusters, int* tile_m, int64_t* num_tiles) {
+int hc_plan_tiles(int64_t n, int groups, int* tile_m, int64_t* num_tiles) {
     if (!tile_m || !num_tiles) return HC_ERR_NULL;
-    if (n < 0 || clusters < 1) return HC_ERR_SHAPE;
-    plan_tiles(n, clusters, tile_m, num_tiles);
+    if (n < 0 || groups < 1) return HC_ERR_SHAPE;
+    plan_tiles(n, groups, tile_m, num_tiles);
     return HC_OK;
 }
 
-int hc_fused_clusters(int* clusters) {
-    if (!clusters) return HC_ERR_NULL;
-    return fused_active_clusters(clusters) == 0 ? HC_OK : HC_ERR_CUDA;
+int hc_fused_groups(int* groups) {
+    if (!groups) return HC_ERR_NULL;
+    return launch_status(fused_active_groups(groups));
 }
 
 int hc_device_error(unsigned int* word, int clear, hc_stream_t stream) {

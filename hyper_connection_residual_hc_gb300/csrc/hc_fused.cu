@@ -12,8 +12,8 @@
 //                                                                      RMSNorm excerpt
 // In pre-step mode X' is the input X itself and nothing is written back to the streams.
 //
-// Decomposition. A cluster of 8 CTAs owns a tile of up to 128 tokens; CTA `rank` owns the
-// d-slice [rank*d/8, (rank+1)*d/8) of every stream. Per 32-column stage a CTA:
+// Decomposition. A group of 8 CTAs owns a tile of up to 128 tokens; CTA `rank` of the group owns
+// the d-slice [rank*d/8, (rank+1)*d/8) of every stream. Per 32-column stage a CTA:
 //   - TMA-loads the four X tiles [tokens x 32 cols], the Delta tile and the four matching
 //     slices of the split projection weights (bf16 planes hi/mid/lo, 72 rows) into shared
 //     memory, 64-byte swizzled;
@@ -27,9 +27,14 @@
 //   - drains the stage's accumulator from TMEM into 12 per-thread fp32 sums (the three planes
 //     added back together); the two TMEM accumulators alternate so the MMA of stage s+1 runs
 //     while stage s drains.
-// At the end of a tile the CTAs exchange their 28 partial sums per token through distributed
-// shared memory: every CTA finishes RMSNorm for its slice of y (read back from TMEM, TMA-stored),
-// and CTA `rank` runs the split and Sinkhorn for the tokens t with t % 8 == rank.
+// At the end of a tile the 8 CTAs of the group exchange their 28 partial sums per token through
+// a caller-provided global workspace (L2-resident, ~14 KB per CTA per tile): each CTA writes its
+// block, publishes a release flag, and waits (bounded) for the 7 other flags. Then every CTA
+// finishes RMSNorm for its slice of y (read back from TMEM, TMA-stored), and CTA `rank` runs the
+// split and Sinkhorn for the tokens t with t % 8 == rank. The groups are formed in software
+// rather than as hardware clusters because only 15 clusters of 8 CTAs fit on a GB300 at once
+// (120 of its 152 SMs); the launch is cooperative, so all CTAs are resident together and the
+// flag waits between them cannot deadlock.
 //
 // Every wait on an mbarrier is bounded in time; on expiry the kernel records an error in a
 // device word, stops waiting everywhere, finishes its loops without hanging, frees its tensor
@@ -54,7 +59,8 @@ constexpr int kMix = 24;
 constexpr int kBRows = 72;        // 3 planes x 24 mixes
 constexpr int kUmmaM = 128;
 constexpr int kUmmaN = 80;        // smallest legal N >= 72 at M = 128
-constexpr int kCluster = 8;
+constexpr int kGroup = 8;          // CTAs sharing one token tile
+constexpr int kMaxGroups = 32;     // workspace capacity: up to 256 co-resident CTAs
 constexpr int kTileMax = 128;
 constexpr int kChunk = 32;        // columns per stage: 64-byte rows
 constexpr int kStages = 3;
@@ -76,17 +82,23 @@ constexpr int kOffB = kOffD + kXTileBytes;
 constexpr int kStageBytes = kOffB + 4 * kBTileBytes;          // 59392
 constexpr int kOffYStage = kStages * kStageBytes;
 constexpr int kYStageBytes = 32 * 16 * 2;                     // 32 rows x 32 B
-constexpr int kOffPart = kOffYStage + kComputeWarps * 2 * kYStageBytes;
 constexpr int kPartRows = 28;  // 24 mixes, sum x^2 (two halves), sum y^2 (two halves)
-constexpr int kPartBytes = kPartRows * kTileMax * 4;
-constexpr int kOffNormW = kOffPart + 2 * kPartBytes;
+constexpr int kPartFloats = kPartRows * kTileMax;
+constexpr int kOffNormW = kOffYStage + kComputeWarps * 2 * kYStageBytes;
 constexpr int kOffBar = kOffNormW + kMaxDSlice * 4;
 constexpr int kBarFull = 0, kBarXReady = 3, kBarEmpty = 6, kBarAccFull = 9, kBarAccEmpty = 11, kBarMmaDone = 13;
-constexpr int kNumBars = 14;
+constexpr int kBarXchg = 14, kBarSplitDone = 15;
+constexpr int kNumBars = 16;
 constexpr int kOffTmemPtr = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemPtr + 4;
 constexpr int kSmemUsed = kOffAbort + 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
+
+// global workspace: partial sums [group][tile parity][rank][28][128] fp32, then one 64-bit flag
+// per [group][tile parity][rank]
+constexpr size_t kWsPartBytes = static_cast<size_t>(kMaxGroups) * 2 * kGroup * kPartFloats * 4;
+constexpr size_t kWsFlagBytes = static_cast<size_t>(kMaxGroups) * 2 * kGroup * 8;
+constexpr size_t kWorkspaceBytes = kWsPartBytes + kWsFlagBytes;
 
 static_assert(kWarpSplit == kThreads / 32 - 1, "the split warp is the last one");
 static_assert(kStageBytes % 1024 == 0, "stage buffers keep 1024-byte alignment");
@@ -113,7 +125,8 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 // device error word: bit set = which wait gave up
 __device__ unsigned int g_hc_error = 0;
 enum : unsigned int {
-    kErrProducer = 1u, kErrMma = 2u, kErrComputeFull = 4u, kErrComputeAcc = 8u, kErrStore = 16u, kErrDrain = 32u
+    kErrProducer = 1u, kErrMma = 2u, kErrComputeFull = 4u, kErrComputeAcc = 8u, kErrStore = 16u, kErrDrain = 32u,
+    kErrExchange = 64u, kErrSplit = 128u
 };
 
 struct FusedParams {
@@ -127,6 +140,9 @@ struct FusedParams {
     float* post_out;
     float* comb_out;
     float* mixes_out;
+    float* ws_part;                 // workspace partial-sum blocks
+    unsigned long long* ws_flags;   // workspace flags
+    unsigned long long epoch_base;  // (launch id) << 32; tile `it` publishes epoch_base + it + 1
     long long n;
     long long num_tiles;
     int write_y;
@@ -175,7 +191,26 @@ struct Waiter {
             }
         }
     }
-    // Same, but ignores an abort raised elsewhere: used at exit to let copies in flight land.
+    // Wait until the 8 flags at f[0..7] all equal `epoch` (acquire at GPU scope).
+    __device__ __forceinline__ bool wait_flags(const unsigned long long* f, unsigned long long epoch,
+                                               unsigned int code) const {
+        const uint64_t t0 = global_timer_ns();
+        int r = 0;
+        while (r < kGroup) {
+            if (ld_acquire_gpu_u64(f + r) == epoch) {
+                ++r;
+                continue;
+            }
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort = 1u;
+                atomicOr(&g_hc_error, code);
+                return false;
+            }
+        }
+        return true;
+    }
+    // Same as wait, but ignores an abort raised elsewhere: used at exit to let copies in flight land.
     __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) const {
         const uint64_t t0 = global_timer_ns();
         while (!mbar_test(bar, parity)) {
@@ -250,9 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const uint32_t cid = cluster_id_x();
-    const uint32_t ncl = num_clusters_x();
+    const uint32_t rank = blockIdx.x % kGroup;    // d-slice of this CTA
+    const uint32_t cid = blockIdx.x / kGroup;     // group: owns tiles cid, cid + ncl, ...
+    const uint32_t ncl = gridDim.x / kGroup;
     const int d0 = static_cast<int>(rank) * p.d_slice;
     const int S = p.stages_per_tile;
 
@@ -271,6 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kBarAccEmpty + a), kComputeWarps);
         }
         mbar_init(bar(kBarMmaDone), 1);
+        mbar_init(bar(kBarXchg), 1);
+        mbar_init(bar(kBarSplitDone), 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -422,23 +459,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             drain(g - 1);
 
-            // partial sums of this CTA's slice -> shared memory for the cluster exchange
-            float* P = reinterpret_cast<float*>(smem + kOffPart + (it & 1) * kPartBytes);
+            // exchange: this CTA's partial sums -> workspace, publish, wait for the group
+            const int buf = static_cast<int>(it & 1);
+            float* blk = p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kGroup) * kPartFloats;
+            unsigned long long* flg = p.ws_flags + static_cast<size_t>(cid * 2 + buf) * kGroup;
+            const unsigned long long epoch = p.epoch_base + static_cast<unsigned long long>(it) + 1ull;
+            {
+                float* P = blk + static_cast<size_t>(rank) * kPartFloats;
 #pragma unroll
-            for (int i = 0; i < 12; ++i) P[(12 * h + i) * kTileMax + row] = acc[i];
-            P[(24 + h) * kTileMax + row] = (sx[0] + sx[1]) + (sx[2] + sx[3]);
-            P[(26 + h) * kTileMax + row] = sy[0] + sy[1];
+                for (int i = 0; i < 12; ++i) P[(12 * h + i) * kTileMax + row] = acc[i];
+                P[(24 + h) * kTileMax + row] = (sx[0] + sx[1]) + (sx[2] + sx[3]);
+                P[(26 + h) * kTileMax + row] = sy[0] + sy[1];
+            }
+            __threadfence();
             tmem_st_wait();
-            cluster_arrive();
-            cluster_wait();
+            named_bar_sync(1, kComputeWarps * 32);
+            if (threadIdx.x == 0) {
+                // this CTA's split warp must be done reading the previous tile's blocks before the
+                // flag tells the group that the buffer of tile it+1 may be reused
+                if (it > 0) W.wait(bar(kBarSplitDone), static_cast<uint32_t>((it - 1) & 1), kErrExchange);
+                st_release_gpu_u64(flg + rank, epoch);
+                W.wait_flags(flg, epoch, kErrExchange);
+                mbar_arrive(bar(kBarXchg));
+            }
+            named_bar_sync(1, kComputeWarps * 32);
 
             // RMSNorm of y: the statistic is the sum over all 8 slices
-            const uint32_t pa = sbase + kOffPart + static_cast<uint32_t>((it & 1) * kPartBytes);
             float syt = 0.f;
-            for (uint32_t r = 0; r < kCluster; ++r) {
-                const uint32_t ra = dsmem_addr(pa, r);
-                syt += ld_dsmem_f32(ra + static_cast<uint32_t>((26 * kTileMax + row) * 4)) +
-                       ld_dsmem_f32(ra + static_cast<uint32_t>((27 * kTileMax + row) * 4));
+            for (int r = 0; r < kGroup; ++r) {
+                const float* Pr = blk + static_cast<size_t>(r) * kPartFloats;
+                syt += ld_relaxed_gpu_f32(Pr + 26 * kTileMax + row) + ld_relaxed_gpu_f32(Pr + 27 * kTileMax + row);
             }
             const float ry = 1.0f / sqrtf(syt / static_cast<float>(p.d) + p.norm_eps);
 
@@ -502,10 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
-            if (it > 0) cluster_wait();
-            cluster_arrive();
         }
-        if (my_tiles > 0) cluster_wait();
         // let every load issued land before the CTA can exit
         const long long issued = g;
         for (long long gg = (issued > kStages ? issued - kStages : 0); gg < issued; ++gg)
@@ -539,10 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
-            if (it > 0) cluster_wait();
-            cluster_arrive();
         }
-        if (my_tiles > 0) cluster_wait();
         if (lane == 0) {
             umma_commit(bar(kBarMmaDone));
             W.drain(bar(kBarMmaDone), 0);
@@ -568,10 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarEmpty + slot));
             }
-            if (it > 0) cluster_wait();
-            cluster_arrive();
         }
-        if (my_tiles > 0) cluster_wait();
         if (lane == 0) bulk_wait<0>();
     } else {  // warp == kWarpSplit
         // ================= split + Sinkhorn for this CTA's share of each tile ===================
@@ -581,26 +622,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kMix; ++i) bs[i] = __ldg(p.hc_base + i);
         for (long long it = 0; it < my_tiles; ++it) {
-            cluster_arrive();
-            cluster_wait();
+            W.wait(bar(kBarXchg), static_cast<uint32_t>(it & 1), kErrSplit);
             const long long tile = cid + it * ncl;
             const long long t0 = tile * p.tile_m;
-            const int r_tok = static_cast<int>(rank) + kCluster * lane;
-            if (lane < kTileMax / kCluster && r_tok < p.tile_m && t0 + r_tok < p.n) {
-                const long long tok = t0 + r_tok;
-                const uint32_t pa = sbase + kOffPart + static_cast<uint32_t>((it & 1) * kPartBytes);
-                float m[kMix];
+            const int r_tok = static_cast<int>(rank) + kGroup * lane;
+            const bool mine = lane < kTileMax / kGroup && r_tok < p.tile_m && t0 + r_tok < p.n;
+            const float* blk = p.ws_part + (static_cast<size_t>(cid * 2 + (it & 1)) * kGroup) * kPartFloats;
+            float m[kMix];
 #pragma unroll
-                for (int i = 0; i < kMix; ++i) m[i] = 0.f;
-                float sxt = 0.f;
-                for (uint32_t r = 0; r < kCluster; ++r) {
-                    const uint32_t ra = dsmem_addr(pa, r);
+            for (int i = 0; i < kMix; ++i) m[i] = 0.f;
+            float sxt = 0.f;
+            if (mine) {
+                for (int r = 0; r < kGroup; ++r) {
+                    const float* Pr = blk + static_cast<size_t>(r) * kPartFloats;
 #pragma unroll
-                    for (int i = 0; i < kMix; ++i)
-                        m[i] += ld_dsmem_f32(ra + static_cast<uint32_t>((i * kTileMax + r_tok) * 4));
-                    sxt += ld_dsmem_f32(ra + static_cast<uint32_t>((24 * kTileMax + r_tok) * 4)) +
-                           ld_dsmem_f32(ra + static_cast<uint32_t>((25 * kTileMax + r_tok) * 4));
+                    for (int i = 0; i < kMix; ++i) m[i] += ld_relaxed_gpu_f32(Pr + i * kTileMax + r_tok);
+                    sxt += ld_relaxed_gpu_f32(Pr + 24 * kTileMax + r_tok) + ld_relaxed_gpu_f32(Pr + 25 * kTileMax + r_tok);
                 }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarSplitDone));  // the blocks of this tile may be reused
+            if (mine) {
+                const long long tok = t0 + r_tok;
                 const float rr = 1.0f / sqrtf(sxt / static_cast<float>(4 * p.d) + p.norm_eps);
 #pragma unroll
                 for (int i = 0; i < kMix; ++i) m[i] *= rr;
@@ -623,9 +666,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // nobody may read this CTA's shared memory after it exits
-    cluster_arrive();
-    cluster_wait();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -668,14 +708,15 @@ bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, co
 
 struct DeviceState {
     bool ready = false;
-    int clusters = 0;
+    int groups = 0;
 };
 
 constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
+unsigned int g_launch_id = 0;  // numbers the fused launches of this process (flag epochs)
 
-int prepare_device(int* clusters) {
+int prepare_device(int* groups) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -7;
     std::lock_guard<std::mutex> lk(g_dev_mu);
@@ -683,48 +724,42 @@ int prepare_device(int* clusters) {
     if (!st.ready) {
         const void* kernels[2] = {reinterpret_cast<const void*>(&hc_fused_kernel<false>),
                                   reinterpret_cast<const void*>(&hc_fused_kernel<true>)};
-        for (const void* k : kernels)
+        int per_sm = 1 << 30;
+        for (const void* k : kernels) {
             if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
                 return -7;
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = kCluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(kCluster, 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = kSmemBytes;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int nc = 0;
-        if (cudaOccupancyMaxActiveClusters(&nc, reinterpret_cast<const void*>(&hc_fused_kernel<true>), &cfg) !=
-                cudaSuccess ||
-            nc < 1)
-            return -7;
-        st.clusters = nc;
+            int b = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k, kThreads, kSmemBytes) != cudaSuccess || b < 1)
+                return -7;
+            per_sm = std::min(per_sm, b);
+        }
+        int sms = 0, coop = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -7;
+        if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) return -3;
+        st.groups = std::min(kMaxGroups, sms * per_sm / kGroup);
+        if (st.groups < 1) return -3;
         st.ready = true;
     }
-    *clusters = st.clusters;
+    *groups = st.groups;
     return 0;
 }
 
 }  // namespace
 
-void plan_tiles(int64_t n, int clusters, int* tile_m, int64_t* num_tiles) {
+void plan_tiles(int64_t n, int groups, int* tile_m, int64_t* num_tiles) {
     if (n <= 0) {
         *tile_m = kTileMax;
         *num_tiles = 0;
         return;
     }
-    if (clusters < 1) clusters = 1;
+    if (groups < 1) groups = 1;
     if (n <= kTileMax) {
-        // one tile per cluster at most; spread small batches over clusters in 32-token tiles
+        // one tile per group at most; spread small batches over groups in 32-token tiles
         int64_t best_tiles = 1;
         int best_m = static_cast<int>(n);
         for (int m = 32; m < n && m <= kTileMax; m += 32) {
             const int64_t tiles = (n + m - 1) / m;
-            if (tiles <= clusters) {
+            if (tiles <= groups) {
                 best_m = m;
                 best_tiles = tiles;
                 break;
@@ -740,7 +775,7 @@ void plan_tiles(int64_t n, int clusters, int* tile_m, int64_t* num_tiles) {
     int best_m = kTileMax;
     for (int m = kTileMax; m >= 32; m -= 32) {
         const int64_t tiles = (n + m - 1) / m;
-        const int64_t waves = (tiles + clusters - 1) / clusters;
+        const int64_t waves = (tiles + groups - 1) / groups;
         const int64_t cost = waves * (m + overhead);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
@@ -751,14 +786,17 @@ void plan_tiles(int64_t n, int clusters, int* tile_m, int64_t* num_tiles) {
     *num_tiles = (n + best_m - 1) / best_m;
 }
 
-int fused_active_clusters(int* clusters) { return prepare_device(clusters); }
+int fused_active_groups(int* groups) { return prepare_device(groups); }
+
+size_t workspace_bytes() { return kWorkspaceBytes; }
 
 int launch_fused(const FusedArgs& a, cudaStream_t stream) {
-    int clusters = 0;
-    if (prepare_device(&clusters) != 0) return -7;
+    int groups = 0;
+    const int st = prepare_device(&groups);
+    if (st != 0) return st;
     int tile_m = 0;
     int64_t num_tiles = 0;
-    plan_tiles(a.n, clusters, &tile_m, &num_tiles);
+    plan_tiles(a.n, groups, &tile_m, &num_tiles);
     if (num_tiles == 0) return 0;
 
     const uint64_t n = static_cast<uint64_t>(a.n), d = static_cast<uint64_t>(a.d);
@@ -798,25 +836,31 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     p.post_out = a.post_out;
     p.comb_out = a.comb_out;
     p.mixes_out = a.mixes_out;
+    p.ws_part = reinterpret_cast<float*>(a.workspace);
+    p.ws_flags = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(a.workspace) + kWsPartBytes);
+    {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        ++g_launch_id;
+        if (g_launch_id == 0) ++g_launch_id;  // 0 is what a zeroed workspace holds
+        p.epoch_base = static_cast<unsigned long long>(g_launch_id) << 32;
+    }
     p.n = a.n;
     p.num_tiles = num_tiles;
     p.write_y = a.y_normed != nullptr;
     p.d = a.d;
-    p.d_slice = a.d / kCluster;
+    p.d_slice = a.d / kGroup;
     p.stages_per_tile = p.d_slice / kChunk;
     p.tile_m = tile_m;
     p.iters = a.iters;
     p.hc_eps = a.hc_eps;
     p.norm_eps = a.norm_eps;
 
-    const int64_t grid_clusters = std::min<int64_t>(num_tiles, clusters);
+    const int64_t grid_groups = std::min<int64_t>(num_tiles, groups);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(grid_clusters * kCluster), 1, 1);
+    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident together: the group flags can be awaited
+    attr[0].val.cooperative = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_groups * kGroup), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;

@@ -25,6 +25,7 @@ struct FusedArgs {
     float* post_out;         // fp32 [n, 4]
     float* comb_out;         // fp32 [n, 4, 4]
     float* mixes_out;        // fp32 [n, 24]           (null: not written)
+    void* workspace;         // workspace_bytes(), zero-filled before its first use
     int64_t n;
     int d;
     int iters;
@@ -33,16 +34,19 @@ struct FusedArgs {
 };
 
 // Tile plan of the fused kernel: tokens per tile and number of tiles for n tokens when
-// `clusters` thread-block clusters run concurrently.
-void plan_tiles(int64_t n, int clusters, int* tile_m, int64_t* num_tiles);
+// `groups` groups of 8 CTAs run concurrently.
+void plan_tiles(int64_t n, int groups, int* tile_m, int64_t* num_tiles);
 
-// Launches the fused kernel; returns an HC_* status.
+// Launches the fused kernel; returns 0, -7 (CUDA failure) or -3 (no cooperative launch).
 int launch_fused(const FusedArgs& a, cudaStream_t stream);
 
 // Reads (and optionally clears) the device error word of the current device.
 int read_device_error(unsigned int* word, int clear, cudaStream_t stream);
 
-// Co-resident clusters of the fused kernel on the current device (cached per device).
-int fused_active_clusters(int* clusters);
+// Co-resident groups of 8 CTAs of the fused kernel on the current device (cached per device).
+int fused_active_groups(int* groups);
+
+// Bytes of the workspace the fused kernel exchanges partial sums through.
+size_t workspace_bytes();
 
 }  // namespace hc

@@ -94,6 +94,14 @@ int hc_prepare_params_size(int hc, int d, size_t* bytes);
  * No counterpart on the pages: it is this library's weight packing. hc must be 4. */
 int hc_prepare_params(const float* hc_fn, int hc, int d, void* planes, hc_stream_t stream);
 
+/* Size in bytes of the workspace the fused calls (hc_pre_step, hc_post_then_pre, hc_debug_mixes)
+ * need: the 8 CTAs that share a token tile exchange their per-token partial sums through it
+ * (about 14 KB per CTA per tile, L2-resident) together with one 64-bit flag per CTA and tile
+ * parity. The caller allocates it once [device], 16-byte aligned, fills it with zeros before its
+ * first use and then keeps passing it unchanged (no re-zeroing needed). Calls that may run at
+ * the same time on the GPU must not share a workspace. Host-only, no CUDA call. */
+int hc_workspace_size(size_t* bytes);
+
 /* Reading half of one sublayer ("Source layer, pairs pooled" page, Block.forward excerpt, the
  * lines up to the sublayer's norm): hc_mixes of X with `p`, hc_pre of X with pre_mix, RMSNorm.
  *   X        [device] bf16 [n, hc, d]      the incoming streams
@@ -102,9 +110,12 @@ int hc_prepare_params(const float* hc_fn, int hc, int d, void* planes, hc_stream
  *   y_normed [device] bf16 [n, d]          out: the sublayer's input
  *   pre, post [device] fp32 [n, hc]; comb [device] fp32 [n, hc, hc]   out: this sublayer's
  *            coefficients (pre goes to the next sublayer, post/comb to this one's hc_post)
- * Outputs must not overlap each other or any input (HC_ERR_ALIAS). */
+ *   workspace [device]                     see hc_workspace_size
+ * Outputs and the workspace must not overlap each other or any input (HC_ERR_ALIAS). The launch
+ * is cooperative (all its CTAs resident at once); HC_ERR_UNSUPPORTED if the device cannot. */
 int hc_pre_step(const void* X, const float* pre_mix, hc_params_t p, int64_t n, hc_shape_t s,
-                void* y_normed, float* pre, float* post, float* comb, hc_stream_t stream);
+                void* y_normed, float* pre, float* post, float* comb, void* workspace,
+                hc_stream_t stream);
 
 /* Writing half of a sublayer, then the reading half of the next one, fused in one pass:
  *   X_out = hc_post(delta, X, post, comb)   ("Write the streams" page, formula for X')
@@ -115,11 +126,13 @@ int hc_pre_step(const void* X, const float* pre_mix, hc_params_t p, int64_t n, h
  *   pre_mix [device] fp32 [n, hc]   the reading mix for the next sublayer (the pre returned by
  *                                   the call that produced post/comb)
  *   next                            the next sublayer's parameters
- * X_out is written once. Outputs must not overlap each other or any input (HC_ERR_ALIAS). */
+ *   workspace [device]              see hc_workspace_size
+ * X_out is written once. Outputs and the workspace must not overlap each other or any input
+ * (HC_ERR_ALIAS). Cooperative launch, as hc_pre_step. */
 int hc_post_then_pre(const void* delta, const void* X, const float* post, const float* comb,
                      const float* pre_mix, hc_params_t next, int64_t n, hc_shape_t s, void* X_out,
                      void* y_normed, float* pre_out, float* post_out, float* comb_out,
-                     hc_stream_t stream);
+                     void* workspace, hc_stream_t stream);
 
 /* Writing half alone ("Write the streams" page): X_out = bf16(post_k*delta + sum_j comb[j,k]*X_j).
  * For the last sublayer of a stack and for boundaries where another module edits the streams
@@ -132,15 +145,15 @@ int hc_post(const void* delta, const void* X, const float* post, const float* co
  * fused reading half computes them (same kernel, same tensor-core projection), for checking the
  * projection on its own. p.hc_scale, p.hc_base and p.norm_w are not read. */
 int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float* mixes,
-                   hc_stream_t stream);
+                   void* workspace, hc_stream_t stream);
 
-/* Tile plan of the fused calls for n tokens when `clusters` 8-CTA clusters run at once: tokens per
+/* Tile plan of the fused calls for n tokens when `groups` groups of 8 CTAs run at once: tokens per
  * tile (a multiple of 32 unless one tile holds all n <= 128 tokens) and the number of tiles.
  * Host-only, no CUDA call. Returns HC_ERR_NULL / HC_ERR_SHAPE on bad arguments. */
-int hc_plan_tiles(int64_t n, int clusters, int* tile_m, int64_t* num_tiles);
+int hc_plan_tiles(int64_t n, int groups, int* tile_m, int64_t* num_tiles);
 
-/* How many 8-CTA clusters of the fused kernel fit on the current device at once. */
-int hc_fused_clusters(int* clusters);
+/* How many groups of 8 CTAs of the fused kernel fit on the current device at once. */
+int hc_fused_groups(int* groups);
 
 /* Read the device-side error word of the current device: nonzero when a kernel gave up a
  * bounded wait (it then returned early and its outputs are not valid). Synchronises `stream`.

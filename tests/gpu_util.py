@@ -58,6 +58,17 @@ class DevParams:
         self.c = hc.params(self.planes, self.hc_scale, self.hc_base, self.norm_w)
 
 
+_WS = None
+
+
+def workspace():
+    """One zero-filled workspace shared by the (sequential) test calls."""
+    global _WS
+    if _WS is None:
+        _WS = hc.new_workspace()
+    return _WS
+
+
 def alloc_outputs(n: int, d: int, post_mode: bool):
     o = dict(y_normed=torch.empty((n, d), dtype=torch.bfloat16, device="cuda"),
              pre=torch.empty((n, 4), dtype=torch.float32, device="cuda"),
@@ -70,20 +81,20 @@ def alloc_outputs(n: int, d: int, post_mode: bool):
 
 def run_pre_step(X, pre_mix, P: DevParams, s, n):
     o = alloc_outputs(n, s.d, False)
-    hc.hc_pre_step(X, pre_mix, P.c, n, s, o["y_normed"], o["pre"], o["post"], o["comb"])
+    hc.hc_pre_step(X, pre_mix, P.c, n, s, o["y_normed"], o["pre"], o["post"], o["comb"], workspace())
     return o
 
 
 def run_post_then_pre(delta, X, post, comb, pre_mix, P: DevParams, s, n):
     o = alloc_outputs(n, s.d, True)
     hc.hc_post_then_pre(delta, X, post, comb, pre_mix, P.c, n, s, o["X_out"], o["y_normed"], o["pre"], o["post"],
-                        o["comb"])
+                        o["comb"], workspace())
     return o
 
 
 def debug_mixes(X, P: DevParams, s, n):
     m = torch.empty((n, 24), dtype=torch.float32, device="cuda")
-    hc.hc_debug_mixes(X, P.c, n, s, m)
+    hc.hc_debug_mixes(X, P.c, n, s, m, workspace())
     return m
 
 

@@ -68,32 +68,40 @@ def _expect(status, fn, *args):
     assert e.value.status == status, (e.value.status, status)
 
 
+def test_workspace_size(lib):
+    assert hc.hc_workspace_size() == 32 * 2 * 8 * 28 * 128 * 4 + 32 * 2 * 8 * 8
+
+
 def test_pre_step_validation(lib):
     s = hc.shape()
     st = 0
-    _expect(hc.HC_ERR_NULL, hc.hc_pre_step, None, A[1], _p(), 8, s, A[2], A[3], A[4], A[5], st)
-    _expect(hc.HC_ERR_NULL, hc.hc_pre_step, A[0], A[1], hc.params(None, A[11], A[12], A[13]), 8, s, A[2], A[3], A[4], A[5], st)
-    _expect(hc.HC_ERR_SHAPE, hc.hc_pre_step, A[0], A[1], _p(), -1, s, A[2], A[3], A[4], A[5], st)
-    _expect(hc.HC_ERR_SHAPE, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(d=5000), A[2], A[3], A[4], A[5], st)
-    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(hc=2), A[2], A[3], A[4], A[5], st)
-    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(d=5376), A[2], A[3], A[4], A[5], st)
-    _expect(hc.HC_ERR_ARG, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(sinkhorn_iters=0), A[2], A[3], A[4], A[5], st)
-    _expect(hc.HC_ERR_ARG, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(hc_eps=float("nan")), A[2], A[3], A[4], A[5], st)
-    _expect(hc.HC_ERR_ARG, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(norm_eps=-1.0), A[2], A[3], A[4], A[5], st)
-    _expect(hc.HC_ERR_ALIGN, hc.hc_pre_step, A[0] + 8, A[1], _p(), 8, s, A[2], A[3], A[4], A[5], st)
-    _expect(hc.HC_ERR_ALIGN, hc.hc_pre_step, A[0], A[1], hc.params(A[10] + 4, A[11], A[12], A[13]), 8, s, A[2], A[3], A[4], A[5], st)
-    # y_normed overlapping X, pre overlapping post
-    _expect(hc.HC_ERR_ALIAS, hc.hc_pre_step, A[0], A[1], _p(), 8, s, A[0] + 1024, A[3], A[4], A[5], st)
-    _expect(hc.HC_ERR_ALIAS, hc.hc_pre_step, A[0], A[1], _p(), 8, s, A[2], A[3], A[3] + 64, A[5], st)
+    W = A[14]
+    _expect(hc.HC_ERR_NULL, hc.hc_pre_step, None, A[1], _p(), 8, s, A[2], A[3], A[4], A[5], W, st)
+    _expect(hc.HC_ERR_NULL, hc.hc_pre_step, A[0], A[1], _p(), 8, s, A[2], A[3], A[4], A[5], None, st)
+    _expect(hc.HC_ERR_NULL, hc.hc_pre_step, A[0], A[1], hc.params(None, A[11], A[12], A[13]), 8, s, A[2], A[3], A[4], A[5], W, st)
+    _expect(hc.HC_ERR_SHAPE, hc.hc_pre_step, A[0], A[1], _p(), -1, s, A[2], A[3], A[4], A[5], W, st)
+    _expect(hc.HC_ERR_SHAPE, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(d=5000), A[2], A[3], A[4], A[5], W, st)
+    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(hc=2), A[2], A[3], A[4], A[5], W, st)
+    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(d=5376), A[2], A[3], A[4], A[5], W, st)
+    _expect(hc.HC_ERR_ARG, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(sinkhorn_iters=0), A[2], A[3], A[4], A[5], W, st)
+    _expect(hc.HC_ERR_ARG, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(hc_eps=float("nan")), A[2], A[3], A[4], A[5], W, st)
+    _expect(hc.HC_ERR_ARG, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(norm_eps=-1.0), A[2], A[3], A[4], A[5], W, st)
+    _expect(hc.HC_ERR_ALIGN, hc.hc_pre_step, A[0] + 8, A[1], _p(), 8, s, A[2], A[3], A[4], A[5], W, st)
+    _expect(hc.HC_ERR_ALIGN, hc.hc_pre_step, A[0], A[1], _p(), 8, s, A[2], A[3], A[4], A[5], W + 8, st)
+    _expect(hc.HC_ERR_ALIGN, hc.hc_pre_step, A[0], A[1], hc.params(A[10] + 4, A[11], A[12], A[13]), 8, s, A[2], A[3], A[4], A[5], W, st)
+    # y_normed overlapping X, pre overlapping post, the workspace overlapping X
+    _expect(hc.HC_ERR_ALIAS, hc.hc_pre_step, A[0], A[1], _p(), 8, s, A[0] + 1024, A[3], A[4], A[5], W, st)
+    _expect(hc.HC_ERR_ALIAS, hc.hc_pre_step, A[0], A[1], _p(), 8, s, A[2], A[3], A[3] + 64, A[5], W, st)
+    _expect(hc.HC_ERR_ALIAS, hc.hc_pre_step, A[0], A[1], _p(), 8, s, A[2], A[3], A[4], A[5], A[0] + 256, st)
     # n == 0 is a no-op
-    hc.hc_pre_step(A[0], A[1], _p(), 0, s, A[2], A[3], A[4], A[5], st)
+    hc.hc_pre_step(A[0], A[1], _p(), 0, s, A[2], A[3], A[4], A[5], W, st)
 
 
 def test_post_then_pre_validation(lib):
     s = hc.shape()
     st = 0
-    args = [A[0], A[1], A[2], A[3], A[4], _p(), 8, s, A[5], A[6], A[7], A[8], A[9], st]
-    for i in (0, 1, 2, 3, 4, 8, 9, 10, 11, 12):
+    args = [A[0], A[1], A[2], A[3], A[4], _p(), 8, s, A[5], A[6], A[7], A[8], A[9], A[14], st]
+    for i in (0, 1, 2, 3, 4, 8, 9, 10, 11, 12, 13):
         bad = list(args)
         bad[i] = None
         _expect(hc.HC_ERR_NULL, hc.hc_post_then_pre, *bad)
@@ -105,6 +113,9 @@ def test_post_then_pre_validation(lib):
     _expect(hc.HC_ERR_ALIAS, hc.hc_post_then_pre, *bad)
     bad = list(args)
     bad[9] = A[0]  # y_normed on delta
+    _expect(hc.HC_ERR_ALIAS, hc.hc_post_then_pre, *bad)
+    bad = list(args)
+    bad[13] = A[5] + 64  # workspace inside X_out
     _expect(hc.HC_ERR_ALIAS, hc.hc_post_then_pre, *bad)
     bad = list(args)
     bad[2] = A[2] + 12
@@ -126,9 +137,9 @@ def test_post_validation(lib):
 
 
 def test_plan_tiles(lib):
-    for clusters in (1, 7, 16, 18, 19):
+    for groups in (1, 7, 16, 18, 19):
         for n in [1, 2, 31, 32, 33, 64, 100, 127, 128, 129, 255, 256, 1000, 4096, 16384, 16385, 65536, 100003]:
-            tm, nt = hc.hc_plan_tiles(n, clusters)
+            tm, nt = hc.hc_plan_tiles(n, groups)
             assert 1 <= tm <= 128
             assert nt * tm >= n and (nt - 1) * tm < n
             if nt > 1:
@@ -137,7 +148,7 @@ def test_plan_tiles(lib):
     tm, nt = hc.hc_plan_tiles(16384, 19)
     waves = -(-nt // 19)
     assert waves * tm <= 1.1 * 16384 / 19
-    # decode batches use small tiles so that many clusters work
+    # decode batches use small tiles so that many groups work
     tm, nt = hc.hc_plan_tiles(256, 19)
     assert tm == 32 and nt == 8
     assert hc.hc_plan_tiles(0, 19) == (128, 0)

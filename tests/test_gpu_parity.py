@@ -210,7 +210,7 @@ def test_zero_tokens_is_a_noop():
     o["y_normed"].fill_(3.0)
     X = torch.zeros((4, 4, d), dtype=torch.bfloat16, device="cuda")
     pm = torch.zeros((4, 4), dtype=torch.float32, device="cuda")
-    hc.hc_pre_step(X, pm, P.c, 0, hc.shape(), o["y_normed"], o["pre"], o["post"], o["comb"])
+    hc.hc_pre_step(X, pm, P.c, 0, hc.shape(), o["y_normed"], o["pre"], o["post"], o["comb"], gu.workspace())
     torch.cuda.synchronize()
     assert bool((o["y_normed"] == 3.0).all())
 
