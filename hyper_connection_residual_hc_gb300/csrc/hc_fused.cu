@@ -69,7 +69,8 @@ constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpStore = 10;
 constexpr int kWarpSplit = 11;
-constexpr int kThreads = 12 * 32;
+constexpr int kWarpEpi0 = 12;       // warps 12..15: y_normed epilogue, TMEM lane quadrant = warp % 4
+constexpr int kThreads = 16 * 32;
 constexpr int kMaxDSlice = 640;   // d <= 5120
 
 // shared memory layout, offsets from a 1024-byte aligned base
@@ -80,15 +81,18 @@ constexpr int kOffX = 0;
 constexpr int kOffD = 4 * kXTileBytes;
 constexpr int kOffB = kOffD + kXTileBytes;
 constexpr int kStageBytes = kOffB + 4 * kBTileBytes;          // 59392
-constexpr int kOffYStage = kStages * kStageBytes;
-constexpr int kYStageBytes = 32 * 16 * 2;                     // 32 rows x 32 B
-constexpr int kPartRows = 28;  // 24 mixes, sum x^2 (two halves), sum y^2 (two halves)
+constexpr int kOffNormW = kStages * kStageBytes;
+// One CTA's partial sums for one tile: mixes [128 tokens][24] (token-major), then
+// sum x^2 [2 column halves][128], then sum y^2 [2][128].
+constexpr int kPartRows = 28;
 constexpr int kPartFloats = kPartRows * kTileMax;
-constexpr int kOffNormW = kOffYStage + kComputeWarps * 2 * kYStageBytes;
-constexpr int kOffBar = kOffNormW + kMaxDSlice * 4;
-constexpr int kBarFull = 0, kBarXReady = 3, kBarEmpty = 6, kBarAccFull = 9, kBarAccEmpty = 11, kBarMmaDone = 13;
-constexpr int kBarXchg = 14, kBarSplitDone = 15;
-constexpr int kNumBars = 16;
+constexpr int kPartSx = kMix * kTileMax, kPartSy = kPartSx + 2 * kTileMax;
+constexpr int kOffRy = kOffNormW + kMaxDSlice * 4;           // r_y of the last two tiles [2][128]
+constexpr int kOffBar = kOffRy + 2 * kTileMax * 4;
+constexpr int kBarFull = 0, kBarXReady = 3, kBarEmpty = 6, kBarAccFull = 9, kBarAccEmpty = 10, kBarMmaDone = 11;
+constexpr int kBarSplitDone = 12, kBarRyFull = 13, kBarRyEmpty = 15, kBarYReady = 17, kBarYFree = 17 + 27;
+constexpr int kNumBars = 17 + 2 * 27;
+constexpr uint32_t kBarIdPublish = 1;  // named barrier: compute warps arrive, the split warp syncs
 constexpr int kOffTmemPtr = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemPtr + 4;
 constexpr int kSmemUsed = kOffAbort + 4;
@@ -100,16 +104,22 @@ constexpr size_t kWsPartBytes = static_cast<size_t>(kMaxGroups) * 2 * kGroup * k
 constexpr size_t kWsFlagBytes = static_cast<size_t>(kMaxGroups) * 2 * kGroup * 8;
 constexpr size_t kWorkspaceBytes = kWsPartBytes + kWsFlagBytes;
 
-static_assert(kWarpSplit == kThreads / 32 - 1, "the split warp is the last one");
+static_assert(kWarpEpi0 + 4 == kThreads / 32 && kWarpEpi0 % 4 == 0, "one epilogue warp per TMEM lane quadrant");
+static_assert(kWarpSplit + 1 == kWarpEpi0, "warp roles: 8 compute, producer, MMA, store, split, 4 epilogue");
 static_assert(kStageBytes % 1024 == 0, "stage buffers keep 1024-byte alignment");
 static_assert(kOffB % 512 == 0 && kBTileBytes % 512 == 0, "B tiles start on 512-byte swizzle atoms");
-static_assert(kOffYStage % 256 == 0, "32-byte swizzle staging needs 256-byte alignment");
 static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in shared memory of one CTA");
 // the MMA of the last B tile of the last stage reads 8 rows (512 B) past it: still inside the CTA
 static_assert(kOffB + 3 * kBTileBytes + kUmmaN * 64 + (kStages - 1) * kStageBytes <= kSmemUsed, "B overrun");
 
+// TMEM: one accumulator (N = 80 columns), then a ring of kRing y chunks of 16 columns each
+// (32 rows x 16 bf16 pairs per warp quadrant). A tile has at most 20 stages, so the compute warps
+// can run 7 stages into the next tile before they must have stored the previous tile's y.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol0 = 0, kAccCol1 = 96, kYCol = 192;  // y slice: up to 320 columns
+constexpr uint32_t kAccCol = 0, kYCol = 80;
+constexpr int kRing = 27;
+static_assert(kYCol + kRing * 16 <= kTmemCols, "y ring fits in TMEM");
+static_assert(kBarYFree == kBarYReady + kRing, "one ready and one free barrier per ring slot");
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
@@ -126,7 +136,7 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 __device__ unsigned int g_hc_error = 0;
 enum : unsigned int {
     kErrProducer = 1u, kErrMma = 2u, kErrComputeFull = 4u, kErrComputeAcc = 8u, kErrStore = 16u, kErrDrain = 32u,
-    kErrExchange = 64u, kErrSplit = 128u
+    kErrExchange = 64u, kErrSplit = 128u, kErrEpilogue = 256u, kErrComputeY = 512u
 };
 
 struct FusedParams {
@@ -140,6 +150,7 @@ struct FusedParams {
     float* post_out;
     float* comb_out;
     float* mixes_out;
+    void* y_normed;
     float* ws_part;                 // workspace partial-sum blocks
     unsigned long long* ws_flags;   // workspace flags
     unsigned long long epoch_base;  // (launch id) << 32; tile `it` publishes epoch_base + it + 1
@@ -210,6 +221,26 @@ struct Waiter {
         }
         return true;
     }
+    // Whole warp: lanes 0..7 each wait for flag f[lane] to equal `epoch`; returns when all 8 do.
+    __device__ __forceinline__ bool wait_flags_warp(const unsigned long long* f, unsigned long long epoch, int lane,
+                                                    unsigned int code) const {
+        const uint64_t t0 = global_timer_ns();
+        bool mine = lane >= kGroup;
+        while (true) {
+            if (!mine) mine = ld_acquire_gpu_u64(f + lane) == epoch;
+            if (__all_sync(0xffffffffu, mine)) return true;
+            const bool aborted = *abort != 0u;
+            const bool late = global_timer_ns() - t0 > kWaitLimitNs;
+            if (__any_sync(0xffffffffu, aborted || late)) {  // one decision for the whole warp
+                if (lane == 0 && !aborted) {
+                    *abort = 1u;
+                    atomicOr(&g_hc_error, code);
+                }
+                __syncwarp();
+                return false;
+            }
+        }
+    }
     // Same as wait, but ignores an abort raised elsewhere: used at exit to let copies in flight land.
     __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) const {
         const uint64_t t0 = global_timer_ns();
@@ -279,7 +310,7 @@ template <bool kPost>
 __global__ void __launch_bounds__(kThreads, 1)
     hc_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmD,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmXo,
-                    const __grid_constant__ CUtensorMap tmY, const FusedParams p) {
+                    const FusedParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     const uint32_t sbase = smem_u32(smem);
@@ -301,13 +332,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kBarXReady + s), kComputeWarps);
             mbar_init(bar(kBarEmpty + s), 2);  // MMA completion + X' store done reading
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(bar(kBarAccFull + a), 1);
-            mbar_init(bar(kBarAccEmpty + a), kComputeWarps);
-        }
+        mbar_init(bar(kBarAccFull), 1);
+        mbar_init(bar(kBarAccEmpty), kComputeWarps);
         mbar_init(bar(kBarMmaDone), 1);
-        mbar_init(bar(kBarXchg), 1);
         mbar_init(bar(kBarSplitDone), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(kBarRyFull + b), 1);
+            mbar_init(bar(kBarRyEmpty + b), 4);  // the epilogue warps
+        }
+        for (int r = 0; r < kRing; ++r) {
+            mbar_init(bar(kBarYReady + r), kComputeWarps);
+            mbar_init(bar(kBarYFree + r), 4);
+        }
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -333,14 +369,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         (static_cast<long long>(cid) < p.num_tiles) ? (p.num_tiles - 1 - cid) / ncl + 1 : 0;
 
     if (warp < kComputeWarps) {
-        // ================= compute warps: X', sums, y, accumulator drain, epilogue ============
+        // ================= compute warps: X', sums, y, accumulator drain ========================
         const int q = warp & 3;             // TMEM lane quadrant = token rows 32q..32q+31
         const int h = warp >> 2;            // column half of each 32-column stage
         const int row = 32 * q + lane;      // token row inside the tile
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        const float* nw = reinterpret_cast<const float*>(smem + kOffNormW);
         long long g = 0;        // global stage counter (same sequence in every role)
-        uint32_t ycount = 0;    // y_normed staging buffers used by this warp
+        // tell the epilogue warps that the y chunk of stage gy is in TMEM
+        auto y_ready = [&](long long gy) {
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarYReady + static_cast<int>(gy % kRing)));
+        };
         for (long long it = 0; it < my_tiles; ++it) {
             const long long tile = cid + it * ncl;
             const long long t0 = tile * p.tile_m;
@@ -371,22 +412,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             float sy[2] = {0.f, 0.f};
 
             auto drain = [&](long long gd) {
-                const uint32_t a = static_cast<uint32_t>(gd & 1);
-                const uint32_t par = static_cast<uint32_t>((gd >> 1) & 1);
-                W.wait(bar(kBarAccFull + a), par, kErrComputeAcc);
+                W.wait(bar(kBarAccFull), static_cast<uint32_t>(gd & 1), kErrComputeAcc);
                 tc_fence_after();
                 uint32_t v[36];
-                const uint32_t col = (a ? kAccCol1 : kAccCol0) + 36u * h;
+                const uint32_t col = kAccCol + 36u * h;
                 tmem_ld36_wait(tl + col, tl + col + 32u, v);
 #pragma unroll
                 for (int i = 0; i < 12; ++i)
                     acc[i] += (__uint_as_float(v[i]) + __uint_as_float(v[12 + i])) + __uint_as_float(v[24 + i]);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kBarAccEmpty + a));
+                if (lane == 0) mbar_arrive(bar(kBarAccEmpty));
             };
 
             for (int s = 0; s < S; ++s, ++g) {
+                if (s > 0) {
+                    // the y store of the previous stage has had a stage to complete: hand it over,
+                    // then drain the previous accumulator (its MMA ran meanwhile), so that the MMA
+                    // of this stage can be issued the moment its X' is ready
+                    y_ready(g - 1);
+                    drain(g - 1);
+                }
+                // the ring slot of this stage's y last held the chunk of stage g - kRing
+                const long long yround = g / kRing;
+                if (yround > 0)
+                    W.wait(bar(kBarYFree + static_cast<int>(g % kRing)), static_cast<uint32_t>((yround - 1) & 1),
+                           kErrComputeY);
                 const int slot = static_cast<int>(g % kStages);
                 const uint32_t par = static_cast<uint32_t>((g / kStages) & 1);
                 W.wait(bar(kBarFull + slot), par, kErrComputeFull);
@@ -451,77 +502,77 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sy[cc] = fmaf(a1, a1, sy[cc]);
                     }
                 }
-                tmem_st8(tl + kYCol + static_cast<uint32_t>(s * 16 + h * 8), yb);
+                tmem_st8(tl + kYCol + static_cast<uint32_t>((g % kRing) * 16 + h * 8), yb);
                 if (kPost) fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarXReady + slot));
-                if (s > 0) drain(g - 1);
             }
             drain(g - 1);
+            y_ready(g - 1);
 
-            // exchange: this CTA's partial sums -> workspace, publish, wait for the group
+            // publish this CTA's partial sums of the tile to the group; the split warp collects them.
+            // The block of tile it reuses that of tile it - 2, which the other CTAs of the group may
+            // still be reading; each of them publishes tile it - 1 only after it has read tile it - 2,
+            // and this CTA's split warp signals split_done(it - 1) only after it has seen all those
+            // flags (and read tile it - 1 itself).
+            if (it > 0) W.wait(bar(kBarSplitDone), static_cast<uint32_t>((it - 1) & 1), kErrExchange);
             const int buf = static_cast<int>(it & 1);
-            float* blk = p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kGroup) * kPartFloats;
-            unsigned long long* flg = p.ws_flags + static_cast<size_t>(cid * 2 + buf) * kGroup;
-            const unsigned long long epoch = p.epoch_base + static_cast<unsigned long long>(it) + 1ull;
+            float* P = p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kGroup + rank) * kPartFloats;
             {
-                float* P = blk + static_cast<size_t>(rank) * kPartFloats;
+                float4* pm4 = reinterpret_cast<float4*>(P + row * kMix + 12 * h);
+                pm4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                pm4[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                pm4[2] = make_float4(acc[8], acc[9], acc[10], acc[11]);
+            }
+            P[kPartSx + h * kTileMax + row] = (sx[0] + sx[1]) + (sx[2] + sx[3]);
+            P[kPartSy + h * kTileMax + row] = sy[0] + sy[1];
+            // hand the block to the split warp, which publishes it; no waiting here
+            named_bar_arrive(kBarIdPublish, (kComputeWarps + 1) * 32);
+        }
+    } else if (warp >= kWarpEpi0) {
+        // ================= epilogue warps: y_normed = bf16(norm_w * y * r_y), one quadrant each ===
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        const float* nw = reinterpret_cast<const float*>(smem + kOffNormW);
+        const float* ry_s = reinterpret_cast<const float*>(smem + kOffRy);
+        long long g = 0;
+        for (long long it = 0; it < my_tiles; ++it) {
+            const int buf = static_cast<int>(it & 1);
+            W.wait(bar(kBarRyFull + buf), static_cast<uint32_t>((it >> 1) & 1), kErrEpilogue);
+            const float ry = ry_s[buf * kTileMax + row];
+            const long long t0 = (cid + it * ncl) * p.tile_m;
+            const bool store = p.write_y && row < p.tile_m && t0 + row < p.n;
+            uint16_t* yrow = static_cast<uint16_t*>(p.y_normed) + (store ? (t0 + row) * p.d + d0 : 0);
+            for (int s = 0; s < S; ++s, ++g) {
+                const int ys = static_cast<int>(g % kRing);
+                W.wait(bar(kBarYReady + ys), static_cast<uint32_t>((g / kRing) & 1), kErrEpilogue);
+                tc_fence_after();
+                uint32_t yv[16];
+                tmem_ld16_wait(tl + kYCol + static_cast<uint32_t>(ys * 16), yv);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarYFree + ys));
+                if (store) {
+                    // TMEM columns ys*16 + 0..7 hold stage columns 0..15 (half 0), + 8..15 hold 16..31
+                    const float* w = nw + s * 32;
+                    uint32_t ov[16];
 #pragma unroll
-                for (int i = 0; i < 12; ++i) P[(12 * h + i) * kTileMax + row] = acc[i];
-                P[(24 + h) * kTileMax + row] = (sx[0] + sx[1]) + (sx[2] + sx[3]);
-                P[(26 + h) * kTileMax + row] = sy[0] + sy[1];
-            }
-            __threadfence();
-            tmem_st_wait();
-            named_bar_sync(1, kComputeWarps * 32);
-            if (threadIdx.x == 0) {
-                // this CTA's split warp must be done reading the previous tile's blocks before the
-                // flag tells the group that the buffer of tile it+1 may be reused
-                if (it > 0) W.wait(bar(kBarSplitDone), static_cast<uint32_t>((it - 1) & 1), kErrExchange);
-                st_release_gpu_u64(flg + rank, epoch);
-                W.wait_flags(flg, epoch, kErrExchange);
-                mbar_arrive(bar(kBarXchg));
-            }
-            named_bar_sync(1, kComputeWarps * 32);
-
-            // RMSNorm of y: the statistic is the sum over all 8 slices
-            float syt = 0.f;
-            for (int r = 0; r < kGroup; ++r) {
-                const float* Pr = blk + static_cast<size_t>(r) * kPartFloats;
-                syt += ld_relaxed_gpu_f32(Pr + 26 * kTileMax + row) + ld_relaxed_gpu_f32(Pr + 27 * kTileMax + row);
-            }
-            const float ry = 1.0f / sqrtf(syt / static_cast<float>(p.d) + p.norm_eps);
-
-            if (p.write_y && 32 * q < p.tile_m) {
-                for (int s = 0; s < S; ++s) {
-                    uint32_t yv[8];
-                    tmem_ld8_wait(tl + kYCol + static_cast<uint32_t>(s * 16 + h * 8), yv);
-                    const float* w = nw + s * 32 + h * 16;
-                    uint32_t ov[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
+                    for (int e = 0; e < 16; ++e) {
                         const float a0 = w[2 * e] * (bf_lo(yv[e]) * ry);
                         const float a1 = w[2 * e + 1] * (bf_hi(yv[e]) * ry);
                         ov[e] = pack_bf16(a0, a1);
                     }
-                    const uint32_t buf = ycount & 1u;
-                    ++ycount;
-                    if (lane == 0) bulk_wait_read<1>();
-                    __syncwarp();
-                    const uint32_t st = sbase + kOffYStage + static_cast<uint32_t>((warp * 2 + buf) * kYStageBytes);
-                    const uint32_t sw = static_cast<uint32_t>((lane >> 2) & 1);
-                    st_smem_v4(st + lane * 32 + ((0u ^ sw) << 4), make_uint4(ov[0], ov[1], ov[2], ov[3]));
-                    st_smem_v4(st + lane * 32 + ((1u ^ sw) << 4), make_uint4(ov[4], ov[5], ov[6], ov[7]));
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmY, st, d0 + s * 32 + h * 16, static_cast<int>(t0 + 32 * q));
-                        bulk_commit();
-                    }
+                    uint4* dst = reinterpret_cast<uint4*>(yrow + s * 32);
+                    dst[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+                    dst[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
+                    dst[2] = make_uint4(ov[8], ov[9], ov[10], ov[11]);
+                    dst[3] = make_uint4(ov[12], ov[13], ov[14], ov[15]);
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarRyEmpty + buf));  // r_y buffer of this tile may be refilled
         }
-        if (lane == 0) bulk_wait<0>();
     } else if (warp == kWarpProducer) {
         // ================= TMA producer =========================================================
         uint64_t pol_stream = 0, pol_keep = 0;
@@ -564,14 +615,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (long long it = 0; it < my_tiles; ++it) {
             for (int s = 0; s < S; ++s, ++g) {
                 const int slot = static_cast<int>(g % kStages);
-                const uint32_t a = static_cast<uint32_t>(g & 1);
-                const long long ra = g >> 1;
-                if (ra > 0) W.wait(bar(kBarAccEmpty + a), static_cast<uint32_t>((ra - 1) & 1), kErrMma);
+                // the single accumulator must have been drained (stage g - 1)
+                if (g > 0) W.wait(bar(kBarAccEmpty), static_cast<uint32_t>((g - 1) & 1), kErrMma);
                 W.wait(bar(kBarXReady + slot), static_cast<uint32_t>((g / kStages) & 1), kErrMma);
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t sb = sbase + slot * kStageBytes;
-                    const uint32_t dcol = tmem + (a ? kAccCol1 : kAccCol0);
+                    const uint32_t dcol = tmem + kAccCol;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
 #pragma unroll
@@ -582,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     umma_commit(bar(kBarEmpty + slot));
-                    umma_commit(bar(kBarAccFull + a));
+                    umma_commit(bar(kBarAccFull));
                 }
                 __syncwarp();
             }
@@ -615,34 +665,90 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) bulk_wait<0>();
     } else {  // warp == kWarpSplit
-        // ================= split + Sinkhorn for this CTA's share of each tile ===================
+        // ===== group exchange, r_y of every row, split + Sinkhorn for this CTA's share ==========
         float sc[3], bs[kMix];
 #pragma unroll
         for (int i = 0; i < 3; ++i) sc[i] = __ldg(p.hc_scale + i);
 #pragma unroll
         for (int i = 0; i < kMix; ++i) bs[i] = __ldg(p.hc_base + i);
+        float* ry_s = reinterpret_cast<float*>(smem + kOffRy);
         for (long long it = 0; it < my_tiles; ++it) {
-            W.wait(bar(kBarXchg), static_cast<uint32_t>(it & 1), kErrSplit);
+            const int buf = static_cast<int>(it & 1);
+            // the compute warps have written this CTA's block of the tile: publish it, then wait for
+            // the group (lanes 0..7 poll one flag each)
+            named_bar_sync(kBarIdPublish, (kComputeWarps + 1) * 32);
+            unsigned long long* flg = p.ws_flags + static_cast<size_t>(cid * 2 + buf) * kGroup;
+            const unsigned long long epoch = p.epoch_base + static_cast<unsigned long long>(it) + 1ull;
+            if (lane == 0) {
+                fence_acq_rel_gpu();  // after the barrier: the compute threads' block writes come first
+                st_release_gpu_u64(flg + rank, epoch);
+            }
+            W.wait_flags_warp(flg, epoch, lane, kErrExchange);
+            // the compute warps must be done with the r_y buffer of tile it - 2
+            if (it >= 2) W.wait(bar(kBarRyEmpty + buf), static_cast<uint32_t>(((it >> 1) - 1) & 1), kErrSplit);
             const long long tile = cid + it * ncl;
             const long long t0 = tile * p.tile_m;
-            const int r_tok = static_cast<int>(rank) + kGroup * lane;
-            const bool mine = lane < kTileMax / kGroup && r_tok < p.tile_m && t0 + r_tok < p.n;
-            const float* blk = p.ws_part + (static_cast<size_t>(cid * 2 + (it & 1)) * kGroup) * kPartFloats;
+            const float* blk = p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kGroup) * kPartFloats;
+            {
+                // r_y of rows 4*lane .. 4*lane+3: sum y^2 over the 8 slices, 16 independent 16-byte loads
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int r = 0; r < kGroup; ++r) {
+                    const float* Pr = blk + static_cast<size_t>(r) * kPartFloats + kPartSy + 4 * lane;
+                    const float4 u = ld_cg_f4(Pr), v = ld_cg_f4(Pr + kTileMax);
+                    a.x += u.x + v.x; a.y += u.y + v.y; a.z += u.z + v.z; a.w += u.w + v.w;
+                }
+                const float inv_d = 1.0f / static_cast<float>(p.d);
+                float4 rv;
+                rv.x = 1.0f / sqrtf(a.x * inv_d + p.norm_eps);
+                rv.y = 1.0f / sqrtf(a.y * inv_d + p.norm_eps);
+                rv.z = 1.0f / sqrtf(a.z * inv_d + p.norm_eps);
+                rv.w = 1.0f / sqrtf(a.w * inv_d + p.norm_eps);
+                reinterpret_cast<float4*>(ry_s + buf * kTileMax)[lane] = rv;
+            }
+            // the owned tokens t = rank + 8i (i = lane % 16): lanes < 16 sum mixes 0..11 and sum x^2,
+            // lanes >= 16 mixes 12..23; the halves are then swapped between the two lanes
+            const int oi = lane & 15, oh = lane >> 4;
+            const int r_tok = static_cast<int>(rank) + kGroup * oi;
+            const bool mine = r_tok < p.tile_m && t0 + r_tok < p.n;
             float m[kMix];
 #pragma unroll
             for (int i = 0; i < kMix; ++i) m[i] = 0.f;
             float sxt = 0.f;
             if (mine) {
+                float part[12];
+#pragma unroll
+                for (int i = 0; i < 12; ++i) part[i] = 0.f;
+#pragma unroll
                 for (int r = 0; r < kGroup; ++r) {
                     const float* Pr = blk + static_cast<size_t>(r) * kPartFloats;
+                    const float* mp = Pr + r_tok * kMix + 12 * oh;
+                    const float4 u0 = ld_cg_f4(mp), u1 = ld_cg_f4(mp + 4), u2 = ld_cg_f4(mp + 8);
+                    part[0] += u0.x; part[1] += u0.y; part[2] += u0.z; part[3] += u0.w;
+                    part[4] += u1.x; part[5] += u1.y; part[6] += u1.z; part[7] += u1.w;
+                    part[8] += u2.x; part[9] += u2.y; part[10] += u2.z; part[11] += u2.w;
+                    if (oh == 0) sxt += Pr[kPartSx + r_tok] + Pr[kPartSx + kTileMax + r_tok];
+                }
 #pragma unroll
-                    for (int i = 0; i < kMix; ++i) m[i] += ld_relaxed_gpu_f32(Pr + i * kTileMax + r_tok);
-                    sxt += ld_relaxed_gpu_f32(Pr + 24 * kTileMax + r_tok) + ld_relaxed_gpu_f32(Pr + 25 * kTileMax + r_tok);
+                for (int i = 0; i < 12; ++i) {
+                    m[i] = oh ? 0.f : part[i];
+                    m[12 + i] = oh ? part[i] : 0.f;
                 }
             }
+            // lanes i and i + 16 hold the two halves of the same token's mixes
+#pragma unroll
+            for (int i = 0; i < 12; ++i) {
+                const float lo = __shfl_sync(0xffffffffu, m[i], oi);
+                const float hi = __shfl_sync(0xffffffffu, m[12 + i], oi + 16);
+                m[i] = lo;
+                m[12 + i] = hi;
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarSplitDone));  // the blocks of this tile may be reused
-            if (mine) {
+            if (lane == 0) {
+                mbar_arrive(bar(kBarRyFull + buf));  // r_y of this tile is in shared memory
+                mbar_arrive(bar(kBarSplitDone));     // the blocks of this tile may be reused
+            }
+            if (mine && oh == 0) {
                 const long long tok = t0 + r_tok;
                 const float rr = 1.0f / sqrtf(sxt / static_cast<float>(4 * p.d) + p.norm_eps);
 #pragma unroll
@@ -800,7 +906,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     if (num_tiles == 0) return 0;
 
     const uint64_t n = static_cast<uint64_t>(a.n), d = static_cast<uint64_t>(a.d);
-    CUtensorMap tmX, tmD, tmB, tmXo, tmY;
+    CUtensorMap tmX, tmD, tmB, tmXo;
     {
         const uint64_t dims[3] = {d, 4, n};
         const uint64_t str[2] = {d * 2, 4 * d * 2};
@@ -815,8 +921,6 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
         if (!encode(&tmD, a.post_mode ? a.delta : a.X, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B,
                     HC_STREAM_PROMOTION))
             return -7;
-        const uint32_t boxy[2] = {16, 32};
-        if (!encode(&tmY, a.y_normed ? a.y_normed : a.X, 2, dims, str, boxy, CU_TENSOR_MAP_SWIZZLE_32B)) return -7;
     }
     {
         const uint64_t dims[2] = {4 * d, static_cast<uint64_t>(kBRows)};
@@ -836,6 +940,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     p.post_out = a.post_out;
     p.comb_out = a.comb_out;
     p.mixes_out = a.mixes_out;
+    p.y_normed = a.y_normed;
     p.ws_part = reinterpret_cast<float*>(a.workspace);
     p.ws_flags = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(a.workspace) + kWsPartBytes);
     {
@@ -868,9 +973,9 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     cfg.numAttrs = 1;
     cudaError_t e;
     if (a.post_mode)
-        e = cudaLaunchKernelEx(&cfg, hc_fused_kernel<true>, tmX, tmD, tmB, tmXo, tmY, p);
+        e = cudaLaunchKernelEx(&cfg, hc_fused_kernel<true>, tmX, tmD, tmB, tmXo, p);
     else
-        e = cudaLaunchKernelEx(&cfg, hc_fused_kernel<false>, tmX, tmD, tmB, tmXo, tmY, p);
+        e = cudaLaunchKernelEx(&cfg, hc_fused_kernel<false>, tmX, tmD, tmB, tmXo, p);
     return e == cudaSuccess ? 0 : -7;
 }
 

@@ -51,6 +51,19 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity (acquire, CTA scope).
+__device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // ---- TMA (bulk tensor copies) ------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -183,6 +196,18 @@ __device__ __forceinline__ void tmem_ld8_wait(uint32_t taddr, uint32_t (&v)[8]) 
         : "memory");
 }
 
+// 32 lanes x 32-bit, 16 consecutive columns, load to registers and wait for the load.
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+
 // 32 lanes x 32-bit: 32 columns at taddr and 4 columns at taddr2, one wait for both.
 __device__ __forceinline__ void tmem_ld36_wait(uint32_t taddr, uint32_t taddr2, uint32_t (&v)[36]) {
     asm volatile(
@@ -280,9 +305,25 @@ __device__ __forceinline__ float ld_relaxed_gpu_f32(const float* p) {
     return v;
 }
 
-// Barrier `id` over the first `count` threads of the CTA (whole warps).
+// 16-byte load cached in L2 only: after an acquire it sees other CTAs' writes, never a stale L1 line.
+__device__ __forceinline__ float4 ld_cg_f4(const float* p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Named barrier `id` expecting `count` threads (whole warps): bar.sync waits for all of them,
+// bar.arrive counts the calling warp without waiting. Memory accesses made before either are
+// visible to the threads that return from bar.sync.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---- plain shared-memory vector access --------------------------------------------------------

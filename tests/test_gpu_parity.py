@@ -133,6 +133,23 @@ def test_hc_post_matches_oracle(n, d):
     assert np.array_equal(gu.host_u16(X), gu.host_u16(out))
 
 
+@pytest.mark.parametrize("d", [256, 512])
+def test_many_tiles_per_group_short_rows(d):
+    """d = 256 gives one 32-column stage per CTA and tile: tiles end every stage, so the group
+    exchange, the r_y hand-over and the y ring turn over at their fastest (about 17 tiles per group)."""
+    n = 40000
+    w = synth.small("step_b1_t64", 1, n, d, seed=500 + d)
+    inp = _inputs(w)
+    prm = synth.params(w, 0)
+    P = gu.DevParams(prm, d)
+    s = _shape(w)
+    dev = {k: (gu.dev_bf16(v) if v.dtype == np.uint16 else gu.dev_f32(v)) for k, v in inp.items()}
+    out = gu.run_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, s, n)
+    idx = _sample(n, 600, np.random.default_rng(d))
+    _check_sampled(w, 0, dev, out, prm, idx, True, "short rows d=%d" % d)
+    gu.device_error_clear()
+
+
 # ---- special cases with closed forms ------------------------------------------------------------
 
 def test_identity_comb_returns_streams_bit_exact():
