@@ -303,6 +303,63 @@ int hc_post_then_pre(const void* delta, const void* X, const float* post, const 
     return launch_status(launch_fused(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int hc_post_then_pre_noalloc(const void* delta, const void* X, const float* post, const float* comb,
+                             const float* pre_mix, hc_params_t next, int64_t n, hc_shape_t s, void* X_out,
+                             void* y_normed, float* pre_out, float* post_out, float* comb_out, hc_stream_t stream) {
+    // the same checks as hc_post_then_pre, before anything touches the device
+    if (!delta || !X || !post || !comb || !pre_mix || !X_out || !y_normed || !pre_out || !post_out || !comb_out)
+        return HC_ERR_NULL;
+    int st = check_params(next);
+    if (st != HC_OK) return st;
+    st = check_shape_fused(n, s);
+    if (st != HC_OK) return st;
+    const void* ptrs[10] = {delta, X, post, comb, pre_mix, X_out, y_normed, pre_out, post_out, comb_out};
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return HC_ERR_ALIGN;
+    const size_t N = static_cast<size_t>(n);
+    const size_t xb = N * kHC * s.d * 2, yb = N * s.d * 2, cb = N * 16, kb = N * 64;
+    const void* ins[5] = {delta, X, post, comb, pre_mix};
+    const size_t isz[5] = {yb, xb, cb, kb, cb};
+    const void* outs[5] = {X_out, y_normed, pre_out, post_out, comb_out};
+    const size_t osz[5] = {xb, yb, cb, cb, kb};
+    for (int i = 0; i < 5; ++i) {
+        for (int j = 0; j < 5; ++j)
+            if (overlap(outs[i], osz[i], ins[j], isz[j])) return HC_ERR_ALIAS;
+        for (int j = i + 1; j < 5; ++j)
+            if (overlap(outs[i], osz[i], outs[j], osz[j])) return HC_ERR_ALIAS;
+    }
+    if (n == 0) return HC_OK;
+    // the scratch is the library's fixed array: find this device's copy (first call only) and make
+    // sure the launch needs no more of it than it holds
+    void* ws = nullptr;
+    size_t capacity = 0;
+    if (noalloc_workspace(&ws, &capacity) != 0) return HC_ERR_CUDA;
+    if (workspace_bytes() > capacity) return HC_ERR_UNSUPPORTED;
+    FusedArgs a = {};
+    a.post_mode = true;
+    a.X = X;
+    a.delta = delta;
+    a.post = post;
+    a.comb = comb;
+    a.pre_mix = pre_mix;
+    a.planes = next.hc_fn_planes;
+    a.hc_scale = next.hc_scale;
+    a.hc_base = next.hc_base;
+    a.norm_w = next.norm_w;
+    a.X_out = X_out;
+    a.y_normed = y_normed;
+    a.pre_out = pre_out;
+    a.post_out = post_out;
+    a.comb_out = comb_out;
+    a.workspace = ws;
+    a.n = n;
+    a.d = s.d;
+    a.iters = s.sinkhorn_iters;
+    a.hc_eps = s.hc_eps;
+    a.norm_eps = s.norm_eps;
+    return launch_status(launch_fused(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float* mixes, void* workspace,
                    hc_stream_t stream) {
     if (!X || !mixes || !p.hc_fn_planes || !workspace) return HC_ERR_NULL;

@@ -979,6 +979,33 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     return e == cudaSuccess ? 0 : -7;
 }
 
+// ---- scratch that needs no allocation ------------------------------------------------------------
+// The workspace of hc_post_then_pre_noalloc: a fixed array in the library's device image, one per
+// GPU that loads the library, zero at load and kept until the process exits. Its size is the same
+// kWorkspaceBytes (7,344,128 bytes: room for 32 groups of 8 CTAs) that hc_workspace_size reports.
+static __device__ __align__(256) unsigned char g_noalloc_workspace[kWorkspaceBytes];
+
+namespace {
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+}  // namespace
+
+int noalloc_workspace(void** ptr, size_t* capacity) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -7;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        // host code only knows the array by its host-side stand-in: ask the runtime for the
+        // address of this device's copy, once, with this device current
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || !p) return -7;
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    *capacity = sizeof(g_noalloc_workspace);
+    return 0;
+}
+
 int read_device_error(unsigned int* word, int clear, cudaStream_t stream) {
     unsigned int v = 0;
     if (cudaMemcpyFromSymbolAsync(&v, g_hc_error, sizeof(v), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess)

@@ -49,4 +49,8 @@ int fused_active_groups(int* groups);
 // Bytes of the workspace the fused kernel exchanges partial sums through.
 size_t workspace_bytes();
 
+// Device address and size of the library's own fixed workspace on the current device (resolved
+// once per device); returns 0 or -7.
+int noalloc_workspace(void** ptr, size_t* capacity);
+
 }  // namespace hc

@@ -134,6 +134,28 @@ int hc_post_then_pre(const void* delta, const void* X, const float* post, const 
                      void* y_normed, float* pre_out, float* post_out, float* comb_out,
                      void* workspace, hc_stream_t stream);
 
+/* hc_post_then_pre for callers that cannot allocate device memory. Some callers can never call
+ * cudaMalloc (or any allocator) at the point where they run this step: a plugin hosted by an
+ * engine that owns all device memory and hands it no workspace, a runtime whose memory plan is
+ * frozen after start-up, or a program that must not risk an allocation failing mid-run. This
+ * entry point takes the same arguments as hc_post_then_pre minus the workspace, and computes the
+ * same results: its scratch is a fixed array inside the library's device image, 7,344,128 bytes
+ * (the hc_workspace_size figure), which every GPU that loads the library keeps until the process
+ * exits. It allocates nothing and calls no allocating routine.
+ *   - The first call on a device looks up that device's copy of the array (a runtime query, no
+ *     allocation); make that first call before any stream capture.
+ *   - A launch that would need more scratch than the array holds is refused with
+ *     HC_ERR_UNSUPPORTED (not possible on GPUs with up to 256 SMs).
+ *   - All calls share the one array. It needs no clearing between calls: it is zero at load and
+ *     every call tags its exchange flags with a new launch number. But two calls whose kernels
+ *     could run at the same time on the GPU (other streams, other threads) race on it and produce
+ *     wrong results; serialise them, or use hc_post_then_pre with separate workspaces.
+ * The pages have no counterpart to this call: it is a packaging of hc_post_then_pre only. */
+int hc_post_then_pre_noalloc(const void* delta, const void* X, const float* post, const float* comb,
+                             const float* pre_mix, hc_params_t next, int64_t n, hc_shape_t s,
+                             void* X_out, void* y_normed, float* pre_out, float* post_out,
+                             float* comb_out, hc_stream_t stream);
+
 /* Writing half alone ("Write the streams" page): X_out = bf16(post_k*delta + sum_j comb[j,k]*X_j).
  * For the last sublayer of a stack and for boundaries where another module edits the streams
  * before the next reading half. s.sinkhorn_iters and the eps fields are ignored; d is a multiple
