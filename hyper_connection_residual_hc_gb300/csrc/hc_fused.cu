@@ -13,28 +13,29 @@
 // In pre-step mode X' is the input X itself and nothing is written back to the streams.
 //
 // Decomposition. A group of 8 CTAs owns a tile of up to 128 tokens; CTA `rank` of the group owns
-// the d-slice [rank*d/8, (rank+1)*d/8) of every stream. Per 32-column stage a CTA:
-//   - TMA-loads the four X tiles [tokens x 32 cols], the Delta tile and the four matching
-//     slices of the split projection weights (bf16 planes hi/mid/lo, 72 rows) into shared
-//     memory, 64-byte swizzled;
-//   - computes X' in place (thread = token: 8 compute warps, two per TMEM lane quadrant, each
-//     warp owning 16 of the 32 columns), accumulates sum(X'^2), forms y, rounds it, accumulates
-//     sum(y^2) and parks the bf16 y row-slice in tensor memory;
-//   - lets one thread issue 8 tcgen05.mma (M=128 tokens, N=80 >= 72 plane rows, K=16) that
-//     project the bf16 X' tile on the three planes; the products are exact in fp32, so the
-//     split projection has fp32-FFMA accuracy;
-//   - TMA-stores the X' tile (written once) from the same shared-memory buffer;
-//   - drains the stage's accumulator from TMEM into 12 per-thread fp32 sums (the three planes
-//     added back together); the two TMEM accumulators alternate so the MMA of stage s+1 runs
-//     while stage s drains.
-// At the end of a tile the 8 CTAs of the group exchange their 28 partial sums per token through
-// a caller-provided global workspace (L2-resident, ~14 KB per CTA per tile): each CTA writes its
-// block, publishes a release flag, and waits (bounded) for the 7 other flags. Then every CTA
-// finishes RMSNorm for its slice of y (read back from TMEM, TMA-stored), and CTA `rank` runs the
-// split and Sinkhorn for the tokens t with t % 8 == rank. The groups are formed in software
-// rather than as hardware clusters because only 15 clusters of 8 CTAs fit on a GB300 at once
-// (120 of its 152 SMs); the launch is cooperative, so all CTAs are resident together and the
-// flag waits between them cannot deadlock.
+// the d-slice [rank*d/8, (rank+1)*d/8) of every stream. The 16 warps of a CTA have fixed roles:
+//   producer (warp 8): per 32-column stage, TMA-loads the four X tiles [tokens x 32 cols], the
+//     Delta tile and the four matching slices of the split projection weights (bf16 planes
+//     hi/mid/lo, 72 rows) into one of 3 shared-memory slots, 64-byte swizzled;
+//   compute (warps 0-7, thread = token, two warps per TMEM lane quadrant, 16 columns each):
+//     compute X' in place, accumulate sum(X'^2), form and round y, accumulate sum(y^2), store the
+//     bf16 y chunk into a ring of 27 chunk slots in tensor memory, and drain the previous
+//     stage's accumulator into 12 per-thread fp32 sums (the three planes added back together);
+//   MMA (warp 9): one thread issues 8 tcgen05.mma per stage (M=128 tokens, N=80 >= 72 plane
+//     rows, K=16) projecting the bf16 X' tile on the three planes into a TMEM accumulator; the
+//     products are exact in fp32, so the split projection has fp32-FFMA accuracy;
+//   store (warp 10): TMA-stores the X' tile (written once) from the same slot, then frees it;
+//   split (warp 11): at each tile end, publishes the CTA's partial sums (28 per token, in a
+//     caller-provided global workspace) with a release flag, waits (bounded) for the 7 other flags
+//     of the group, turns the sums of y^2 into r_y for all 128 rows, and runs the split and
+//     Sinkhorn for the tokens t with t % 8 == rank;
+//   epilogue (warps 12-15, one per TMEM lane quadrant): read each y chunk back from the ring,
+//     scale it by norm_w and r_y and write y_normed with 64-byte row stores.
+// The ring gives the exchange 7 stages of slack: the compute warps stream on into the next tile
+// while the group finishes the previous one. The groups are formed in software rather than as
+// hardware clusters because only 15 clusters of 8 CTAs fit on a GB300 at once (120 of its 152
+// SMs); the launch is cooperative, so all CTAs are resident together and the flag waits between
+// them cannot deadlock.
 //
 // Every wait on an mbarrier is bounded in time; on expiry the kernel records an error in a
 // device word, stops waiting everywhere, finishes its loops without hanging, frees its tensor
