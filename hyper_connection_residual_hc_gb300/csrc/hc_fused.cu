@@ -13,7 +13,9 @@
 // In pre-step mode X' is the input X itself and nothing is written back to the streams.
 //
 // Decomposition. A group of 8 CTAs owns a tile of up to 128 tokens; CTA `rank` of the group owns
-// the d-slice [rank*d/8, (rank+1)*d/8) of every stream. The 16 warps of a CTA have fixed roles:
+// d/8 columns of every stream, the 32-column chunks rank, rank+8, rank+16, ... (interleaved, so
+// the group's loads of one stage cover 256 contiguous columns of each row). The 16 warps of a
+// CTA have fixed roles:
 //   producer (warp 8): per 32-column stage, TMA-loads the four X tiles [tokens x 32 cols], the
 //     Delta tile and the four matching slices of the split projection weights (bf16 planes
 //     hi/mid/lo, 72 rows) into one of 3 shared-memory slots, 64-byte swizzled;
@@ -317,10 +319,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = blockIdx.x % kGroup;    // d-slice of this CTA
+    const uint32_t rank = blockIdx.x % kGroup;    // column share of this CTA
     const uint32_t cid = blockIdx.x / kGroup;     // group: owns tiles cid, cid + ncl, ...
     const uint32_t ncl = gridDim.x / kGroup;
-    const int d0 = static_cast<int>(rank) * p.d_slice;
+    // first column of stage s of this CTA: the 8 CTAs of a group take interleaved 32-column
+    // chunks, so at any moment they read and write 512 contiguous bytes of each stream row
+    auto stage_col = [&](int s) -> int { return (s * kGroup + static_cast<int>(rank)) * kChunk; };
     const int S = p.stages_per_tile;
 
     auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
@@ -355,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     {
         float* nw = reinterpret_cast<float*>(smem + kOffNormW);
-        for (int i = threadIdx.x; i < p.d_slice; i += kThreads) nw[i] = p.norm_w[d0 + i];
+        for (int i = threadIdx.x; i < p.d_slice; i += kThreads) nw[i] = p.norm_w[stage_col(i / kChunk) + i % kChunk];
     }
     if (warp == 0) {
         tmem_alloc(sbase + kOffTmemPtr, kTmemCols);
@@ -544,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float ry = ry_s[buf * kTileMax + row];
             const long long t0 = (cid + it * ncl) * p.tile_m;
             const bool store = p.write_y && row < p.tile_m && t0 + row < p.n;
-            uint16_t* yrow = static_cast<uint16_t*>(p.y_normed) + (store ? (t0 + row) * p.d + d0 : 0);
+            uint16_t* yrow = static_cast<uint16_t*>(p.y_normed) + (store ? (t0 + row) * p.d : 0);
             for (int s = 0; s < S; ++s, ++g) {
                 const int ys = static_cast<int>(g % kRing);
                 W.wait(bar(kBarYReady + ys), static_cast<uint32_t>((g / kRing) & 1), kErrEpilogue);
@@ -564,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float a1 = w[2 * e + 1] * (bf_hi(yv[e]) * ry);
                         ov[e] = pack_bf16(a0, a1);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(yrow + s * 32);
+                    uint4* dst = reinterpret_cast<uint4*>(yrow + stage_col(s));
                     dst[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
                     dst[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
                     dst[2] = make_uint4(ov[8], ov[9], ov[10], ov[11]);
@@ -594,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     const uint32_t sb = sbase + slot * kStageBytes;
                     const uint32_t fb = bar(kBarFull + slot);
-                    const int col = d0 + s * kChunk;
+                    const int col = stage_col(s);
                     mbar_arrive_expect_tx(fb, bytes);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) tma_load_3d(sb + kOffX + j * kXTileBytes, &tmX, fb, col, j, t0, pol_stream);
@@ -654,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 W.wait(bar(kBarXReady + slot), static_cast<uint32_t>((g / kStages) & 1), kErrStore);
                 if (kPost && lane == 0) {
                     const uint32_t sb = sbase + slot * kStageBytes;
-                    const int col = d0 + s * kChunk;
+                    const int col = stage_col(s);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) tma_store_3d(&tmXo, sb + kOffX + k * kXTileBytes, col, k, t0);
                     bulk_commit();
