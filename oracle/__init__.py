@@ -10,7 +10,8 @@ patterns (``numpy.uint16``).
 
 Sources, cited per function in ``hc_oracle.cpp`` (DeepSeek V4.1 model-atlas pages):
 "Source layer, pairs pooled" (Block excerpts), "Reading weights" (hc_split_sinkhorn excerpt and the
-formula for p), "Final RMSNorm" (RMSNorm excerpt and formula), "Write the streams" (formula for X').
+formula for p), "Final RMSNorm" (RMSNorm excerpt and formula, Transformer.forward excerpt for the
+ends of the stack), "Write the streams" (formula for X').
 """
 
 from __future__ import annotations
@@ -63,6 +64,10 @@ def _declare(lib):
                                        _P, _P, _P, _P, _P, _P, _P, _P, _I]
     lib.oracle_hc_post_then_pre.argtypes = [_I64, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                             _I, _D, _D, _P, _P, _P, _P, _P, _I]
+    lib.oracle_hc_expand.argtypes = [_I64, _I, _I, _P, _P, _I]
+    lib.oracle_hc_expand_pre_step.argtypes = [_I64, _I, _I, _P, _P, _P, _P, _P, _I, _D, _D, _P, _P, _P, _P, _P, _I]
+    lib.oracle_hc_final.argtypes = [_I64, _I, _I, _P, _P, _P, _D, _P, _P, _P, _I]
+    lib.oracle_hc_post_then_final.argtypes = [_I64, _I, _I, _P, _P, _P, _P, _P, _P, _D, _P, _P, _I]
     lib.oracle_hardware_threads.restype = _I
     lib.oracle_hardware_threads.argtypes = []
 
@@ -222,4 +227,58 @@ def hc_post_then_pre(delta, X, post, comb, pre_mix, hc_fn, hc_scale, hc_base, no
                                 _p(hc_scale), _p(hc_base), _p(norm_w), int(iters), float(hc_eps), float(norm_eps),
                                 _p(out["X_out"]), _p(out["y_normed"]), _p(out["pre"]), _p(out["post"]),
                                 _p(out["comb"]), threads)
+    return out
+
+
+def hc_expand(h, hc=4, threads=0, lib=None):
+    """The embedding rows h [n,d] (u16) copied into hc streams: [n,hc,d]."""
+    lib = lib or load()
+    h = _c(h, np.uint16)
+    n, d = h.shape
+    out = np.empty((n, hc, d), np.uint16)
+    lib.oracle_hc_expand(n, hc, d, _p(h), _p(out), threads)
+    return out
+
+
+def hc_expand_pre_step(h, hc_fn, hc_scale, hc_base, norm_w, iters, hc_eps, norm_eps, hc=4, threads=0, lib=None):
+    """Head of the stack: expand, then the first reading half with the identity pre_mix. Returns a
+    dict: X_out, y_normed, pre, post, comb."""
+    lib = lib or load()
+    h = _c(h, np.uint16)
+    n, d = h.shape
+    hc_fn, hc_scale, hc_base, norm_w = (_c(hc_fn, np.float32), _c(hc_scale, np.float32),
+                                        _c(hc_base, np.float32), _c(norm_w, np.float32))
+    out = dict(X_out=np.empty((n, hc, d), np.uint16), y_normed=np.empty((n, d), np.uint16), pre=np.empty((n, hc)),
+               post=np.empty((n, hc)), comb=np.empty((n, hc, hc)))
+    lib.oracle_hc_expand_pre_step(n, hc, d, _p(h), _p(hc_fn), _p(hc_scale), _p(hc_base), _p(norm_w), int(iters),
+                                  float(hc_eps), float(norm_eps), _p(out["X_out"]), _p(out["y_normed"]),
+                                  _p(out["pre"]), _p(out["post"]), _p(out["comb"]), threads)
+    return out
+
+
+def hc_final(X, pre_mix, norm_w, norm_eps, threads=0, lib=None):
+    """Tail of the stack: collapse with pre_mix, then the final RMSNorm. Returns (z, y, z before
+    rounding)."""
+    lib = lib or load()
+    X = _c(X, np.uint16)
+    n, hc, d = X.shape
+    pre_mix, norm_w = _c(pre_mix, np.float32), _c(norm_w, np.float32)
+    z = np.empty((n, d), np.uint16)
+    y = np.empty((n, d), np.uint16)
+    ze = np.empty((n, d), np.float64)
+    lib.oracle_hc_final(n, hc, d, _p(X), _p(pre_mix), _p(norm_w), float(norm_eps), _p(z), _p(y), _p(ze), threads)
+    return z, y, ze
+
+
+def hc_post_then_final(delta, X, post, comb, pre_mix, norm_w, norm_eps, threads=0, lib=None):
+    """The last writing half, then the tail of the stack. Returns a dict: X_out, z."""
+    lib = lib or load()
+    X = _c(X, np.uint16)
+    n, hc, d = X.shape
+    delta, post, comb, pre_mix = (_c(delta, np.uint16), _c(post, np.float32), _c(comb, np.float32),
+                                  _c(pre_mix, np.float32))
+    norm_w = _c(norm_w, np.float32)
+    out = dict(X_out=np.empty_like(X), z=np.empty((n, d), np.uint16))
+    lib.oracle_hc_post_then_final(n, hc, d, _p(delta), _p(X), _p(post), _p(comb), _p(pre_mix), _p(norm_w),
+                                  float(norm_eps), _p(out["X_out"]), _p(out["z"]), threads)
     return out

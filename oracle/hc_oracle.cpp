@@ -13,7 +13,10 @@
 //         Block.hc_mixes / hc_pre / hc_post excerpts; Parameters table (stream weights 491,547).
 //   [RW]  "Reading weights" page: the formula for p_{n+1,j}, and the Code section's
 //         hc_split_sinkhorn kernel excerpt and its wrapper.
-//   [FN]  "Final RMSNorm" page: the m_2(x) formula and the RMSNorm excerpt.
+//   [FN]  "Final RMSNorm" page: the m_2(x) formula (with its epsilon of 1e-20), the RMSNorm
+//         excerpt, and the Transformer.forward excerpt (the embedding copied into the hc streams
+//         before the first block; after the last block one more collapse with the last pre_mix,
+//         then the final norm).
 //   [WS]  "Write the streams" page: the formula for X'_{n,k} and its in/out shapes.
 //   [RT]  "Router" page, config.json excerpt: hc_mult 4, hc_sinkhorn_iters 20, hc_eps 1e-6,
 //         norm_eps 1e-20, dim 5120.
@@ -231,6 +234,18 @@ void rmsnorm_token(int d, const uint16_t* x, const float* w, double eps, uint16_
     }
 }
 
+// [FN] Transformer.forward excerpt: the embedding row h [d] becomes hc identical streams.
+void expand_token(int hc, int d, const uint16_t* h, uint16_t* X) {
+    for (int j = 0; j < hc; ++j) std::copy(h, h + d, X + static_cast<int64_t>(j) * d);
+}
+
+// The identity pre_mix the same excerpt hands to the first block is not printed on the pages. On
+// hc identical streams every set of weights summing to 1 collapses them to the embedding itself;
+// the oracle takes the uniform weights 1/hc (exact in binary for hc = 2, 4, 8).
+void identity_pre_mix(int hc, float* pm) {
+    for (int j = 0; j < hc; ++j) pm[j] = 1.0f / static_cast<float>(hc);
+}
+
 }  // namespace
 
 extern "C" {
@@ -330,6 +345,46 @@ void oracle_hc_post_then_pre(int64_t n, int hc, int d, const uint16_t* delta, co
     oracle_hc_post(n, hc, d, X, delta, post_in, comb_in, X_out, threads);
     oracle_hc_pre_step(n, hc, d, X_out, pre_mix, hc_fn, hc_scale, hc_base, norm_w, iters, hc_eps, norm_eps,
                        y_normed, pre, post, comb, nullptr, nullptr, nullptr, nullptr, threads);
+}
+
+// [FN] Transformer.forward excerpt, the head of the stack: expand the embedding h [n,d] into hc
+// streams (X_out [n,hc,d]) and run the first sublayer's reading half on them with the identity
+// pre_mix (uniform 1/hc). Outputs as oracle_hc_pre_step.
+void oracle_hc_expand(int64_t n, int hc, int d, const uint16_t* h, uint16_t* X_out, int threads) {
+    parallel_for(n, threads, [&](int64_t t) { expand_token(hc, d, h + t * d, X_out + t * hc * d); });
+}
+
+void oracle_hc_expand_pre_step(int64_t n, int hc, int d, const uint16_t* h, const float* hc_fn,
+                               const float* hc_scale, const float* hc_base, const float* norm_w, int iters,
+                               double hc_eps, double norm_eps, uint16_t* X_out, uint16_t* y_normed, double* pre,
+                               double* post, double* comb, int threads) {
+    oracle_hc_expand(n, hc, d, h, X_out, threads);
+    std::vector<float> pm(static_cast<size_t>(n) * hc);
+    for (int64_t t = 0; t < n; ++t) identity_pre_mix(hc, pm.data() + t * hc);
+    oracle_hc_pre_step(n, hc, d, X_out, pm.data(), hc_fn, hc_scale, hc_base, norm_w, iters, hc_eps, norm_eps,
+                       y_normed, pre, post, comb, nullptr, nullptr, nullptr, nullptr, threads);
+}
+
+// [FN] Transformer.forward excerpt, the tail of the stack: collapse the streams X [n,hc,d] once more
+// with the pre_mix the last sublayer produced (hc_pre, cast to bf16), then the final RMSNorm with
+// its gain norm_w [d] and epsilon norm_eps (1e-20 on the page's formula). z [n,d] bf16; optional
+// y [n,d] (the bf16 collapse) and z before rounding.
+void oracle_hc_final(int64_t n, int hc, int d, const uint16_t* X, const float* pre_mix, const float* norm_w,
+                     double norm_eps, uint16_t* z, uint16_t* y_out, double* z_exact, int threads) {
+    parallel_for(n, threads, [&](int64_t t) {
+        std::vector<uint16_t> y(d);
+        pre_token(hc, d, X + t * hc * d, pre_mix + t * hc, y.data(), nullptr, nullptr);
+        rmsnorm_token(d, y.data(), norm_w, norm_eps, z + t * d, z_exact ? z_exact + t * d : nullptr);
+        if (y_out) std::copy(y.begin(), y.end(), y_out + t * d);
+    });
+}
+
+// The last sublayer's writing half (hc_post, X_out [n,hc,d]) followed by oracle_hc_final on X_out.
+void oracle_hc_post_then_final(int64_t n, int hc, int d, const uint16_t* delta, const uint16_t* X,
+                               const float* post, const float* comb, const float* pre_mix, const float* norm_w,
+                               double norm_eps, uint16_t* X_out, uint16_t* z, int threads) {
+    oracle_hc_post(n, hc, d, X, delta, post, comb, X_out, threads);
+    oracle_hc_final(n, hc, d, X_out, pre_mix, norm_w, norm_eps, z, nullptr, nullptr, threads);
 }
 
 int oracle_hardware_threads() {

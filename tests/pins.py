@@ -8,8 +8,9 @@ bit-level identities, and invariants the method guarantees (ranges, column sums)
 
 Definitions pinned (DeepSeek V4.1 model-atlas pages): 'Source layer, pairs pooled' page, Block
 excerpts (hc_mixes, hc_pre, hc_post, forward) and Parameters table; 'Reading weights' page,
-hc_split_sinkhorn kernel excerpt and the formula for p; 'Final RMSNorm' page, RMSNorm excerpt and
-the m_2 formula; 'Write the streams' page, the formula for X'.
+hc_split_sinkhorn kernel excerpt and the formula for p; 'Final RMSNorm' page, RMSNorm excerpt, the
+m_2 formula and the Transformer.forward excerpt (ends of the stack); 'Write the streams' page, the
+formula for X'.
 """
 
 from __future__ import annotations
@@ -466,6 +467,97 @@ def pin_parameter_count(lib):
     X = np.zeros((1, hc, dim), np.uint16)
     m, _, _ = orc.hc_mixes(X, np.zeros((mix_hc, hc * dim), np.float32), 1e-6, lib=lib)
     assert m.shape == (1, mix_hc) and np.all(m == 0)
+
+
+# ---- ends of the stack ('Final RMSNorm' page, Transformer.forward excerpt) ------------------------
+
+def _rand_bf16(rng, shape, scale=1.0):
+    return ((rng.standard_normal(shape) * scale).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def pin_expand_copies_embedding(lib):
+    """The embedding row becomes hc identical streams, stream-major: X[t, j, :] = h[t, :]."""
+    h = _rand_bf16(np.random.default_rng(20), (3, 24))
+    X = orc.hc_expand(h, hc=4, lib=lib)
+    assert X.shape == (3, 4, 24)
+    for j in range(4):
+        assert np.array_equal(X[:, j], h)
+
+
+def pin_expand_pre_step_folds(lib):
+    """Head of the stack. With weights summing to 1 the collapse of identical streams is the
+    embedding itself, so y_normed is the closed-form norm of h; the statistic over the hc*d
+    expanded values is the mean over h's d values, and the projection folds over the streams:
+    mixes = r * h . (sum over j of hc_fn's j-th column block), computed here with numpy. Any other
+    identity-like weights (one-hot e_3) give the same y_normed."""
+    rng = np.random.default_rng(21)
+    n, d = 5, 16
+    h = _rand_bf16(rng, (n, d))
+    fn = (rng.standard_normal((24, 4 * d)) * 0.2).astype(np.float32)
+    sc = np.array([0.7, 1.3, 0.9], np.float32)
+    base = rng.standard_normal(24).astype(np.float32)
+    w = (1 + 0.1 * rng.standard_normal(d)).astype(np.float32)
+    out = orc.hc_expand_pre_step(h, fn, sc, base, w, 20, 1e-6, 1e-6, lib=lib)
+    hf = orc.bf16_to_double(h)
+    want = w.astype(np.float64) * hf / np.sqrt((hf ** 2).mean(axis=1, keepdims=True) + 1e-6)
+    assert np.array_equal(out["y_normed"], orc.double_to_bf16(want, lib=lib))
+    r = 1.0 / np.sqrt((hf ** 2).mean(axis=1) + 1e-6)
+    fold = fn.astype(np.float64).reshape(24, 4, d).sum(axis=1)
+    m = (hf @ fold.T) * r[:, None]
+    pre, post, comb = orc.split_sinkhorn(m, sc, base, 4, 20, 1e-6, lib=lib)
+    assert np.allclose(out["pre"], pre, rtol=1e-12, atol=1e-14)
+    assert np.allclose(out["post"], post, rtol=1e-12, atol=1e-14)
+    assert np.allclose(out["comb"], comb, rtol=1e-10, atol=1e-13)
+    pm = np.zeros((n, 4), np.float32)
+    pm[:, 3] = 1.0
+    o2 = orc.hc_pre_step(out["X_out"], pm, fn, sc, base, w, 20, 1e-6, 1e-6, lib=lib)
+    assert np.array_equal(o2["y_normed"], out["y_normed"])
+    # small embeddings, where the eps is not negligible: the norm is no longer scale-invariant, so
+    # this also pins that the weights sum to 1 (y = h, not a multiple of it)
+    hs = _rand_bf16(rng, (n, d), scale=2.0 ** -11)
+    hsf = orc.bf16_to_double(hs)
+    out = orc.hc_expand_pre_step(hs, fn, sc, base, w, 20, 1e-6, 1e-6, lib=lib)
+    want = w.astype(np.float64) * hsf / np.sqrt((hsf ** 2).mean(axis=1, keepdims=True) + 1e-6)
+    assert np.array_equal(out["y_normed"], orc.double_to_bf16(want, lib=lib))
+
+
+def pin_final_norm_epsilon(lib):
+    """Tail of the stack on the hand-worked streams: y = 0.75 stream0 + 0.25 stream1 = (1, 0.5, ...),
+    z = w * y / sqrt(mean(y^2) + eps). At the final norm's eps = 1e-20 streams scaled by 2^-12 give
+    the same z (the eps is negligible against 0.625 * 2^-24); at eps = 1e-6 they do not."""
+    g, hc, d, X, _ = _hand_case()
+    pm = np.array([[0.75, 0.25]], np.float32)
+    w = np.linspace(0.5, 1.5, d).astype(np.float32)
+    wd = w.astype(np.float64)
+    z, y, ze = orc.hc_final(X, pm, w, 1e-20, lib=lib)
+    yv = np.tile([1.0, 0.5], 4)
+    assert np.array_equal(orc.bf16_to_double(y[0]), yv)
+    assert np.allclose(ze[0], wd * yv / math.sqrt(0.625 + 1e-20), rtol=1e-15)
+    assert np.array_equal(z[0], orc.double_to_bf16(ze[0], lib=lib))
+    Xs = _bf(orc.bf16_to_double(X) * 2.0 ** -12)
+    _, _, zs = orc.hc_final(Xs, pm, w, 1e-20, lib=lib)
+    assert np.allclose(zs, ze, rtol=1e-11)
+    _, _, zb = orc.hc_final(Xs, pm, w, 1e-6, lib=lib)
+    assert np.allclose(zb[0], wd * yv * 2.0 ** -12 / math.sqrt(0.625 * 2.0 ** -24 + 1e-6), rtol=1e-14)
+    assert not np.allclose(zb, ze, rtol=1e-3)
+
+
+def pin_post_then_final_hand_case(lib):
+    """Hand-worked step B through the tail of the stack: X' as worked by hand, y = (1.4375, 0.6875,
+    ...) and z the final norm of y at eps 1e-20, which is step B's sublayer norm (eps 1e-6) up to the
+    eps."""
+    g, hc, d, X, _ = _hand_case()
+    b = g["step_b"]
+    delta = _bf(np.full((1, d), b["delta"]))
+    out = orc.hc_post_then_final(delta, X, np.array([b["post_in"]], np.float32), np.array([b["comb_in"]], np.float32),
+                                 np.array([b["pre_mix"]], np.float32), np.ones(d, np.float32), 1e-20, lib=lib)
+    xo = orc.bf16_to_double(out["X_out"][0])
+    assert np.array_equal(xo[0], np.tile(b["X_out_stream0_first_two"], 4))
+    assert np.array_equal(xo[1], np.tile(b["X_out_stream1_first_two"], 4))
+    y = np.tile(b["y_first_two"], 4)
+    want = y / math.sqrt((y ** 2).mean() + 1e-20)
+    assert np.array_equal(out["z"][0], orc.double_to_bf16(want, lib=lib))
+    assert np.allclose(want[:2], b["y_normed_exact_first_two"], rtol=1e-6)
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -59,6 +59,21 @@ MUTANTS = {
                                    " double ss = 0; for (int i = 0; i < d; ++i) ss += ye[i] * ye[i];"
                                    " double rr = 1.0 / std::sqrt(ss / d + norm_eps);"
                                    " for (int i = 0; i < d; ++i) y_normed[t * d + i] = double_to_bf16(norm_w[i] * (ye[i] * rr)); }"),
+    "expand_interleaved": ("for (int j = 0; j < hc; ++j) std::copy(h, h + d, X + static_cast<int64_t>(j) * d);",
+                           "for (int i = 0; i < d; ++i) for (int j = 0; j < hc; ++j) X[i * hc + j] = h[i];"),
+    "expand_identity_not_normalised": ("pm[j] = 1.0f / static_cast<float>(hc);", "pm[j] = 1.0f;"),
+    "expand_identity_one_hot_wrong_scale": ("pm[j] = 1.0f / static_cast<float>(hc);",
+                                            "pm[j] = (j == 0) ? 0.5f : 0.0f;"),
+    "final_uses_fixed_eps": ("rmsnorm_token(d, y.data(), norm_w, norm_eps, z + t * d, z_exact ? z_exact + t * d : nullptr);",
+                             "rmsnorm_token(d, y.data(), norm_w, 1e-6, z + t * d, z_exact ? z_exact + t * d : nullptr);"),
+    "final_skips_collapse_rounding": ("pre_token(hc, d, X + t * hc * d, pre_mix + t * hc, y.data(), nullptr, nullptr);\n"
+                                      "        rmsnorm_token(d, y.data(), norm_w, norm_eps, z + t * d",
+                                      "pre_token(hc, d, X + t * hc * d, pre_mix + t * hc, y.data(), nullptr, nullptr);\n"
+                                      "        for (int i = 0; i < d; ++i) y[i] = X[t * hc * d + i];\n"
+                                      "        rmsnorm_token(d, y.data(), norm_w, norm_eps, z + t * d"),
+    "post_then_final_skips_post": ("oracle_hc_post(n, hc, d, X, delta, post, comb, X_out, threads);\n"
+                                   "    oracle_hc_final(",
+                                   "std::copy(X, X + n * hc * d, X_out);\n    oracle_hc_final("),
 }
 
 
