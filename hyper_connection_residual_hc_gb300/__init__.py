@@ -31,8 +31,8 @@ HC_ERR_DEVICE = -8
 # every symbol include/hc.h declares
 SYMBOLS = (
     "hc_prepare_params_size", "hc_prepare_params", "hc_workspace_size", "hc_pre_step", "hc_post_then_pre",
-    "hc_post_then_pre_noalloc", "hc_post", "hc_debug_mixes", "hc_plan_tiles", "hc_fused_groups", "hc_device_error",
-    "hc_status_string",
+    "hc_post_then_pre_noalloc", "hc_post", "hc_expand_pre_step", "hc_final", "hc_post_then_final", "hc_debug_mixes",
+    "hc_plan_tiles", "hc_fused_groups", "hc_device_error", "hc_status_string",
 )
 
 
@@ -72,6 +72,9 @@ def load(path: str = LIB_PATH):
     lib.hc_post_then_pre.argtypes = [P, P, P, P, P, hc_params_t, I64, hc_shape_t, P, P, P, P, P, P, P]
     lib.hc_post_then_pre_noalloc.argtypes = [P, P, P, P, P, hc_params_t, I64, hc_shape_t, P, P, P, P, P, P]
     lib.hc_post.argtypes = [P, P, P, P, I64, hc_shape_t, P, P]
+    lib.hc_expand_pre_step.argtypes = [P, hc_params_t, I64, hc_shape_t, P, P, P, P, P, P, P]
+    lib.hc_final.argtypes = [P, P, P, I64, hc_shape_t, P, P]
+    lib.hc_post_then_final.argtypes = [P, P, P, P, P, P, I64, hc_shape_t, P, P, P]
     lib.hc_debug_mixes.argtypes = [P, hc_params_t, I64, hc_shape_t, P, P, P]
     lib.hc_plan_tiles.argtypes = [I64, I, ctypes.POINTER(I), ctypes.POINTER(I64)]
     lib.hc_fused_groups.argtypes = [ctypes.POINTER(I)]
@@ -168,6 +171,24 @@ def hc_post_then_pre_noalloc(delta, X, post, comb, pre_mix, nxt: hc_params_t, n:
 def hc_post(delta, X, post, comb, n: int, s: hc_shape_t, X_out, stream=None) -> None:
     _check("hc_post", load().hc_post(_ptr(delta), _ptr(X), _ptr(post), _ptr(comb), n, s, _ptr(X_out),
                                      _stream(stream)))
+
+
+def hc_expand_pre_step(h, p: hc_params_t, n: int, s: hc_shape_t, X_out, y_normed, pre, post, comb, workspace,
+                       stream=None) -> None:
+    _check("hc_expand_pre_step", load().hc_expand_pre_step(
+        _ptr(h), p, n, s, _ptr(X_out), _ptr(y_normed), _ptr(pre), _ptr(post), _ptr(comb), _ptr(workspace),
+        _stream(stream)))
+
+
+def hc_final(X, pre_mix, norm_w, n: int, s: hc_shape_t, z, stream=None) -> None:
+    _check("hc_final", load().hc_final(_ptr(X), _ptr(pre_mix), _ptr(norm_w), n, s, _ptr(z), _stream(stream)))
+
+
+def hc_post_then_final(delta, X, post, comb, pre_mix, norm_w, n: int, s: hc_shape_t, X_out, z, stream=None) -> None:
+    """X_out may be None: the streams after the last block are then not written."""
+    _check("hc_post_then_final", load().hc_post_then_final(
+        _ptr(delta), _ptr(X), _ptr(post), _ptr(comb), _ptr(pre_mix), _ptr(norm_w), n, s, _ptr(X_out), _ptr(z),
+        _stream(stream)))
 
 
 def hc_debug_mixes(X, p: hc_params_t, n: int, s: hc_shape_t, mixes, workspace, stream=None) -> None:

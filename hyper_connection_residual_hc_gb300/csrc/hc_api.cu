@@ -1,6 +1,6 @@
 // C ABI of libhc.so (declared in include/hc.h): host-side argument validation, the two
 // elementwise kernels (standalone writing half, weight splitting) and dispatch to the fused
-// reading-half kernel.
+// reading-half kernel (hc_fused.cu) and the tail-of-stack kernel (hc_final.cu).
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -128,6 +128,27 @@ int check_shape_fused(int64_t n, const hc_shape_t& s) {
     return HC_OK;
 }
 
+// shape rules of the tail-of-stack calls: d a multiple of 8 up to 5120, only norm_eps is used
+int check_shape_final(int64_t n, const hc_shape_t& s) {
+    if (n < 0 || s.hc < 1 || s.d < 1 || s.d % 8 != 0 || n > 0x7FFFFFFFLL) return HC_ERR_SHAPE;
+    if (s.hc != kHC || s.d > kFinalMaxD) return HC_ERR_UNSUPPORTED;
+    if (!std::isfinite(s.norm_eps) || s.norm_eps < 0.f) return HC_ERR_ARG;
+    return HC_OK;
+}
+
+// true if any output overlaps an input or another output (null entries are skipped)
+bool any_overlap(const void* const* outs, const size_t* osz, int no, const void* const* ins, const size_t* isz,
+                 int ni) {
+    for (int i = 0; i < no; ++i) {
+        if (!outs[i]) continue;
+        for (int j = 0; j < ni; ++j)
+            if (ins[j] && overlap(outs[i], osz[i], ins[j], isz[j])) return true;
+        for (int j = i + 1; j < no; ++j)
+            if (outs[j] && overlap(outs[i], osz[i], outs[j], osz[j])) return true;
+    }
+    return false;
+}
+
 int check_params(const hc_params_t& p) {
     if (!p.hc_fn_planes || !p.hc_scale || !p.hc_base || !p.norm_w) return HC_ERR_NULL;
     if (!aligned16(p.hc_fn_planes) || !aligned16(p.hc_scale) || !aligned16(p.hc_base) || !aligned16(p.norm_w))
@@ -232,7 +253,7 @@ int hc_pre_step(const void* X, const float* pre_mix, hc_params_t p, int64_t n, h
     }
     if (n == 0) return HC_OK;
     FusedArgs a = {};
-    a.post_mode = false;
+    a.mode = kModePre;
     a.X = X;
     a.pre_mix = pre_mix;
     a.planes = p.hc_fn_planes;
@@ -279,7 +300,7 @@ int hc_post_then_pre(const void* delta, const void* X, const float* post, const 
     }
     if (n == 0) return HC_OK;
     FusedArgs a = {};
-    a.post_mode = true;
+    a.mode = kModePost;
     a.X = X;
     a.delta = delta;
     a.post = post;
@@ -336,7 +357,7 @@ int hc_post_then_pre_noalloc(const void* delta, const void* X, const float* post
     if (noalloc_workspace(&ws, &capacity) != 0) return HC_ERR_CUDA;
     if (workspace_bytes() > capacity) return HC_ERR_UNSUPPORTED;
     FusedArgs a = {};
-    a.post_mode = true;
+    a.mode = kModePost;
     a.X = X;
     a.delta = delta;
     a.post = post;
@@ -360,6 +381,101 @@ int hc_post_then_pre_noalloc(const void* delta, const void* X, const float* post
     return launch_status(launch_fused(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int hc_expand_pre_step(const void* h, hc_params_t p, int64_t n, hc_shape_t s, void* X_out, void* y_normed, float* pre,
+                       float* post, float* comb, void* workspace, hc_stream_t stream) {
+    if (!h || !X_out || !y_normed || !pre || !post || !comb || !workspace) return HC_ERR_NULL;
+    int st = check_params(p);
+    if (st != HC_OK) return st;
+    st = check_shape_fused(n, s);
+    if (st != HC_OK) return st;
+    const void* ptrs[7] = {h, X_out, y_normed, pre, post, comb, workspace};
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return HC_ERR_ALIGN;
+    const size_t N = static_cast<size_t>(n);
+    const size_t xb = N * kHC * s.d * 2, yb = N * s.d * 2, cb = N * 16, kb = N * 64;
+    const void* ins[1] = {h};
+    const size_t isz[1] = {yb};
+    const void* outs[6] = {X_out, y_normed, pre, post, comb, workspace};
+    const size_t osz[6] = {xb, yb, cb, cb, kb, workspace_bytes()};
+    if (any_overlap(outs, osz, 6, ins, isz, 1)) return HC_ERR_ALIAS;
+    if (n == 0) return HC_OK;
+    FusedArgs a = {};
+    a.mode = kModeExpand;
+    a.embed = h;
+    a.planes = p.hc_fn_planes;
+    a.hc_scale = p.hc_scale;
+    a.hc_base = p.hc_base;
+    a.norm_w = p.norm_w;
+    a.X_out = X_out;
+    a.y_normed = y_normed;
+    a.pre_out = pre;
+    a.post_out = post;
+    a.comb_out = comb;
+    a.workspace = workspace;
+    a.n = n;
+    a.d = s.d;
+    a.iters = s.sinkhorn_iters;
+    a.hc_eps = s.hc_eps;
+    a.norm_eps = s.norm_eps;
+    return launch_status(launch_fused(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int hc_final(const void* X, const float* pre_mix, const float* norm_w, int64_t n, hc_shape_t s, void* z,
+             hc_stream_t stream) {
+    if (!X || !pre_mix || !norm_w || !z) return HC_ERR_NULL;
+    int st = check_shape_final(n, s);
+    if (st != HC_OK) return st;
+    if (!aligned16(X) || !aligned16(pre_mix) || !aligned16(norm_w) || !aligned16(z)) return HC_ERR_ALIGN;
+    const size_t N = static_cast<size_t>(n);
+    const void* ins[3] = {X, pre_mix, norm_w};
+    const size_t isz[3] = {N * kHC * s.d * 2, N * 16, static_cast<size_t>(s.d) * 4};
+    const void* outs[1] = {z};
+    const size_t osz[1] = {N * s.d * 2};
+    if (any_overlap(outs, osz, 1, ins, isz, 3)) return HC_ERR_ALIAS;
+    if (n == 0) return HC_OK;
+    FinalArgs a = {};
+    a.X = X;
+    a.pre_mix = pre_mix;
+    a.norm_w = norm_w;
+    a.z = z;
+    a.n = n;
+    a.d = s.d;
+    a.norm_eps = s.norm_eps;
+    return launch_status(launch_final(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int hc_post_then_final(const void* delta, const void* X, const float* post, const float* comb, const float* pre_mix,
+                       const float* norm_w, int64_t n, hc_shape_t s, void* X_out, void* z, hc_stream_t stream) {
+    if (!delta || !X || !post || !comb || !pre_mix || !norm_w || !z) return HC_ERR_NULL;
+    int st = check_shape_final(n, s);
+    if (st != HC_OK) return st;
+    const void* ptrs[7] = {delta, X, post, comb, pre_mix, norm_w, z};
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return HC_ERR_ALIGN;
+    if (X_out && !aligned16(X_out)) return HC_ERR_ALIGN;
+    const size_t N = static_cast<size_t>(n);
+    const size_t xb = N * kHC * s.d * 2, yb = N * s.d * 2;
+    const void* ins[6] = {delta, X, post, comb, pre_mix, norm_w};
+    const size_t isz[6] = {yb, xb, N * 16, N * 64, N * 16, static_cast<size_t>(s.d) * 4};
+    const void* outs[2] = {z, X_out};
+    const size_t osz[2] = {yb, xb};
+    if (any_overlap(outs, osz, 2, ins, isz, 6)) return HC_ERR_ALIAS;
+    if (n == 0) return HC_OK;
+    FinalArgs a = {};
+    a.X = X;
+    a.delta = delta;
+    a.post = post;
+    a.comb = comb;
+    a.pre_mix = pre_mix;
+    a.norm_w = norm_w;
+    a.X_out = X_out;
+    a.z = z;
+    a.n = n;
+    a.d = s.d;
+    a.norm_eps = s.norm_eps;
+    return launch_status(launch_final(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float* mixes, void* workspace,
                    hc_stream_t stream) {
     if (!X || !mixes || !p.hc_fn_planes || !workspace) return HC_ERR_NULL;
@@ -377,7 +493,7 @@ int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float*
     if (n == 0) return HC_OK;
     // the kernel reads scale/base/norm_w unconditionally: point them at the planes (never used)
     FusedArgs a = {};
-    a.post_mode = false;
+    a.mode = kModePre;
     a.X = X;
     a.planes = p.hc_fn_planes;
     a.hc_scale = static_cast<const float*>(p.hc_fn_planes);

@@ -10,7 +10,11 @@
 //   y        = bf16(sum_j pre_mix_j * X'_j)                            Block.hc_pre excerpt
 //   y_normed = bf16(norm_w * y / sqrt(mean(y^2) + norm_eps))           "Final RMSNorm" page,
 //                                                                      RMSNorm excerpt
-// In pre-step mode X' is the input X itself and nothing is written back to the streams.
+// In pre-step mode X' is the input X itself and nothing is written back to the streams. In expand
+// mode (the head of the stack, "Final RMSNorm" page, Transformer.forward excerpt) X' is the
+// embedding row h in every stream: h is loaded once per stage, serves as the MMA operand of all
+// four streams, is written four times to the streams, and the identity pre_mix (1/4 each)
+// collapses the four copies back to h exactly.
 //
 // Decomposition. A group of 8 CTAs owns a tile of up to 128 tokens; CTA `rank` of the group owns
 // d/8 columns of every stream, the 32-column chunks rank, rank+8, rank+16, ... (interleaved, so
@@ -309,11 +313,14 @@ __device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const flo
 
 // ---- the kernel ---------------------------------------------------------------------------------
 
-template <bool kPost>
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     hc_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmD,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmXo,
                     const FusedParams p) {
+    constexpr bool kPost = kMode == kModePost;
+    constexpr bool kExpand = kMode == kModeExpand;
+    constexpr bool kWriteX = kPost || kExpand;  // X' goes back to the streams
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     const uint32_t sbase = smem_u32(smem);
@@ -355,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpProducer && lane == 0) {
         tma_prefetch_desc(&tmX);
         tma_prefetch_desc(&tmB);
-        if (kPost) tma_prefetch_desc(&tmD);
+        if (kWriteX) tma_prefetch_desc(&tmD);
     }
     {
         float* nw = reinterpret_cast<float*>(smem + kOffNormW);
@@ -395,7 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float cpost[4] = {0.f, 0.f, 0.f, 0.f}, ccomb[16], pm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int i = 0; i < 16; ++i) ccomb[i] = 0.f;
-            if (valid) {
+            if (kExpand) {
+                pm[0] = pm[1] = pm[2] = pm[3] = 0.25f;  // identity pre_mix
+            } else if (valid) {
                 if (p.pre_mix) {
                     float4 v = __ldg(reinterpret_cast<const float4*>(p.pre_mix) + tok);
                     pm[0] = v.x; pm[1] = v.y; pm[2] = v.z; pm[3] = v.w;
@@ -454,8 +463,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t off = static_cast<uint32_t>(row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
                     float xr[4][8];
                     uint4 xv[4];
+                    if (kExpand) {
+                        xv[0] = ld_smem_v4(sb + kOffX + off);  // h, the same in every stream
+                        xv[1] = xv[0];
+                        xv[2] = xv[0];
+                        xv[3] = xv[0];
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) xv[j] = ld_smem_v4(sb + kOffX + j * kXTileBytes + off);
+                        for (int j = 0; j < 4; ++j) xv[j] = ld_smem_v4(sb + kOffX + j * kXTileBytes + off);
+                    }
                     if (kPost) {
                         float dl[8], xf[4][8];
                         unpack8(ld_smem_v4(sb + kOffD + off), dl);
@@ -586,7 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                          : HC_STREAM_POLICY == 2 ? policy_evict_last() : policy_evict_normal();
             pol_keep = policy_evict_last();
         }
-        const uint32_t bytes = static_cast<uint32_t>(4 * p.tile_m * 64 + (kPost ? p.tile_m * 64 : 0) + 4 * kBTileBytes);
+        const uint32_t bytes =
+            static_cast<uint32_t>((kExpand ? 1 : 4) * p.tile_m * 64 + (kPost ? p.tile_m * 64 : 0) + 4 * kBTileBytes);
         long long g = 0;
         for (long long it = 0; it < my_tiles; ++it) {
             const long long tile = cid + it * ncl;
@@ -600,8 +617,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb = bar(kBarFull + slot);
                     const int col = stage_col(s);
                     mbar_arrive_expect_tx(fb, bytes);
+                    if (kExpand) {
+                        tma_load_2d(sb + kOffX, &tmD, fb, col, t0, pol_stream);  // h into the stream-0 tile
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) tma_load_3d(sb + kOffX + j * kXTileBytes, &tmX, fb, col, j, t0, pol_stream);
+                        for (int j = 0; j < 4; ++j)
+                            tma_load_3d(sb + kOffX + j * kXTileBytes, &tmX, fb, col, j, t0, pol_stream);
+                    }
                     if (kPost) tma_load_2d(sb + kOffD, &tmD, fb, col, t0, pol_stream);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) tma_load_2d(sb + kOffB + k * kBTileBytes, &tmB, fb, k * p.d + col, 0, pol_keep);
@@ -631,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < 4; ++k) {
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
-                            const uint64_t ad = sdesc_kmajor_sw64(sb + kOffX + k * kXTileBytes + kk * 32);
+                            const uint64_t ad = sdesc_kmajor_sw64(sb + kOffX + (kExpand ? 0 : k * kXTileBytes) + kk * 32);
                             const uint64_t bd = sdesc_kmajor_sw64(sb + kOffB + k * kBTileBytes + kk * 32);
                             umma_bf16(dcol, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
                         }
@@ -648,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == kWarpStore) {
-        // ================= X' writer (post mode) and slot release ================================
+        // ================= X' writer (post and expand modes) and slot release ====================
         long long g = 0;
         for (long long it = 0; it < my_tiles; ++it) {
             const long long tile = cid + it * ncl;
@@ -656,11 +678,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < S; ++s, ++g) {
                 const int slot = static_cast<int>(g % kStages);
                 W.wait(bar(kBarXReady + slot), static_cast<uint32_t>((g / kStages) & 1), kErrStore);
-                if (kPost && lane == 0) {
+                if (kWriteX && lane == 0) {
                     const uint32_t sb = sbase + slot * kStageBytes;
                     const int col = stage_col(s);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) tma_store_3d(&tmXo, sb + kOffX + k * kXTileBytes, col, k, t0);
+                    for (int k = 0; k < 4; ++k)
+                        tma_store_3d(&tmXo, sb + kOffX + (kExpand ? 0 : k * kXTileBytes), col, k, t0);
                     bulk_commit();
                     bulk_wait_read<0>();
                 }
@@ -833,8 +856,9 @@ int prepare_device(int* groups) {
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DeviceState& st = g_dev[dev];
     if (!st.ready) {
-        const void* kernels[2] = {reinterpret_cast<const void*>(&hc_fused_kernel<false>),
-                                  reinterpret_cast<const void*>(&hc_fused_kernel<true>)};
+        const void* kernels[3] = {reinterpret_cast<const void*>(&hc_fused_kernel<kModePre>),
+                                  reinterpret_cast<const void*>(&hc_fused_kernel<kModePost>),
+                                  reinterpret_cast<const void*>(&hc_fused_kernel<kModeExpand>)};
         int per_sm = 1 << 30;
         for (const void* k : kernels) {
             if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
@@ -911,21 +935,25 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     if (num_tiles == 0) return 0;
 
     const uint64_t n = static_cast<uint64_t>(a.n), d = static_cast<uint64_t>(a.d);
+    // maps a mode does not use are encoded on a buffer of the right shape and never touched:
+    // tmX (streams read) on X, or on X_out in expand mode; tmXo (streams written) on X_out, or on X
+    // in pre mode; tmD ([n, d] rows read) on delta, on the embedding, or on X in pre mode
+    const bool write_x = a.mode != kModePre;
+    const void* x_in = a.mode == kModeExpand ? a.X_out : a.X;
+    const void* rows = a.mode == kModePost ? a.delta : a.mode == kModeExpand ? a.embed : a.X;
     CUtensorMap tmX, tmD, tmB, tmXo;
     {
         const uint64_t dims[3] = {d, 4, n};
         const uint64_t str[2] = {d * 2, 4 * d * 2};
         const uint32_t box[3] = {kChunk, 1, static_cast<uint32_t>(tile_m)};
-        if (!encode(&tmX, a.X, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B, HC_STREAM_PROMOTION)) return -7;
-        if (!encode(&tmXo, a.post_mode ? a.X_out : a.X, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+        if (!encode(&tmX, x_in, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B, HC_STREAM_PROMOTION)) return -7;
+        if (!encode(&tmXo, write_x ? a.X_out : a.X, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
     }
     {
         const uint64_t dims[2] = {d, n};
         const uint64_t str[1] = {d * 2};
         const uint32_t box[2] = {kChunk, static_cast<uint32_t>(tile_m)};
-        if (!encode(&tmD, a.post_mode ? a.delta : a.X, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B,
-                    HC_STREAM_PROMOTION))
-            return -7;
+        if (!encode(&tmD, rows, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B, HC_STREAM_PROMOTION)) return -7;
     }
     {
         const uint64_t dims[2] = {4 * d, static_cast<uint64_t>(kBRows)};
@@ -977,10 +1005,12 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e;
-    if (a.post_mode)
-        e = cudaLaunchKernelEx(&cfg, hc_fused_kernel<true>, tmX, tmD, tmB, tmXo, p);
+    if (a.mode == kModePost)
+        e = cudaLaunchKernelEx(&cfg, hc_fused_kernel<kModePost>, tmX, tmD, tmB, tmXo, p);
+    else if (a.mode == kModeExpand)
+        e = cudaLaunchKernelEx(&cfg, hc_fused_kernel<kModeExpand>, tmX, tmD, tmB, tmXo, p);
     else
-        e = cudaLaunchKernelEx(&cfg, hc_fused_kernel<false>, tmX, tmD, tmB, tmXo, p);
+        e = cudaLaunchKernelEx(&cfg, hc_fused_kernel<kModePre>, tmX, tmD, tmB, tmXo, p);
     return e == cudaSuccess ? 0 : -7;
 }
 

@@ -19,6 +19,8 @@ Distributions (per workload, see ``WORKLOADS``):
   hc_scale fp32 [3]          U(scale_lo, scale_hi)
   norm_w   fp32 [d]          1 + N(0, 0.1^2), rounded to a bf16 value (stored as fp32)
   w_diag   fp32 [d]          N(0, 0.5^2), the stand-in sublayer of the decode chain
+  embed    bf16 [n, d]       N(0,1): the embedding rows the head of the stack expands into streams
+  final_w  fp32 [d]          1 + N(0, 0.1^2) rounded to bf16: the final norm's gain
 bf16 values are drawn in float32 (float64 for Student-t), then rounded to nearest-even bf16.
 """
 
@@ -31,7 +33,7 @@ import numpy as np
 BLOCK = 1024
 
 # tensor ids, part of the seed
-T_X, T_DELTA, T_POST, T_COMB, T_PREMIX, T_FN, T_BASE, T_SCALE, T_NORMW, T_WDIAG = range(10)
+T_X, T_DELTA, T_POST, T_COMB, T_PREMIX, T_FN, T_BASE, T_SCALE, T_NORMW, T_WDIAG, T_EMBED, T_FINALW = range(12)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -111,6 +113,8 @@ def _draw_block(w: Workload, tensor: int, step: int, block: int, rows: int) -> n
         if w.delta_sd != 1.0:
             v *= np.float32(w.delta_sd)
         return f32_to_bf16_bits(v)
+    if tensor == T_EMBED:
+        return f32_to_bf16_bits(g.standard_normal((rows, d), dtype=np.float32))
     if tensor == T_POST:
         return (2.0 * _sigmoid(g.standard_normal((rows, hc)))).astype(np.float32)
     if tensor == T_COMB:
@@ -170,3 +174,9 @@ def small(name: str, B: int, T: int, d: int, seed: int = 77, **kw) -> Workload:
     """A reduced-size workload with the distributions of ``name`` (for fast parity tests)."""
     base = WORKLOADS[name]
     return dataclasses.replace(base, name="%s_small_b%d_t%d_d%d" % (name, B, T, d), seed=seed, B=B, T=T, d=d, **kw)
+
+
+def final_norm_w(w: Workload) -> np.ndarray:
+    """The final RMSNorm's gain [d] (one per stack)."""
+    nw = (1.0 + 0.1 * _rng(w.seed, 0, T_FINALW).standard_normal(w.d)).astype(np.float32)
+    return bf16_bits_to_f32(f32_to_bf16_bits(nw))

@@ -163,6 +163,46 @@ int hc_post_then_pre_noalloc(const void* delta, const void* X, const float* post
 int hc_post(const void* delta, const void* X, const float* post, const float* comb, int64_t n,
             hc_shape_t s, void* X_out, hc_stream_t stream);
 
+/* Head of the stack ("Final RMSNorm" page, Transformer.forward excerpt: the embedding row is copied
+ * into each of the hc streams and the first block reads them with the identity pre_mix), fused
+ * with the first sublayer's reading half:
+ *   X_out[t, j, :] = h[t, :] for every stream j
+ *   (y_normed, pre, post, comb) = hc_pre_step(X_out, identity pre_mix, p)
+ *   h      [device] bf16 [n, d]      the embedding rows
+ *   X_out  [device] bf16 [n, hc, d]  out: the expanded streams (the first sublayer's residual)
+ *   the other arguments as hc_pre_step.
+ * The pages do not print the identity pre_mix; this call weights every stream by 1/hc. Any
+ * weights summing to 1 collapse identical streams to h exactly, so the choice changes no output.
+ * h is read once and the streams are written once. Outputs and the workspace must not overlap
+ * each other or h (HC_ERR_ALIAS). Cooperative launch, as hc_pre_step. */
+int hc_expand_pre_step(const void* h, hc_params_t p, int64_t n, hc_shape_t s, void* X_out,
+                       void* y_normed, float* pre, float* post, float* comb, void* workspace,
+                       hc_stream_t stream);
+
+/* Tail of the stack ("Final RMSNorm" page: Transformer.forward excerpt, RMSNorm excerpt and the
+ * m_2 formula): after the last block the streams are collapsed once more with the last pre_mix
+ * and go through the final RMSNorm:
+ *   y = bf16(sum_j pre_mix_j * X_j)
+ *   z = bf16(norm_w * y / sqrt(mean(y^2) + s.norm_eps))     (the page's eps is 1e-20)
+ *   X       [device] bf16 [n, hc, d]   the streams after the last block
+ *   pre_mix [device] fp32 [n, hc]      the pre returned by the last reading half
+ *   norm_w  [device] fp32 [d]          the final norm's gain
+ *   z       [device] bf16 [n, d]       out
+ * s.sinkhorn_iters and s.hc_eps are ignored; d is a multiple of 8 and at most 5120. z must not
+ * overlap an input (HC_ERR_ALIAS). */
+int hc_final(const void* X, const float* pre_mix, const float* norm_w, int64_t n, hc_shape_t s,
+             void* z, hc_stream_t stream);
+
+/* The last sublayer's writing half fused with hc_final:
+ *   X' = bf16(post_k * delta + sum_j comb[j,k] * X_j), then z = hc_final(X', pre_mix, norm_w)
+ *   delta, X, post, comb as hc_post_then_pre; pre_mix, norm_w, z as hc_final.
+ *   X_out [device] bf16 [n, hc, d] or NULL: receives X' when given. The model reads the streams
+ *         no more after the final collapse, so NULL saves their 2*hc*d bytes per token of writes.
+ * Outputs must not overlap each other or any input (HC_ERR_ALIAS). Other rules as hc_final. */
+int hc_post_then_final(const void* delta, const void* X, const float* post, const float* comb,
+                       const float* pre_mix, const float* norm_w, int64_t n, hc_shape_t s,
+                       void* X_out, void* z, hc_stream_t stream);
+
 /* Diagnostic: the 24 mix numbers r * (X_flat . hc_fn^T) [device] fp32 [n, (2+hc)*hc] exactly as the
  * fused reading half computes them (same kernel, same tensor-core projection), for checking the
  * projection on its own. p.hc_scale, p.hc_base and p.norm_w are not read. */

@@ -228,3 +228,38 @@ def check_step(out, ref, m_gpu, m_ref, S, prm, iters, eps, label):
     assert_coef_close(pre_g, ref["pre"], label + " pre", bp)
     assert_coef_close(post_g, ref["post"], label + " post", bq)
     assert_coef_close(comb_g, ref["comb"], label + " comb", bc)
+
+
+# ---- sampled checks of a full-size step -----------------------------------------------------------
+
+def shape_of(w):
+    return hc.shape(d=w.d, sinkhorn_iters=w.iters, hc_eps=w.hc_eps, norm_eps=w.norm_eps)
+
+
+def sample_tokens(n, k, rng, tile=128):
+    """First and last tokens, tile edges, and k random tokens of n (sorted, unique)."""
+    idx = set(range(min(n, 8))) | set(range(max(0, n - 8), n))
+    for b in range(0, n, tile * 16):
+        idx.update([b, min(n - 1, b + tile - 1), min(n - 1, b + tile)])
+    idx.update(rng.choice(n, size=min(k, n), replace=False).tolist())
+    return np.array(sorted(idx), dtype=np.int64)
+
+
+def check_sampled(w, step, dev_in, out, prm, idx, post_mode, label):
+    """Oracle on the sampled tokens of one step, fed that step's device inputs (teacher-forced)."""
+    X = host_u16(dev_in["X"][idx])
+    pm = host_f32(dev_in["pre_mix"][idx]).astype(np.float32)
+    if post_mode:
+        delta = host_u16(dev_in["delta"][idx])
+        post = host_f32(dev_in["post"][idx]).astype(np.float32)
+        comb = host_f32(dev_in["comb"][idx]).astype(np.float32)
+        xo = host_u16(out["X_out"][idx])
+        check_xprime(xo, X, delta, post, comb, label + " X_out")
+        X = xo
+    ref = orc.hc_pre_step(X, pm, prm["hc_fn"], prm["hc_scale"], prm["hc_base"], prm["norm_w"], w.iters, w.hc_eps,
+                          w.norm_eps)
+    check_y_normed(host_u16(out["y_normed"][idx]), X, pm, prm["norm_w"], w.norm_eps, label + " y_normed")
+    sub = {k: out[k][idx] for k in ("pre", "post", "comb")}
+    P = DevParams(prm, w.d)
+    m_gpu = host_f32(debug_mixes(dev_bf16(X), P, shape_of(w), len(idx)))
+    check_step(sub, ref, m_gpu, ref["mixes"], ref["S"], prm, w.iters, w.hc_eps, label)

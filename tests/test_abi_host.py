@@ -136,6 +136,80 @@ def test_post_validation(lib):
     hc.hc_post(A[0], A[1], A[2], A[3], 0, s, A[1], 0)  # exactly in place is allowed; n == 0 no-op
 
 
+def test_expand_pre_step_validation(lib):
+    s = hc.shape()
+    st = 0
+    args = [A[0], _p(), 8, s, A[1], A[2], A[3], A[4], A[5], A[14], st]
+    for i in (0, 4, 5, 6, 7, 8, 9):
+        bad = list(args)
+        bad[i] = None
+        _expect(hc.HC_ERR_NULL, hc.hc_expand_pre_step, *bad)
+    bad = list(args)
+    bad[1] = hc.params(A[10], None, A[12], A[13])
+    _expect(hc.HC_ERR_NULL, hc.hc_expand_pre_step, *bad)
+    bad = list(args)
+    bad[4] = A[0] + 2048  # the streams written over the embedding
+    _expect(hc.HC_ERR_ALIAS, hc.hc_expand_pre_step, *bad)
+    bad = list(args)
+    bad[5] = A[1] + 512  # y_normed inside the streams
+    _expect(hc.HC_ERR_ALIAS, hc.hc_expand_pre_step, *bad)
+    bad = list(args)
+    bad[0] = A[0] + 2
+    _expect(hc.HC_ERR_ALIGN, hc.hc_expand_pre_step, *bad)
+    bad = list(args)
+    bad[3] = hc.shape(d=264)
+    _expect(hc.HC_ERR_SHAPE, hc.hc_expand_pre_step, *bad)
+    bad = list(args)
+    bad[3] = hc.shape(sinkhorn_iters=0)
+    _expect(hc.HC_ERR_ARG, hc.hc_expand_pre_step, *bad)
+    bad = list(args)
+    bad[2] = 0
+    hc.hc_expand_pre_step(*bad)
+
+
+def test_final_validation(lib):
+    s = hc.shape(norm_eps=1e-20)
+    st = 0
+    args = [A[0], A[1], A[2], 8, s, A[3], st]
+    for i in (0, 1, 2, 5):
+        bad = list(args)
+        bad[i] = None
+        _expect(hc.HC_ERR_NULL, hc.hc_final, *bad)
+    _expect(hc.HC_ERR_SHAPE, hc.hc_final, A[0], A[1], A[2], 8, hc.shape(d=12), A[3], st)
+    _expect(hc.HC_ERR_SHAPE, hc.hc_final, A[0], A[1], A[2], -1, s, A[3], st)
+    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_final, A[0], A[1], A[2], 8, hc.shape(d=5128), A[3], st)
+    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_final, A[0], A[1], A[2], 8, hc.shape(hc=8), A[3], st)
+    _expect(hc.HC_ERR_ARG, hc.hc_final, A[0], A[1], A[2], 8, hc.shape(norm_eps=float("inf")), A[3], st)
+    _expect(hc.HC_ERR_ALIGN, hc.hc_final, A[0], A[1], A[2] + 4, 8, s, A[3], st)
+    _expect(hc.HC_ERR_ALIAS, hc.hc_final, A[0], A[1], A[2], 8, s, A[0] + 16, st)
+    _expect(hc.HC_ERR_ALIAS, hc.hc_final, A[0], A[1], A[2], 8, s, A[2], st)
+    # the Sinkhorn fields are not used here: an invalid iteration count is accepted
+    hc.hc_final(A[0], A[1], A[2], 0, hc.shape(d=8, sinkhorn_iters=0, norm_eps=1e-20), A[3], st)
+
+
+def test_post_then_final_validation(lib):
+    s = hc.shape(norm_eps=1e-20)
+    st = 0
+    args = [A[0], A[1], A[2], A[3], A[4], A[5], 8, s, A[6], A[7], st]
+    for i in (0, 1, 2, 3, 4, 5, 9):
+        bad = list(args)
+        bad[i] = None
+        _expect(hc.HC_ERR_NULL, hc.hc_post_then_final, *bad)
+    bad = list(args)
+    bad[8] = A[1]  # X_out on X
+    _expect(hc.HC_ERR_ALIAS, hc.hc_post_then_final, *bad)
+    bad = list(args)
+    bad[9] = A[6] + 1024  # z inside X_out
+    _expect(hc.HC_ERR_ALIAS, hc.hc_post_then_final, *bad)
+    bad = list(args)
+    bad[8] = A[6] + 8
+    _expect(hc.HC_ERR_ALIGN, hc.hc_post_then_final, *bad)
+    bad = list(args)
+    bad[6] = 0
+    bad[8] = None  # X_out is optional
+    hc.hc_post_then_final(*bad)
+
+
 def test_plan_tiles(lib):
     for groups in (1, 7, 16, 18, 19):
         for n in [1, 2, 31, 32, 33, 64, 100, 127, 128, 129, 255, 256, 1000, 4096, 16384, 16385, 65536, 100003]:

@@ -145,8 +145,8 @@ def test_many_tiles_per_group_short_rows(d):
     s = _shape(w)
     dev = {k: (gu.dev_bf16(v) if v.dtype == np.uint16 else gu.dev_f32(v)) for k, v in inp.items()}
     out = gu.run_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, s, n)
-    idx = _sample(n, 600, np.random.default_rng(d))
-    _check_sampled(w, 0, dev, out, prm, idx, True, "short rows d=%d" % d)
+    idx = gu.sample_tokens(n, 600, np.random.default_rng(d))
+    gu.check_sampled(w, 0, dev, out, prm, idx, True, "short rows d=%d" % d)
     gu.device_error_clear()
 
 
@@ -234,34 +234,6 @@ def test_zero_tokens_is_a_noop():
 
 # ---- the five workloads ------------------------------------------------------------------------------
 
-def _sample(n, k, rng, tile=128):
-    idx = set(range(min(n, 8))) | set(range(max(0, n - 8), n))
-    for b in range(0, n, tile * 16):
-        idx.update([b, min(n - 1, b + tile - 1), min(n - 1, b + tile)])
-    idx.update(rng.choice(n, size=min(k, n), replace=False).tolist())
-    return np.array(sorted(idx), dtype=np.int64)
-
-
-def _check_sampled(w, step, dev_in, out, prm, idx, post_mode, label):
-    """Oracle on the sampled tokens of one step, fed that step's device inputs (teacher-forced)."""
-    X = gu.host_u16(dev_in["X"][idx])
-    pm = gu.host_f32(dev_in["pre_mix"][idx]).astype(np.float32)
-    if post_mode:
-        delta = gu.host_u16(dev_in["delta"][idx])
-        post = gu.host_f32(dev_in["post"][idx]).astype(np.float32)
-        comb = gu.host_f32(dev_in["comb"][idx]).astype(np.float32)
-        xo = gu.host_u16(out["X_out"][idx])
-        gu.check_xprime(xo, X, delta, post, comb, label + " X_out")
-        X = xo
-    ref = orc.hc_pre_step(X, pm, prm["hc_fn"], prm["hc_scale"], prm["hc_base"], prm["norm_w"], w.iters, w.hc_eps,
-                          w.norm_eps)
-    gu.check_y_normed(gu.host_u16(out["y_normed"][idx]), X, pm, prm["norm_w"], w.norm_eps, label + " y_normed")
-    sub = {k: out[k][idx] for k in ("pre", "post", "comb")}
-    P = gu.DevParams(prm, w.d)
-    m_gpu = gu.host_f32(gu.debug_mixes(gu.dev_bf16(X), P, _shape(w), len(idx)))
-    gu.check_step(sub, ref, m_gpu, ref["mixes"], ref["S"], prm, w.iters, w.hc_eps, label)
-
-
 def test_workload_step_b1_t64():
     w = synth.WORKLOADS["step_b1_t64"]
     inp = _inputs(w)
@@ -269,7 +241,7 @@ def test_workload_step_b1_t64():
     P = gu.DevParams(prm, w.d)
     dev = {k: (gu.dev_bf16(v) if v.dtype == np.uint16 else gu.dev_f32(v)) for k, v in inp.items()}
     out = gu.run_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, _shape(w), w.n)
-    _check_sampled(w, 0, dev, out, prm, np.arange(w.n), True, "step_b1_t64")
+    gu.check_sampled(w, 0, dev, out, prm, np.arange(w.n), True, "step_b1_t64")
     gu.device_error_clear()
 
 
@@ -280,8 +252,8 @@ def test_workload_prefill_b4_t4096():
     P = gu.DevParams(prm, w.d)
     dev = {k: (gu.dev_bf16(v) if v.dtype == np.uint16 else gu.dev_f32(v)) for k, v in inp.items()}
     out = gu.run_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, _shape(w), w.n)
-    idx = _sample(w.n, 384, np.random.default_rng(0))
-    _check_sampled(w, 0, dev, out, prm, idx, True, "prefill_b4_t4096")
+    idx = gu.sample_tokens(w.n, 384, np.random.default_rng(0))
+    gu.check_sampled(w, 0, dev, out, prm, idx, True, "prefill_b4_t4096")
     # properties on every token: X_out differs from X, y_normed finite, comb columns sum to 1
     comb = out["comb"]
     assert torch.isfinite(out["y_normed"].float()).all()
@@ -304,8 +276,8 @@ def _run_chain(w, sample_k, first_pre_step, fresh_delta):
         prm = synth.params(w, 0)
         P = gu.DevParams(prm, w.d)
         out = gu.run_pre_step(X, pre_mix, P, s, n)
-        idx = _sample(n, sample_k, rng)
-        _check_sampled(w, 0, dict(X=X, pre_mix=pre_mix), out, prm, idx, False, "%s step 0" % w.name)
+        idx = gu.sample_tokens(n, sample_k, rng)
+        gu.check_sampled(w, 0, dict(X=X, pre_mix=pre_mix), out, prm, idx, False, "%s step 0" % w.name)
         state = dict(X=X, post=out["post"], comb=out["comb"], pre_mix=out["pre"], y=out["y_normed"])
         start = 1
         wd = prm["w_diag"]
@@ -322,9 +294,9 @@ def _run_chain(w, sample_k, first_pre_step, fresh_delta):
         prm = synth.params(w, l)
         P = gu.DevParams(prm, w.d)
         out = gu.run_post_then_pre(delta, state["X"], state["post"], state["comb"], state["pre_mix"], P, s, n)
-        idx = _sample(n, sample_k, rng)
+        idx = gu.sample_tokens(n, sample_k, rng)
         dev_in = dict(X=state["X"], delta=delta, post=state["post"], comb=state["comb"], pre_mix=state["pre_mix"])
-        _check_sampled(w, l, dev_in, out, prm, idx, True, "%s step %d" % (w.name, l))
+        gu.check_sampled(w, l, dev_in, out, prm, idx, True, "%s step %d" % (w.name, l))
         state = dict(X=out["X_out"], post=out["post"], comb=out["comb"], pre_mix=out["pre"], y=out["y_normed"])
         wd = prm["w_diag"]
         worst = max(worst, float(state["X"].float().abs().max()))
