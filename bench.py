@@ -8,9 +8,12 @@ against the measured HBM copy bandwidth; `e2e` repeats the step through the same
 the inputs copied from pinned host memory and the results copied back inside the timed region;
 `cpu_baseline` times the CPU oracle (double precision) on this host's cores on a sample.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--op OP]
 Under torchrun every rank runs its own batch (weak scaling, no data-path collective).
 `--impl reference` times the CPU oracle itself as the reference arm.
+`--op` times another entry point on the same batch, against its own algorithmic bytes:
+post_then_pre (the default step), pre_step, expand_pre_step (head of the stack), post_then_final
+and final (tail of the stack, eps 1e-20), post (writing half alone).
 """
 
 from __future__ import annotations
@@ -32,8 +35,38 @@ WORKLOAD = "prefill_b4_t4096"
 BYTES_PER_TOKEN = 102592      # read X 40960 + delta 10240 + post 16 + comb 64 + pre_mix 16;
                               # write X' 40960 + y_normed 10240 + pre/post/comb 96
 PARAM_BYTES = 1986668         # hc_fn fp32 1966080 + norm_w 20480 + hc_base 96 + hc_scale 12
-FUSED_SOURCES = ["hyper_connection_residual_hc_gb300/csrc/hc_fused.cu", "hyper_connection_residual_hc_gb300/csrc/hc_ptx.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "hc_fused_prefill_b4_t4096_traffic.json")
+FINAL_EPS = 1e-20             # the final RMSNorm's eps ("Final RMSNorm" page)
+CSRC = "hyper_connection_residual_hc_gb300/csrc/"
+FUSED_SOURCES = [CSRC + "hc_fused.cu", CSRC + "hc_ptx.cuh"]
+FINAL_SOURCES = [CSRC + "hc_final.cu"]
+
+# Per entry point: algorithmic bytes per token and per call (parameters), the kernel it launches,
+# the sources that kernel is built from, and the ncu traffic summary of that kernel on this workload.
+OPS = {
+    "post_then_pre": dict(bytes_per_token=BYTES_PER_TOKEN, param_bytes=PARAM_BYTES, kernel="hc_fused_kernel<1>",
+                          sources=FUSED_SOURCES, traffic="hc_fused_prefill_b4_t4096_traffic.json"),
+    # read X 40960 + pre_mix 16; write y_normed 10240 + pre/post/comb 96
+    "pre_step": dict(bytes_per_token=51312, param_bytes=PARAM_BYTES, kernel="hc_fused_kernel<0>",
+                     sources=FUSED_SOURCES, traffic="hc_fused_pre_step_prefill_b4_t4096_traffic.json"),
+    # read h 10240; write X' 40960 + y_normed 10240 + pre/post/comb 96
+    "expand_pre_step": dict(bytes_per_token=61536, param_bytes=PARAM_BYTES, kernel="hc_fused_kernel<2>",
+                            sources=FUSED_SOURCES, traffic="hc_fused_expand_prefill_b4_t4096_traffic.json"),
+    # read X 40960 + delta 10240 + post 16 + comb 64 + pre_mix 16; write z 10240 (X' not written)
+    "post_then_final": dict(bytes_per_token=61536, param_bytes=20480, kernel="hc_final_kernel<true,false>",
+                            sources=FINAL_SOURCES, traffic="hc_final_post_then_final_prefill_b4_t4096_traffic.json"),
+    # read X 40960 + pre_mix 16; write z 10240
+    "final": dict(bytes_per_token=51216, param_bytes=20480, kernel="hc_final_kernel<false,false>",
+                  sources=FINAL_SOURCES, traffic="hc_final_final_prefill_b4_t4096_traffic.json"),
+    # read X 40960 + delta 10240 + post 16 + comb 64; write X' 40960
+    "post": dict(bytes_per_token=92240, param_bytes=0, kernel="hc_post_kernel", sources=[CSRC + "hc_api.cu"],
+                 traffic="hc_post_prefill_b4_t4096_traffic.json"),
+}
+
+
+def _metric(op):
+    if op == "post_then_pre":
+        return METRIC
+    return "HC %s tokens/s and achieved HBM GB/s vs peak, prefill B=4 T=4096" % op
 
 
 def _dist():
@@ -52,23 +85,24 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def _source_hash():
+def _source_hash(sources=FUSED_SOURCES):
     h = hashlib.sha256()
-    for rel in FUSED_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def _traffic_per_launch(n_tokens):
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary, scaled to this
+def _traffic_per_launch(n_tokens, op="post_then_pre"):
+    """DRAM bytes per launch of the op's kernel from the committed ncu summary, scaled to this
     launch's token count; None when absent or taken on another version of the kernel."""
+    spec = OPS[op]
     try:
-        with open(TRAFFIC_FILE) as f:
+        with open(os.path.join(ROOT, "profiles", spec["traffic"])) as f:
             t = json.load(f)
     except Exception:
         return None
-    if t.get("source_sha256_16") != _source_hash():
+    if t.get("source_sha256_16") != _source_hash(spec["sources"]):
         return None
     return float(t["dram_bytes_per_launch"]) * n_tokens / float(t["tokens"])
 
@@ -120,18 +154,44 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _oracle_sample_rate(w, tokens, threads):
-    """Oracle hc_post_then_pre on the first `tokens` tokens of the workload: tokens/s."""
+def _oracle_call(w, tokens, threads, op="post_then_pre"):
+    """A no-argument call of the oracle's version of the op on the first `tokens` tokens of the
+    workload, its inputs drawn beforehand."""
     import oracle as orc
     from hyper_connection_residual_hc_gb300 import synth
-    from hyper_connection_residual_hc_gb300.synth import T_COMB, T_DELTA, T_POST, T_PREMIX, T_X
+    from hyper_connection_residual_hc_gb300.synth import T_COMB, T_DELTA, T_EMBED, T_POST, T_PREMIX, T_X
     prm = synth.params(w, 0)
-    args = (synth.tokens(w, T_DELTA, 0, 0, tokens), synth.tokens(w, T_X, 0, 0, tokens),
-            synth.tokens(w, T_POST, 0, 0, tokens), synth.tokens(w, T_COMB, 0, 0, tokens),
-            synth.tokens(w, T_PREMIX, 0, 0, tokens))
+
+    def tk(t):
+        return synth.tokens(w, t, 0, 0, tokens)
+
+    coef = (prm["hc_fn"], prm["hc_scale"], prm["hc_base"], prm["norm_w"], w.iters, w.hc_eps, w.norm_eps)
+    if op == "post_then_pre":
+        args = (tk(T_DELTA), tk(T_X), tk(T_POST), tk(T_COMB), tk(T_PREMIX))
+        fn = lambda: orc.hc_post_then_pre(*args, *coef, threads=threads)  # noqa: E731
+    elif op == "pre_step":
+        args = (tk(T_X), tk(T_PREMIX))
+        fn = lambda: orc.hc_pre_step(*args, *coef, threads=threads)  # noqa: E731
+    elif op == "expand_pre_step":
+        h = tk(T_EMBED)
+        fn = lambda: orc.hc_expand_pre_step(h, *coef, threads=threads)  # noqa: E731
+    elif op == "post_then_final":
+        args = (tk(T_DELTA), tk(T_X), tk(T_POST), tk(T_COMB), tk(T_PREMIX), synth.final_norm_w(w))
+        fn = lambda: orc.hc_post_then_final(*args, FINAL_EPS, threads=threads)  # noqa: E731
+    elif op == "final":
+        args = (tk(T_X), tk(T_PREMIX), synth.final_norm_w(w))
+        fn = lambda: orc.hc_final(*args, FINAL_EPS, threads=threads)  # noqa: E731
+    else:
+        args = (tk(T_X), tk(T_DELTA), tk(T_POST), tk(T_COMB))
+        fn = lambda: orc.hc_post(*args, threads=threads)  # noqa: E731
+    return fn
+
+
+def _oracle_sample_rate(w, tokens, threads, op="post_then_pre"):
+    """The oracle's version of the op on the first `tokens` tokens: tokens/s (input drawing untimed)."""
+    fn = _oracle_call(w, tokens, threads, op)
     t0 = time.perf_counter()
-    orc.hc_post_then_pre(*args, prm["hc_fn"], prm["hc_scale"], prm["hc_base"], prm["norm_w"], w.iters, w.hc_eps,
-                         w.norm_eps, threads=threads)
+    fn()
     return tokens / (time.perf_counter() - t0)
 
 
@@ -145,20 +205,23 @@ def run_reference(args):
     w = synth.WORKLOADS[WORKLOAD]
     threads = orc.hardware_threads()
     # size each step so that warmup + steps take about two minutes at most
-    rate = _oracle_sample_rate(w, 2 * threads, threads)
+    op = args.op
+    rate = _oracle_sample_rate(w, 4 * threads, threads, op)
     per_step = max(threads, min(w.n, int(rate * 120.0 / max(1, args.steps + args.warmup))))
+    fn = _oracle_call(w, per_step, threads, op)  # the same sample every step, drawn once
     for _ in range(args.warmup):
-        _oracle_sample_rate(w, per_step, threads)
+        fn()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _oracle_sample_rate(w, per_step, threads)
+        fn()
     el = time.perf_counter() - t0
     value = per_step * args.steps / el
-    sample = "first %d of the %d tokens of %s per step (hc_post_then_pre, float64 oracle)" % (per_step, w.n, WORKLOAD)
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+    sample = "first %d of the %d tokens of %s per step (hc_%s, float64 oracle)" % (per_step, w.n, WORKLOAD, op)
+    line = {"impl": "reference", "metric": _metric(op), "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "tokens": w.n, "hc": w.hc, "d": w.d, "sinkhorn_iters": w.iters},
+            "config": {"workload": WORKLOAD, "entry_point": "hc_" + op, "tokens": w.n, "hc": w.hc, "d": w.d,
+                       "sinkhorn_iters": w.iters},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -171,8 +234,10 @@ def run_ours(args):
 
     import hyper_connection_residual_hc_gb300 as hc
     from hyper_connection_residual_hc_gb300 import synth
-    from hyper_connection_residual_hc_gb300.synth import T_COMB, T_DELTA, T_POST, T_PREMIX, T_X
+    from hyper_connection_residual_hc_gb300.synth import T_COMB, T_DELTA, T_EMBED, T_POST, T_PREMIX, T_X
 
+    op = args.op
+    spec = OPS[op]
     rank, world, local = _dist()
     torch.cuda.set_device(local)
     dist = None
@@ -193,9 +258,14 @@ def run_ours(args):
     def f32(a):
         return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
 
-    host = dict(delta=bf(synth.tokens(w, T_DELTA, 0)), X=bf(synth.tokens(w, T_X, 0)),
-                post=f32(synth.tokens(w, T_POST, 0)), comb=f32(synth.tokens(w, T_COMB, 0)),
-                pre_mix=f32(synth.tokens(w, T_PREMIX, 0)))
+    # per-token inputs of the op (copied host -> device every step of the e2e run)
+    names = {"post_then_pre": ("delta", "X", "post", "comb", "pre_mix"), "pre_step": ("X", "pre_mix"),
+             "expand_pre_step": ("h",), "post_then_final": ("delta", "X", "post", "comb", "pre_mix"),
+             "final": ("X", "pre_mix"), "post": ("delta", "X", "post", "comb")}[op]
+    draw = dict(delta=lambda: bf(synth.tokens(w, T_DELTA, 0)), X=lambda: bf(synth.tokens(w, T_X, 0)),
+                post=lambda: f32(synth.tokens(w, T_POST, 0)), comb=lambda: f32(synth.tokens(w, T_COMB, 0)),
+                pre_mix=lambda: f32(synth.tokens(w, T_PREMIX, 0)), h=lambda: bf(synth.tokens(w, T_EMBED, 0)))
+    host = {k: draw[k]() for k in names}
     dev = {k: v.cuda() for k, v in host.items()}
     hc_fn = f32(prm["hc_fn"]).cuda()
     planes = torch.empty(hc.hc_prepare_params_size(4, d) // 2, dtype=torch.bfloat16, device="cuda")
@@ -203,17 +273,42 @@ def run_ours(args):
     scale, base, nw = f32(prm["hc_scale"]).cuda(), f32(prm["hc_base"]).cuda(), f32(prm["norm_w"]).cuda()
     P = hc.params(planes, scale, base, nw)
     s = hc.shape(d=d, sinkhorn_iters=w.iters, hc_eps=w.hc_eps, norm_eps=w.norm_eps)
-    out = dict(X_out=torch.empty((n, 4, d), dtype=torch.bfloat16, device="cuda"),
-               y_normed=torch.empty((n, d), dtype=torch.bfloat16, device="cuda"),
-               pre=torch.empty((n, 4), dtype=torch.float32, device="cuda"),
-               post=torch.empty((n, 4), dtype=torch.float32, device="cuda"),
-               comb=torch.empty((n, 4, 4), dtype=torch.float32, device="cuda"))
+    sf = hc.shape(d=d, norm_eps=FINAL_EPS)
+    fw = f32(synth.final_norm_w(w)).cuda()
+
+    def empty(*shape, dt=torch.bfloat16):
+        return torch.empty(shape, dtype=dt, device="cuda")
+
+    coef = lambda: dict(pre=empty(n, 4, dt=torch.float32), post=empty(n, 4, dt=torch.float32),  # noqa: E731
+                        comb=empty(n, 4, 4, dt=torch.float32))
+    if op in ("post_then_pre", "expand_pre_step"):
+        out = dict(X_out=empty(n, 4, d), y_normed=empty(n, d), **coef())
+    elif op == "pre_step":
+        out = dict(y_normed=empty(n, d), **coef())
+    elif op in ("post_then_final", "final"):
+        out = dict(z=empty(n, d))
+    else:
+        out = dict(X_out=empty(n, 4, d))
     stream = torch.cuda.current_stream()
     ws = hc.new_workspace()
 
     def step():
-        hc.hc_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, n, s, out["X_out"],
-                            out["y_normed"], out["pre"], out["post"], out["comb"], ws, stream)
+        if op == "post_then_pre":
+            hc.hc_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, n, s,
+                                out["X_out"], out["y_normed"], out["pre"], out["post"], out["comb"], ws, stream)
+        elif op == "pre_step":
+            hc.hc_pre_step(dev["X"], dev["pre_mix"], P, n, s, out["y_normed"], out["pre"], out["post"], out["comb"],
+                           ws, stream)
+        elif op == "expand_pre_step":
+            hc.hc_expand_pre_step(dev["h"], P, n, s, out["X_out"], out["y_normed"], out["pre"], out["post"],
+                                  out["comb"], ws, stream)
+        elif op == "post_then_final":
+            hc.hc_post_then_final(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], fw, n, sf, None,
+                                  out["z"], stream)
+        elif op == "final":
+            hc.hc_final(dev["X"], dev["pre_mix"], fw, n, sf, out["z"], stream)
+        else:
+            hc.hc_post(dev["delta"], dev["X"], dev["post"], dev["comb"], n, s, out["X_out"], stream)
 
     def barrier():
         torch.cuda.synchronize()
@@ -279,7 +374,7 @@ def run_ours(args):
     tokens_total = n * world
     value = tokens_total * args.steps / (el_ms / 1e3)
     peak, peak_kind = _peaks()
-    alg_bytes = n * BYTES_PER_TOKEN + PARAM_BYTES
+    alg_bytes = n * spec["bytes_per_token"] + spec["param_bytes"]
     achieved = alg_bytes / (kern_ms / 1e3) / 1e9
     groups = hc.hc_fused_groups()
     tile_m, tiles = hc.hc_plan_tiles(n, groups)
@@ -288,28 +383,28 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle as orc
         threads = orc.hardware_threads()
-        r0 = _oracle_sample_rate(w, 2 * threads, threads)
+        r0 = _oracle_sample_rate(w, 2 * threads, threads, op)
         sample_tokens = int(max(threads, min(n, r0 * 15.0)))  # about 15 s of wall time at most
-        rate = _oracle_sample_rate(w, sample_tokens, threads)
+        rate = _oracle_sample_rate(w, sample_tokens, threads, op)
         cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": "hc_post_then_pre on the first %d of the %d tokens of %s, float64 oracle, %d threads"
-                         % (sample_tokens, n, WORKLOAD, threads)}
+               "sample": "hc_%s on the first %d of the %d tokens of %s, float64 oracle, %d threads"
+                         % (op, sample_tokens, n, WORKLOAD, threads)}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "metric": _metric(op), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": el_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "tokens_per_gpu": n, "B": w.B, "T": w.T, "hc": w.hc, "d": d,
+            "config": {"workload": WORKLOAD, "entry_point": "hc_" + op, "tokens_per_gpu": n, "B": w.B, "T": w.T, "hc": w.hc, "d": d,
                        "sinkhorn_iters": w.iters, "hc_eps": w.hc_eps, "norm_eps": w.norm_eps,
                        "stream_dtype": "bf16", "coefficient_dtype": "f32",
-                       "l2": "no flush: every step reads 839 MB of inputs and writes 839 MB, far above the 129 MB L2",
+                       "l2": "no flush: every step moves %d MB, far above the 129 MB L2" % (alg_bytes // 10 ** 6),
                        "tile_tokens": tile_m, "tiles": tiles, "groups_of_8_ctas": groups,
                        "hbm_gb_per_s": alg_bytes * args.steps / (el_ms / 1e3) / 1e9},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": _traffic_per_launch(n), "algorithmic_bytes": alg_bytes,
-                         "kernel": "hc_fused_kernel<true>", "kernel_ms": kern_ms},
+                         "traffic": _traffic_per_launch(n, op), "algorithmic_bytes": alg_bytes,
+                         "kernel": spec["kernel"], "kernel_ms": kern_ms},
             "cpu_baseline": cpu,
             "e2e": {"value": tokens_total * e2e_steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
@@ -331,6 +426,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="post_then_pre", choices=sorted(OPS))
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

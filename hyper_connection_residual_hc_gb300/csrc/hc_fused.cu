@@ -187,9 +187,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
-    f[0] = bf_lo(v.x); f[1] = bf_hi(v.x); f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
-    f[4] = bf_lo(v.z); f[5] = bf_hi(v.z); f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
+// Pairs of adjacent columns travel as float2 through the packed fp32 instructions of sm_100+
+// (__ffma2_rn and friends: two independent IEEE operations per instruction, each lane rounded
+// exactly like its scalar counterpart).
+__device__ __forceinline__ float2 bf2(uint32_t u) { return make_float2(bf_lo(u), bf_hi(u)); }
+__device__ __forceinline__ uint32_t pack_bf16(float2 v) { return pack_bf16(v.x, v.y); }
+__device__ __forceinline__ float2 bcast(float a) { return make_float2(a, a); }
+
+__device__ __forceinline__ void unpack4(const uint4& v, float2 (&f)[4]) {
+    f[0] = bf2(v.x); f[1] = bf2(v.y); f[2] = bf2(v.z); f[3] = bf2(v.w);
 }
 
 // Bounded mbarrier wait shared by all roles of one CTA.
@@ -399,31 +405,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long t0 = tile * p.tile_m;
             const long long tok = t0 + row;
             const bool valid = (row < p.tile_m) && (tok < p.n);
-            float cpost[4] = {0.f, 0.f, 0.f, 0.f}, ccomb[16], pm[4] = {0.f, 0.f, 0.f, 0.f};
+            // this token's coefficients, each broadcast to both lanes of a float2
+            float2 cpost[4], ccomb[16], pm[4];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) ccomb[i] = 0.f;
+            for (int i = 0; i < 4; ++i) cpost[i] = pm[i] = bcast(0.f);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ccomb[i] = bcast(0.f);
             if (kExpand) {
-                pm[0] = pm[1] = pm[2] = pm[3] = 0.25f;  // identity pre_mix
+                pm[0] = pm[1] = pm[2] = pm[3] = bcast(0.25f);  // identity pre_mix
             } else if (valid) {
                 if (p.pre_mix) {
                     float4 v = __ldg(reinterpret_cast<const float4*>(p.pre_mix) + tok);
-                    pm[0] = v.x; pm[1] = v.y; pm[2] = v.z; pm[3] = v.w;
+                    pm[0] = bcast(v.x); pm[1] = bcast(v.y); pm[2] = bcast(v.z); pm[3] = bcast(v.w);
                 }
                 if (kPost) {
                     float4 v = __ldg(reinterpret_cast<const float4*>(p.post) + tok);
-                    cpost[0] = v.x; cpost[1] = v.y; cpost[2] = v.z; cpost[3] = v.w;
+                    cpost[0] = bcast(v.x); cpost[1] = bcast(v.y); cpost[2] = bcast(v.z); cpost[3] = bcast(v.w);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         float4 c = __ldg(reinterpret_cast<const float4*>(p.comb) + tok * 4 + j);
-                        ccomb[4 * j] = c.x; ccomb[4 * j + 1] = c.y; ccomb[4 * j + 2] = c.z; ccomb[4 * j + 3] = c.w;
+                        ccomb[4 * j] = bcast(c.x); ccomb[4 * j + 1] = bcast(c.y);
+                        ccomb[4 * j + 2] = bcast(c.z); ccomb[4 * j + 3] = bcast(c.w);
                     }
                 }
             }
-            float acc[12];
+            float2 acc[6];  // the 12 mixes of this thread's column half, in pairs
 #pragma unroll
-            for (int i = 0; i < 12; ++i) acc[i] = 0.f;
-            float sx[4] = {0.f, 0.f, 0.f, 0.f};
-            float sy[2] = {0.f, 0.f};
+            for (int i = 0; i < 6; ++i) acc[i] = bcast(0.f);
+            float2 sx[4], sy[2];  // sums of squares, each split over the two lanes
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sx[i] = bcast(0.f);
+            sy[0] = sy[1] = bcast(0.f);
 
             auto drain = [&](long long gd) {
                 W.wait(bar(kBarAccFull), static_cast<uint32_t>(gd & 1), kErrComputeAcc);
@@ -431,22 +443,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[36];
                 const uint32_t col = kAccCol + 36u * h;
                 tmem_ld36_wait(tl + col, tl + col + 32u, v);
+                auto f2 = [&](int i) { return make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])); };
 #pragma unroll
-                for (int i = 0; i < 12; ++i)
-                    acc[i] += (__uint_as_float(v[i]) + __uint_as_float(v[12 + i])) + __uint_as_float(v[24 + i]);
+                for (int i = 0; i < 6; ++i)
+                    acc[i] = __fadd2_rn(acc[i], __fadd2_rn(__fadd2_rn(f2(2 * i), f2(12 + 2 * i)), f2(24 + 2 * i)));
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarAccEmpty));
             };
 
             for (int s = 0; s < S; ++s, ++g) {
-                if (s > 0) {
-                    // the y store of the previous stage has had a stage to complete: hand it over,
-                    // then drain the previous accumulator (its MMA ran meanwhile), so that the MMA
-                    // of this stage can be issued the moment its X' is ready
-                    y_ready(g - 1);
-                    drain(g - 1);
-                }
+                // the y store of the previous stage has had a stage to complete: hand it over
+                if (s > 0) y_ready(g - 1);
                 // the ring slot of this stage's y last held the chunk of stage g - kRing
                 const long long yround = g / kRing;
                 if (yround > 0)
@@ -461,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int cc = 0; cc < 2; ++cc) {
                     const int c = 2 * h + cc;
                     const uint32_t off = static_cast<uint32_t>(row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
-                    float xr[4][8];
+                    float2 xr[4][4];  // X' of the 8 columns, 4 pairs per stream
                     uint4 xv[4];
                     if (kExpand) {
                         xv[0] = ld_smem_v4(sb + kOffX + off);  // h, the same in every stream
@@ -473,60 +481,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 4; ++j) xv[j] = ld_smem_v4(sb + kOffX + j * kXTileBytes + off);
                     }
                     if (kPost) {
-                        float dl[8], xf[4][8];
-                        unpack8(ld_smem_v4(sb + kOffD + off), dl);
+                        // X'_k = post_k * Delta + sum_j comb[j,k] X_j, in this order for every column
+                        float2 dl[4], xf[4][4];
+                        unpack4(ld_smem_v4(sb + kOffD + off), dl);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) unpack8(xv[j], xf[j]);
+                        for (int j = 0; j < 4; ++j) unpack4(xv[j], xf[j]);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            float o[8];
+                            uint32_t o[4];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                float t = cpost[k] * dl[e];
-                                t = fmaf(ccomb[0 * 4 + k], xf[0][e], t);
-                                t = fmaf(ccomb[1 * 4 + k], xf[1][e], t);
-                                t = fmaf(ccomb[2 * 4 + k], xf[2][e], t);
-                                t = fmaf(ccomb[3 * 4 + k], xf[3][e], t);
-                                o[e] = t;
+                            for (int e = 0; e < 4; ++e) {
+                                float2 t = __fmul2_rn(cpost[k], dl[e]);
+                                t = __ffma2_rn(ccomb[0 * 4 + k], xf[0][e], t);
+                                t = __ffma2_rn(ccomb[1 * 4 + k], xf[1][e], t);
+                                t = __ffma2_rn(ccomb[2 * 4 + k], xf[2][e], t);
+                                t = __ffma2_rn(ccomb[3 * 4 + k], xf[3][e], t);
+                                o[e] = pack_bf16(t);
                             }
-                            uint4 ov;
-                            ov.x = pack_bf16(o[0], o[1]);
-                            ov.y = pack_bf16(o[2], o[3]);
-                            ov.z = pack_bf16(o[4], o[5]);
-                            ov.w = pack_bf16(o[6], o[7]);
+                            const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
                             st_smem_v4(sb + kOffX + k * kXTileBytes + off, ov);
-                            unpack8(ov, xr[k]);
+                            unpack4(ov, xr[k]);
                         }
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) unpack8(xv[j], xr[j]);
+                        for (int j = 0; j < 4; ++j) unpack4(xv[j], xr[j]);
                     }
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) sx[k] = fmaf(xr[k][e], xr[k][e], sx[k]);
-                    float yv[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        float t = pm[0] * xr[0][e];
-                        t = fmaf(pm[1], xr[1][e], t);
-                        t = fmaf(pm[2], xr[2][e], t);
-                        t = fmaf(pm[3], xr[3][e], t);
-                        yv[e] = t;
-                    }
+                        for (int e = 0; e < 4; ++e) sx[k] = __ffma2_rn(xr[k][e], xr[k][e], sx[k]);
+                    // y = sum_j pre_mix_j X'_j, rounded to bf16; its squares summed from the rounded values
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const uint32_t u = pack_bf16(yv[2 * e], yv[2 * e + 1]);
+                        float2 t = __fmul2_rn(pm[0], xr[0][e]);
+                        t = __ffma2_rn(pm[1], xr[1][e], t);
+                        t = __ffma2_rn(pm[2], xr[2][e], t);
+                        t = __ffma2_rn(pm[3], xr[3][e], t);
+                        const uint32_t u = pack_bf16(t);
                         yb[cc * 4 + e] = u;
-                        const float a0 = bf_lo(u), a1 = bf_hi(u);
-                        sy[cc] = fmaf(a0, a0, sy[cc]);
-                        sy[cc] = fmaf(a1, a1, sy[cc]);
+                        const float2 a = bf2(u);
+                        sy[cc] = __ffma2_rn(a, a, sy[cc]);
                     }
                 }
                 tmem_st8(tl + kYCol + static_cast<uint32_t>((g % kRing) * 16 + h * 8), yb);
                 if (kPost) fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarXReady + slot));
+                // drain the previous stage's accumulator now: its MMA ran while this stage was
+                // computed, so nothing waits here, and the MMA of this stage (which needs the
+                // accumulator empty) is issued right after
+                if (s > 0) drain(g - 1);
             }
             drain(g - 1);
             y_ready(g - 1);
@@ -541,12 +545,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* P = p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kGroup + rank) * kPartFloats;
             {
                 float4* pm4 = reinterpret_cast<float4*>(P + row * kMix + 12 * h);
-                pm4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                pm4[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-                pm4[2] = make_float4(acc[8], acc[9], acc[10], acc[11]);
+                pm4[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+                pm4[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+                pm4[2] = make_float4(acc[4].x, acc[4].y, acc[5].x, acc[5].y);
             }
-            P[kPartSx + h * kTileMax + row] = (sx[0] + sx[1]) + (sx[2] + sx[3]);
-            P[kPartSy + h * kTileMax + row] = sy[0] + sy[1];
+            const float2 sxx = __fadd2_rn(__fadd2_rn(sx[0], sx[1]), __fadd2_rn(sx[2], sx[3]));
+            const float2 syy = __fadd2_rn(sy[0], sy[1]);
+            P[kPartSx + h * kTileMax + row] = sxx.x + sxx.y;
+            P[kPartSy + h * kTileMax + row] = syy.x + syy.y;
             // hand the block to the split warp, which publishes it; no waiting here
             named_bar_arrive(kBarIdPublish, (kComputeWarps + 1) * 32);
         }
@@ -575,15 +581,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarYFree + ys));
                 if (store) {
-                    // TMEM columns ys*16 + 0..7 hold stage columns 0..15 (half 0), + 8..15 hold 16..31
-                    const float* w = nw + s * 32;
+                    // TMEM columns ys*16 + 0..7 hold stage columns 0..15 (half 0), + 8..15 hold 16..31;
+                    // y_normed = norm_w * (y * r_y), two columns per instruction
+                    const float2* w = reinterpret_cast<const float2*>(nw + s * 32);
+                    const float2 ry2 = bcast(ry);
                     uint32_t ov[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float a0 = w[2 * e] * (bf_lo(yv[e]) * ry);
-                        const float a1 = w[2 * e + 1] * (bf_hi(yv[e]) * ry);
-                        ov[e] = pack_bf16(a0, a1);
-                    }
+                    for (int e = 0; e < 16; ++e) ov[e] = pack_bf16(__fmul2_rn(w[e], __fmul2_rn(bf2(yv[e]), ry2)));
                     uint4* dst = reinterpret_cast<uint4*>(yrow + stage_col(s));
                     dst[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
                     dst[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
