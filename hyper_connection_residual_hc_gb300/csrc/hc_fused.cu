@@ -106,10 +106,15 @@ constexpr int kSmemUsed = kOffAbort + 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
 
 // global workspace: partial sums [group][tile parity][rank][28][128] fp32, then one 64-bit flag
-// per [group][tile parity][rank]
+// per [group][tile parity][rank], then one 64-bit launch counter per group. A flag holds
+// (launch number of its group) << 32 | (tile index + 1); the launch number is the group's counter
+// + 1, read by every CTA of the group when it starts and stored back by the group's rank-0 CTA
+// after its last exchange, when all 8 have read it. The tags therefore come from the device: a
+// launch replayed from a CUDA graph tags its flags afresh, and a zero-filled workspace holds no tag.
 constexpr size_t kWsPartBytes = static_cast<size_t>(kMaxGroups) * 2 * kGroup * kPartFloats * 4;
 constexpr size_t kWsFlagBytes = static_cast<size_t>(kMaxGroups) * 2 * kGroup * 8;
-constexpr size_t kWorkspaceBytes = kWsPartBytes + kWsFlagBytes;
+constexpr size_t kWsCounterBytes = static_cast<size_t>(kMaxGroups) * 8;
+constexpr size_t kWorkspaceBytes = kWsPartBytes + kWsFlagBytes + kWsCounterBytes;
 
 static_assert(kWarpEpi0 + 4 == kThreads / 32 && kWarpEpi0 % 4 == 0, "one epilogue warp per TMEM lane quadrant");
 static_assert(kWarpSplit + 1 == kWarpEpi0, "warp roles: 8 compute, producer, MMA, store, split, 4 epilogue");
@@ -160,7 +165,7 @@ struct FusedParams {
     void* y_normed;
     float* ws_part;                 // workspace partial-sum blocks
     unsigned long long* ws_flags;   // workspace flags
-    unsigned long long epoch_base;  // (launch id) << 32; tile `it` publishes epoch_base + it + 1
+    unsigned long long* ws_launch;  // workspace launch counters, one per group
     long long n;
     long long num_tiles;
     int write_y;
@@ -704,13 +709,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kMix; ++i) bs[i] = __ldg(p.hc_base + i);
         float* ry_s = reinterpret_cast<float*>(smem + kOffRy);
+        // this launch's number for the group: its counter + 1 (never 0, which a fresh workspace holds)
+        unsigned long long launch_no = 0;
+        if (lane == 0) launch_no = ld_acquire_gpu_u64(p.ws_launch + cid) + 1ull;
+        launch_no = __shfl_sync(0xffffffffu, launch_no, 0);
+        const unsigned long long epoch_base = launch_no << 32;
         for (long long it = 0; it < my_tiles; ++it) {
             const int buf = static_cast<int>(it & 1);
             // the compute warps have written this CTA's block of the tile: publish it, then wait for
             // the group (lanes 0..7 poll one flag each)
             named_bar_sync(kBarIdPublish, (kComputeWarps + 1) * 32);
             unsigned long long* flg = p.ws_flags + static_cast<size_t>(cid * 2 + buf) * kGroup;
-            const unsigned long long epoch = p.epoch_base + static_cast<unsigned long long>(it) + 1ull;
+            const unsigned long long epoch = epoch_base + static_cast<unsigned long long>(it) + 1ull;
             if (lane == 0) {
                 fence_acq_rel_gpu();  // after the barrier: the compute threads' block writes come first
                 st_release_gpu_u64(flg + rank, epoch);
@@ -802,6 +812,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         }
+        // every CTA of the group has read the counter (each published a flag of the last tile,
+        // which this warp has seen): advance it for the group's next launch
+        if (rank == 0 && lane == 0 && my_tiles > 0) st_release_gpu_u64(p.ws_launch + cid, launch_no);
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -852,7 +866,6 @@ struct DeviceState {
 constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
-unsigned int g_launch_id = 0;  // numbers the fused launches of this process (flag epochs)
 
 int prepare_device(int* groups) {
     int dev = 0;
@@ -980,12 +993,8 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     p.y_normed = a.y_normed;
     p.ws_part = reinterpret_cast<float*>(a.workspace);
     p.ws_flags = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(a.workspace) + kWsPartBytes);
-    {
-        std::lock_guard<std::mutex> lk(g_dev_mu);
-        ++g_launch_id;
-        if (g_launch_id == 0) ++g_launch_id;  // 0 is what a zeroed workspace holds
-        p.epoch_base = static_cast<unsigned long long>(g_launch_id) << 32;
-    }
+    p.ws_launch =
+        reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(a.workspace) + kWsPartBytes + kWsFlagBytes);
     p.n = a.n;
     p.num_tiles = num_tiles;
     p.write_y = a.y_normed != nullptr;
@@ -1021,7 +1030,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
 // ---- scratch that needs no allocation ------------------------------------------------------------
 // The workspace of hc_post_then_pre_noalloc: a fixed array in the library's device image, one per
 // GPU that loads the library, zero at load and kept until the process exits. Its size is the same
-// kWorkspaceBytes (7,344,128 bytes: room for 32 groups of 8 CTAs) that hc_workspace_size reports.
+// kWorkspaceBytes (7,344,384 bytes: room for 32 groups of 8 CTAs) that hc_workspace_size reports.
 static __device__ __align__(256) unsigned char g_noalloc_workspace[kWorkspaceBytes];
 
 namespace {

@@ -94,11 +94,13 @@ int hc_prepare_params_size(int hc, int d, size_t* bytes);
  * No counterpart on the pages: it is this library's weight packing. hc must be 4. */
 int hc_prepare_params(const float* hc_fn, int hc, int d, void* planes, hc_stream_t stream);
 
-/* Size in bytes of the workspace the fused calls (hc_pre_step, hc_post_then_pre, hc_debug_mixes)
- * need: the 8 CTAs that share a token tile exchange their per-token partial sums through it
- * (about 14 KB per CTA per tile, L2-resident) together with one 64-bit flag per CTA and tile
- * parity. The caller allocates it once [device], 16-byte aligned, fills it with zeros before its
- * first use and then keeps passing it unchanged (no re-zeroing needed). Calls that may run at
+/* Size in bytes of the workspace the fused calls (hc_pre_step, hc_post_then_pre,
+ * hc_expand_pre_step, hc_debug_mixes) need: the 8 CTAs that share a token tile exchange their
+ * per-token partial sums through it (about 14 KB per CTA per tile, L2-resident) together with one
+ * 64-bit flag per CTA and tile parity, and one 64-bit launch counter per group of 8 CTAs that tags
+ * the flags of each launch (kept on the device, so launches replayed from a CUDA graph are tagged
+ * afresh too). The caller allocates it once [device], 16-byte aligned, fills it with zeros before
+ * its first use and then keeps passing it unchanged (no re-zeroing needed). Calls that may run at
  * the same time on the GPU must not share a workspace. Host-only, no CUDA call. */
 int hc_workspace_size(size_t* bytes);
 
@@ -139,7 +141,7 @@ int hc_post_then_pre(const void* delta, const void* X, const float* post, const 
  * engine that owns all device memory and hands it no workspace, a runtime whose memory plan is
  * frozen after start-up, or a program that must not risk an allocation failing mid-run. This
  * entry point takes the same arguments as hc_post_then_pre minus the workspace, and computes the
- * same results: its scratch is a fixed array inside the library's device image, 7,344,128 bytes
+ * same results: its scratch is a fixed array inside the library's device image, 7,344,384 bytes
  * (the hc_workspace_size figure), which every GPU that loads the library keeps until the process
  * exits. It allocates nothing and calls no allocating routine.
  *   - The first call on a device looks up that device's copy of the array (a runtime query, no

@@ -69,7 +69,8 @@ def _expect(status, fn, *args):
 
 
 def test_workspace_size(lib):
-    assert hc.hc_workspace_size() == 32 * 2 * 8 * 28 * 128 * 4 + 32 * 2 * 8 * 8
+    # partial sums [32 groups][2 parities][8 CTAs][28][128] fp32, flags [32][2][8] u64, counters [32] u64
+    assert hc.hc_workspace_size() == 32 * 2 * 8 * 28 * 128 * 4 + 32 * 2 * 8 * 8 + 32 * 8
 
 
 def test_pre_step_validation(lib):
