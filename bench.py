@@ -376,8 +376,8 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     alg_bytes = n * spec["bytes_per_token"] + spec["param_bytes"]
     achieved = alg_bytes / (kern_ms / 1e3) / 1e9
-    groups = hc.hc_fused_groups()
-    tile_m, tiles = hc.hc_plan_tiles(n, groups)
+    ctas = hc.hc_fused_ctas()
+    group, tile_m, tiles = hc.hc_plan_tiles(n, d, ctas)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -399,7 +399,7 @@ def run_ours(args):
                        "sinkhorn_iters": w.iters, "hc_eps": w.hc_eps, "norm_eps": w.norm_eps,
                        "stream_dtype": "bf16", "coefficient_dtype": "f32",
                        "l2": "no flush: every step moves %d MB, far above the 129 MB L2" % (alg_bytes // 10 ** 6),
-                       "tile_tokens": tile_m, "tiles": tiles, "groups_of_8_ctas": groups,
+                       "tile_tokens": tile_m, "tiles": tiles, "ctas_per_tile": group, "resident_ctas": ctas,
                        "hbm_gb_per_s": alg_bytes * args.steps / (el_ms / 1e3) / 1e9},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,

@@ -32,7 +32,7 @@ HC_ERR_DEVICE = -8
 SYMBOLS = (
     "hc_prepare_params_size", "hc_prepare_params", "hc_workspace_size", "hc_pre_step", "hc_post_then_pre",
     "hc_post_then_pre_noalloc", "hc_post", "hc_expand_pre_step", "hc_final", "hc_post_then_final", "hc_debug_mixes",
-    "hc_plan_tiles", "hc_fused_groups", "hc_device_error", "hc_status_string",
+    "hc_plan_tiles", "hc_fused_ctas", "hc_device_error", "hc_status_string",
 )
 
 
@@ -76,8 +76,8 @@ def load(path: str = LIB_PATH):
     lib.hc_final.argtypes = [P, P, P, I64, hc_shape_t, P, P]
     lib.hc_post_then_final.argtypes = [P, P, P, P, P, P, I64, hc_shape_t, P, P, P]
     lib.hc_debug_mixes.argtypes = [P, hc_params_t, I64, hc_shape_t, P, P, P]
-    lib.hc_plan_tiles.argtypes = [I64, I, ctypes.POINTER(I), ctypes.POINTER(I64)]
-    lib.hc_fused_groups.argtypes = [ctypes.POINTER(I)]
+    lib.hc_plan_tiles.argtypes = [I64, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I64)]
+    lib.hc_fused_ctas.argtypes = [ctypes.POINTER(I)]
     lib.hc_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), I, P]
     lib.hc_status_string.argtypes = [I]
     lib.hc_status_string.restype = ctypes.c_char_p
@@ -195,16 +195,18 @@ def hc_debug_mixes(X, p: hc_params_t, n: int, s: hc_shape_t, mixes, workspace, s
     _check("hc_debug_mixes", load().hc_debug_mixes(_ptr(X), p, n, s, _ptr(mixes), _ptr(workspace), _stream(stream)))
 
 
-def hc_plan_tiles(n: int, groups: int):
+def hc_plan_tiles(n: int, d: int, ctas: int):
+    """(CTAs per tile, tokens per tile, tiles) of the fused calls."""
+    g = ctypes.c_int(0)
     tm = ctypes.c_int(0)
     nt = ctypes.c_int64(0)
-    _check("hc_plan_tiles", load().hc_plan_tiles(n, groups, ctypes.byref(tm), ctypes.byref(nt)))
-    return tm.value, nt.value
+    _check("hc_plan_tiles", load().hc_plan_tiles(n, d, ctas, ctypes.byref(g), ctypes.byref(tm), ctypes.byref(nt)))
+    return g.value, tm.value, nt.value
 
 
-def hc_fused_groups() -> int:
+def hc_fused_ctas() -> int:
     c = ctypes.c_int(0)
-    _check("hc_fused_groups", load().hc_fused_groups(ctypes.byref(c)))
+    _check("hc_fused_ctas", load().hc_fused_ctas(ctypes.byref(c)))
     return c.value
 
 

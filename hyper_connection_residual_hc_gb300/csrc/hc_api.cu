@@ -509,16 +509,16 @@ int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float*
     return launch_status(launch_fused(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int hc_plan_tiles(int64_t n, int groups, int* tile_m, int64_t* num_tiles) {
-    if (!tile_m || !num_tiles) return HC_ERR_NULL;
-    if (n < 0 || groups < 1) return HC_ERR_SHAPE;
-    plan_tiles(n, groups, tile_m, num_tiles);
+int hc_plan_tiles(int64_t n, int d, int ctas, int* group, int* tile_m, int64_t* num_tiles) {
+    if (!group || !tile_m || !num_tiles) return HC_ERR_NULL;
+    if (n < 0 || d < 1 || d % 256 != 0 || ctas < 8) return HC_ERR_SHAPE;
+    plan_tiles(n, d, ctas, group, tile_m, num_tiles);
     return HC_OK;
 }
 
-int hc_fused_groups(int* groups) {
-    if (!groups) return HC_ERR_NULL;
-    return launch_status(fused_active_groups(groups));
+int hc_fused_ctas(int* ctas) {
+    if (!ctas) return HC_ERR_NULL;
+    return launch_status(fused_ctas(ctas));
 }
 
 int hc_device_error(unsigned int* word, int clear, hc_stream_t stream) {

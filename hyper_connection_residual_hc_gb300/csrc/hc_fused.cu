@@ -66,8 +66,11 @@ constexpr int kMix = 24;
 constexpr int kBRows = 72;        // 3 planes x 24 mixes
 constexpr int kUmmaM = 128;
 constexpr int kUmmaN = 80;        // smallest legal N >= 72 at M = 128
-constexpr int kGroup = 8;          // CTAs sharing one token tile
-constexpr int kMaxGroups = 32;     // workspace capacity: up to 256 co-resident CTAs
+// A group of kG CTAs (8, 16 or 32, a template parameter) shares one token tile, each CTA taking
+// d/kG columns; small batches use larger groups so that each CTA has fewer column stages.
+constexpr int kMaxCtas = 256;      // workspace capacity: up to 256 co-resident CTAs
+constexpr int kMaxGroups = 32;     // launch counters: group slots (at most 256 / 8)
+constexpr int kFlagRanks = 32;     // flags per (group slot, tile parity): the largest group
 constexpr int kTileMax = 128;
 constexpr int kChunk = 32;        // columns per stage: 64-byte rows
 constexpr int kStages = 3;
@@ -94,25 +97,34 @@ constexpr int kOffNormW = kStages * kStageBytes;
 constexpr int kPartRows = 28;
 constexpr int kPartFloats = kPartRows * kTileMax;
 constexpr int kPartSx = kMix * kTileMax, kPartSy = kPartSx + 2 * kTileMax;
-constexpr int kOffRy = kOffNormW + kMaxDSlice * 4;           // r_y of the last two tiles [2][128]
-constexpr int kOffBar = kOffRy + 2 * kTileMax * 4;
+constexpr int kOffBar = kOffNormW + kMaxDSlice * 4;
 constexpr int kBarFull = 0, kBarXReady = 3, kBarEmpty = 6, kBarAccFull = 9, kBarAccEmpty = 10, kBarMmaDone = 11;
-constexpr int kBarSplitDone = 12, kBarRyFull = 13, kBarRyEmpty = 15, kBarYReady = 17, kBarYFree = 17 + 27;
-constexpr int kNumBars = 17 + 2 * 27;
-constexpr uint32_t kBarIdPublish = 1;  // named barrier: compute warps arrive, the split warp syncs
+// kBarFlagsSeen[2] (per tile parity): the split warp has seen the group's flags of a tile, so the
+// epilogue warps may read its sums of y^2. kBarEpiRead: the epilogue warps have read them (one
+// arrival per warp per tile); the split warp publishes the next tile only after that.
+constexpr int kBarSplitDone = 12, kBarFlagsSeen = 13, kBarEpiRead = 15, kBarYReady = 17, kBarYFree = 17 + 27;
+// kBarPublish: the compute warps have written the CTA's partial sums of a tile (one arrival per
+// warp), the split warp waits before publishing them. kBarExit: every warp is done (one arrival per
+// warp) before TMEM is freed. The CTA-wide hardware barriers are not used after the set-up: in
+// this kernel, whose warps spend most of their time in mbarrier waits, a block-wide bar.sync at
+// the end was measured releasing warp 0 while other warps had not reached it; mbarriers hold.
+constexpr int kBarPublish = 17 + 2 * 27, kBarExit = kBarPublish + 1;
+constexpr int kNumBars = kBarExit + 1;
 constexpr int kOffTmemPtr = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemPtr + 4;
 constexpr int kSmemUsed = kOffAbort + 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
 
-// global workspace: partial sums [group][tile parity][rank][28][128] fp32, then one 64-bit flag
-// per [group][tile parity][rank], then one 64-bit launch counter per group. A flag holds
+// global workspace: partial sums [group][tile parity][rank][28][128] fp32 (a block per CTA and
+// tile parity), then 64-bit flags [group slot][tile parity][32 ranks], then one 64-bit launch
+// counter per group slot. A flag slot is always tagged from the same counter, whatever the group
+// size of the launch that writes it, so tags never repeat on one workspace. A flag holds
 // (launch number of its group) << 32 | (tile index + 1); the launch number is the group's counter
 // + 1, read by every CTA of the group when it starts and stored back by the group's rank-0 CTA
 // after its last exchange, when all 8 have read it. The tags therefore come from the device: a
 // launch replayed from a CUDA graph tags its flags afresh, and a zero-filled workspace holds no tag.
-constexpr size_t kWsPartBytes = static_cast<size_t>(kMaxGroups) * 2 * kGroup * kPartFloats * 4;
-constexpr size_t kWsFlagBytes = static_cast<size_t>(kMaxGroups) * 2 * kGroup * 8;
+constexpr size_t kWsPartBytes = static_cast<size_t>(kMaxCtas) * 2 * kPartFloats * 4;
+constexpr size_t kWsFlagBytes = static_cast<size_t>(kMaxGroups) * 2 * kFlagRanks * 8;
 constexpr size_t kWsCounterBytes = static_cast<size_t>(kMaxGroups) * 8;
 constexpr size_t kWorkspaceBytes = kWsPartBytes + kWsFlagBytes + kWsCounterBytes;
 
@@ -220,30 +232,11 @@ struct Waiter {
             }
         }
     }
-    // Wait until the 8 flags at f[0..7] all equal `epoch` (acquire at GPU scope).
-    __device__ __forceinline__ bool wait_flags(const unsigned long long* f, unsigned long long epoch,
-                                               unsigned int code) const {
-        const uint64_t t0 = global_timer_ns();
-        int r = 0;
-        while (r < kGroup) {
-            if (ld_acquire_gpu_u64(f + r) == epoch) {
-                ++r;
-                continue;
-            }
-            if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                *abort = 1u;
-                atomicOr(&g_hc_error, code);
-                return false;
-            }
-        }
-        return true;
-    }
-    // Whole warp: lanes 0..7 each wait for flag f[lane] to equal `epoch`; returns when all 8 do.
+    // Whole warp: lanes 0..g-1 each wait for flag f[lane] to equal `epoch`; returns when all g do.
     __device__ __forceinline__ bool wait_flags_warp(const unsigned long long* f, unsigned long long epoch, int lane,
-                                                    unsigned int code) const {
+                                                    int g, unsigned int code) const {
         const uint64_t t0 = global_timer_ns();
-        bool mine = lane >= kGroup;
+        bool mine = lane >= g;
         while (true) {
             if (!mine) mine = ld_acquire_gpu_u64(f + lane) == epoch;
             if (__all_sync(0xffffffffu, mine)) return true;
@@ -273,7 +266,11 @@ struct Waiter {
 
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
 
-// "Reading weights" page, hc_split_sinkhorn kernel excerpt and the formula for p, in fp32.
+// "Reading weights" page, hc_split_sinkhorn kernel excerpt and the formula for p, in fp32. Every
+// normalisation multiplies by the hardware approximate reciprocal of its sum (1 ulp): the sums are
+// at least eps or 1, never subnormal, and the 2 * iters dependent normalisations run about four
+// times faster than with correctly rounded reciprocals (20 rounds: 2.1 us instead of 8.0 us on one
+// thread), which matters when a small batch waits for them.
 __device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const float (&sc)[3], const float (&b)[kMix],
                                                int iters, float eps, float (&pre)[4], float (&post)[4],
                                                float (&C)[16]) {
@@ -289,7 +286,7 @@ __device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const flo
         float mx = fmaxf(fmaxf(C[4 * j], C[4 * j + 1]), fmaxf(C[4 * j + 2], C[4 * j + 3]));
         float e0 = expf(C[4 * j] - mx), e1 = expf(C[4 * j + 1] - mx);
         float e2 = expf(C[4 * j + 2] - mx), e3 = expf(C[4 * j + 3] - mx);
-        float inv = __frcp_rn((e0 + e1) + (e2 + e3));
+        float inv = rcp_approx((e0 + e1) + (e2 + e3));
         C[4 * j] = e0 * inv + eps;
         C[4 * j + 1] = e1 * inv + eps;
         C[4 * j + 2] = e2 * inv + eps;
@@ -298,7 +295,7 @@ __device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const flo
     auto col_norm = [&]() {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            float inv = __frcp_rn(((C[k] + C[4 + k]) + (C[8 + k] + C[12 + k])) + eps);
+            float inv = rcp_approx(((C[k] + C[4 + k]) + (C[8 + k] + C[12 + k])) + eps);
             C[k] *= inv;
             C[4 + k] *= inv;
             C[8 + k] *= inv;
@@ -308,7 +305,7 @@ __device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const flo
     auto row_norm = [&]() {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            float inv = __frcp_rn(((C[4 * j] + C[4 * j + 1]) + (C[4 * j + 2] + C[4 * j + 3])) + eps);
+            float inv = rcp_approx(((C[4 * j] + C[4 * j + 1]) + (C[4 * j + 2] + C[4 * j + 3])) + eps);
             C[4 * j] *= inv;
             C[4 * j + 1] *= inv;
             C[4 * j + 2] *= inv;
@@ -324,7 +321,7 @@ __device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const flo
 
 // ---- the kernel ---------------------------------------------------------------------------------
 
-template <int kMode>
+template <int kMode, int kG>
 __global__ void __launch_bounds__(kThreads, 1)
     hc_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmD,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmXo,
@@ -337,12 +334,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = blockIdx.x % kGroup;    // column share of this CTA
-    const uint32_t cid = blockIdx.x / kGroup;     // group: owns tiles cid, cid + ncl, ...
-    const uint32_t ncl = gridDim.x / kGroup;
-    // first column of stage s of this CTA: the 8 CTAs of a group take interleaved 32-column
-    // chunks, so at any moment they read and write 512 contiguous bytes of each stream row
-    auto stage_col = [&](int s) -> int { return (s * kGroup + static_cast<int>(rank)) * kChunk; };
+    static_assert(kG == 8 || kG == 16 || kG == 32, "group sizes");
+    const uint32_t rank = blockIdx.x % kG;    // column share of this CTA
+    const uint32_t cid = blockIdx.x / kG;     // group: owns tiles cid, cid + ncl, ...
+    const uint32_t ncl = gridDim.x / kG;
+    // first column of stage s of this CTA: the kG CTAs of a group take interleaved 32-column
+    // chunks, so at any moment they read and write kG * 64 contiguous bytes of each stream row
+    auto stage_col = [&](int s) -> int { return (s * kG + static_cast<int>(rank)) * kChunk; };
     const int S = p.stages_per_tile;
 
     auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
@@ -359,14 +357,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(kBarAccEmpty), kComputeWarps);
         mbar_init(bar(kBarMmaDone), 1);
         mbar_init(bar(kBarSplitDone), 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(kBarRyFull + b), 1);
-            mbar_init(bar(kBarRyEmpty + b), 4);  // the epilogue warps
-        }
+        for (int b = 0; b < 2; ++b) mbar_init(bar(kBarFlagsSeen + b), 1);
+        mbar_init(bar(kBarEpiRead), 4);  // the epilogue warps
         for (int r = 0; r < kRing; ++r) {
             mbar_init(bar(kBarYReady + r), kComputeWarps);
             mbar_init(bar(kBarYFree + r), 4);
         }
+        mbar_init(bar(kBarPublish), kComputeWarps);
+        mbar_init(bar(kBarExit), kThreads / 32);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -547,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // flags (and read tile it - 1 itself).
             if (it > 0) W.wait(bar(kBarSplitDone), static_cast<uint32_t>((it - 1) & 1), kErrExchange);
             const int buf = static_cast<int>(it & 1);
-            float* P = p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kGroup + rank) * kPartFloats;
+            float* P = p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kG + rank) * kPartFloats;
             {
                 float4* pm4 = reinterpret_cast<float4*>(P + row * kMix + 12 * h);
                 pm4[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
@@ -559,7 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             P[kPartSx + h * kTileMax + row] = sxx.x + sxx.y;
             P[kPartSy + h * kTileMax + row] = syy.x + syy.y;
             // hand the block to the split warp, which publishes it; no waiting here
-            named_bar_arrive(kBarIdPublish, (kComputeWarps + 1) * 32);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarPublish));
         }
     } else if (warp >= kWarpEpi0) {
         // ================= epilogue warps: y_normed = bf16(norm_w * y * r_y), one quadrant each ===
@@ -567,12 +566,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = 32 * q + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
         const float* nw = reinterpret_cast<const float*>(smem + kOffNormW);
-        const float* ry_s = reinterpret_cast<const float*>(smem + kOffRy);
+        const float inv_d = 1.0f / static_cast<float>(p.d);
         long long g = 0;
         for (long long it = 0; it < my_tiles; ++it) {
             const int buf = static_cast<int>(it & 1);
-            W.wait(bar(kBarRyFull + buf), static_cast<uint32_t>((it >> 1) & 1), kErrEpilogue);
-            const float ry = ry_s[buf * kTileMax + row];
+            // r_y of this thread's row from the group's sums of y^2 (2 halves of each of the kG
+            // column shares), once the split warp has seen all their flags
+            W.wait(bar(kBarFlagsSeen + buf), static_cast<uint32_t>((it >> 1) & 1), kErrEpilogue);
+            const float* blk = p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kG) * kPartFloats + kPartSy + row;
+            float ssq = 0.f;
+#pragma unroll 8
+            for (int r = 0; r < kG; ++r) {
+                const float* Pr = blk + static_cast<size_t>(r) * kPartFloats;
+                ssq += ld_cg_f32(Pr) + ld_cg_f32(Pr + kTileMax);
+            }
+            const float ry = 1.0f / sqrtf(ssq * inv_d + p.norm_eps);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarEpiRead));  // this warp is done with the tile's blocks
             const long long t0 = (cid + it * ncl) * p.tile_m;
             const bool store = p.write_y && row < p.tile_m && t0 + row < p.n;
             uint16_t* yrow = static_cast<uint16_t*>(p.y_normed) + (store ? (t0 + row) * p.d : 0);
@@ -600,8 +610,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dst[3] = make_uint4(ov[12], ov[13], ov[14], ov[15]);
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarRyEmpty + buf));  // r_y buffer of this tile may be refilled
         }
     } else if (warp == kWarpProducer) {
         // ================= TMA producer =========================================================
@@ -708,7 +716,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 3; ++i) sc[i] = __ldg(p.hc_scale + i);
 #pragma unroll
         for (int i = 0; i < kMix; ++i) bs[i] = __ldg(p.hc_base + i);
-        float* ry_s = reinterpret_cast<float*>(smem + kOffRy);
         // this launch's number for the group: its counter + 1 (never 0, which a fresh workspace holds)
         unsigned long long launch_no = 0;
         if (lane == 0) launch_no = ld_acquire_gpu_u64(p.ws_launch + cid) + 1ull;
@@ -718,78 +725,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int buf = static_cast<int>(it & 1);
             // the compute warps have written this CTA's block of the tile: publish it, then wait for
             // the group (lanes 0..7 poll one flag each)
-            named_bar_sync(kBarIdPublish, (kComputeWarps + 1) * 32);
-            unsigned long long* flg = p.ws_flags + static_cast<size_t>(cid * 2 + buf) * kGroup;
+            W.wait(bar(kBarPublish), static_cast<uint32_t>(it & 1), kErrSplit);
+            // a flag also says that this CTA is done reading the group's blocks of the previous tile
+            // (whose buffer the group reuses after this tile): the split warp read them in its last
+            // iteration, the epilogue warps read the sums of y^2
+            if (it >= 1) W.wait(bar(kBarEpiRead), static_cast<uint32_t>((it - 1) & 1), kErrSplit);
+            unsigned long long* flg = p.ws_flags + static_cast<size_t>(cid * 2 + buf) * kFlagRanks;
             const unsigned long long epoch = epoch_base + static_cast<unsigned long long>(it) + 1ull;
             if (lane == 0) {
                 fence_acq_rel_gpu();  // after the barrier: the compute threads' block writes come first
                 st_release_gpu_u64(flg + rank, epoch);
             }
-            W.wait_flags_warp(flg, epoch, lane, kErrExchange);
-            // the compute warps must be done with the r_y buffer of tile it - 2
-            if (it >= 2) W.wait(bar(kBarRyEmpty + buf), static_cast<uint32_t>(((it >> 1) - 1) & 1), kErrSplit);
+            W.wait_flags_warp(flg, epoch, lane, kG, kErrExchange);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarFlagsSeen + buf));  // the epilogue warps may read the sums of y^2
             const long long tile = cid + it * ncl;
             const long long t0 = tile * p.tile_m;
-            const float* blk = p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kGroup) * kPartFloats;
-            {
-                // r_y of rows 4*lane .. 4*lane+3: sum y^2 over the 8 slices, 16 independent 16-byte loads
-                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int r = 0; r < kGroup; ++r) {
-                    const float* Pr = blk + static_cast<size_t>(r) * kPartFloats + kPartSy + 4 * lane;
-                    const float4 u = ld_cg_f4(Pr), v = ld_cg_f4(Pr + kTileMax);
-                    a.x += u.x + v.x; a.y += u.y + v.y; a.z += u.z + v.z; a.w += u.w + v.w;
-                }
-                const float inv_d = 1.0f / static_cast<float>(p.d);
-                float4 rv;
-                rv.x = 1.0f / sqrtf(a.x * inv_d + p.norm_eps);
-                rv.y = 1.0f / sqrtf(a.y * inv_d + p.norm_eps);
-                rv.z = 1.0f / sqrtf(a.z * inv_d + p.norm_eps);
-                rv.w = 1.0f / sqrtf(a.w * inv_d + p.norm_eps);
-                reinterpret_cast<float4*>(ry_s + buf * kTileMax)[lane] = rv;
-            }
-            // the owned tokens t = rank + 8i (i = lane % 16): lanes < 16 sum mixes 0..11 and sum x^2,
-            // lanes >= 16 mixes 12..23; the halves are then swapped between the two lanes
-            const int oi = lane & 15, oh = lane >> 4;
-            const int r_tok = static_cast<int>(rank) + kGroup * oi;
+            const float* blk = p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kG) * kPartFloats;
+            // the owned tokens t = rank + kG i (i < kT = 128 / kG): lane = part * kT + i sums mixes
+            // part * kMP .. part * kMP + kMP - 1 of token i over the kG blocks (part 0 also sum x^2);
+            // the parts are then gathered into every lane of the token by shuffles
+            constexpr int kT = kTileMax / kG, kParts = 32 / kT, kMP = kMix / kParts;
+            const int oi = lane % kT, part = lane / kT;
+            const int r_tok = static_cast<int>(rank) + kG * oi;
             const bool mine = r_tok < p.tile_m && t0 + r_tok < p.n;
-            float m[kMix];
+            float v[kMP];
 #pragma unroll
-            for (int i = 0; i < kMix; ++i) m[i] = 0.f;
+            for (int i = 0; i < kMP; ++i) v[i] = 0.f;
             float sxt = 0.f;
             if (mine) {
-                float part[12];
-#pragma unroll
-                for (int i = 0; i < 12; ++i) part[i] = 0.f;
-#pragma unroll
-                for (int r = 0; r < kGroup; ++r) {
+#pragma unroll 8
+                for (int r = 0; r < kG; ++r) {
                     const float* Pr = blk + static_cast<size_t>(r) * kPartFloats;
-                    const float* mp = Pr + r_tok * kMix + 12 * oh;
-                    const float4 u0 = ld_cg_f4(mp), u1 = ld_cg_f4(mp + 4), u2 = ld_cg_f4(mp + 8);
-                    part[0] += u0.x; part[1] += u0.y; part[2] += u0.z; part[3] += u0.w;
-                    part[4] += u1.x; part[5] += u1.y; part[6] += u1.z; part[7] += u1.w;
-                    part[8] += u2.x; part[9] += u2.y; part[10] += u2.z; part[11] += u2.w;
-                    if (oh == 0) sxt += Pr[kPartSx + r_tok] + Pr[kPartSx + kTileMax + r_tok];
-                }
+                    const float* mp = Pr + r_tok * kMix + kMP * part;
+                    if (kMP % 4 == 0) {
 #pragma unroll
-                for (int i = 0; i < 12; ++i) {
-                    m[i] = oh ? 0.f : part[i];
-                    m[12 + i] = oh ? part[i] : 0.f;
+                        for (int q = 0; q < kMP / 4; ++q) {
+                            const float4 u = ld_cg_f4(mp + 4 * q);
+                            v[4 * q] += u.x; v[4 * q + 1] += u.y; v[4 * q + 2] += u.z; v[4 * q + 3] += u.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kMP; ++i) v[i] += ld_cg_f32(mp + i);
+                    }
+                    if (part == 0) sxt += ld_cg_f32(Pr + kPartSx + r_tok) + ld_cg_f32(Pr + kPartSx + kTileMax + r_tok);
                 }
             }
-            // lanes i and i + 16 hold the two halves of the same token's mixes
+            float m[kMix];
 #pragma unroll
-            for (int i = 0; i < 12; ++i) {
-                const float lo = __shfl_sync(0xffffffffu, m[i], oi);
-                const float hi = __shfl_sync(0xffffffffu, m[12 + i], oi + 16);
-                m[i] = lo;
-                m[12 + i] = hi;
-            }
+            for (int q = 0; q < kParts; ++q)
+#pragma unroll
+                for (int i = 0; i < kMP; ++i) m[q * kMP + i] = __shfl_sync(0xffffffffu, v[i], q * kT + oi);
+            const bool oh = part != 0;
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar(kBarRyFull + buf));  // r_y of this tile is in shared memory
-                mbar_arrive(bar(kBarSplitDone));     // the blocks of this tile may be reused
-            }
+            if (lane == 0) mbar_arrive(bar(kBarSplitDone));  // the blocks of this tile may be reused
             if (mine && oh == 0) {
                 const long long tok = t0 + r_tok;
                 const float rr = 1.0f / sqrtf(sxt / static_cast<float>(4 * p.d) + p.norm_eps);
@@ -818,8 +807,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     }
 
+    // every warp is done with TMEM (and with everything else) before warp 0 frees it
     tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kBarExit));
+    W.drain(bar(kBarExit), 0);
+    __syncwarp();
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -860,22 +853,31 @@ bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, co
 
 struct DeviceState {
     bool ready = false;
-    int groups = 0;
+    int ctas = 0;
 };
 
 constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-int prepare_device(int* groups) {
+// every instantiation of the fused kernel: [mode][group size 8, 16, 32]
+template <int kMode>
+void kernels_of_mode(const void** k) {
+    k[0] = reinterpret_cast<const void*>(&hc_fused_kernel<kMode, 8>);
+    k[1] = reinterpret_cast<const void*>(&hc_fused_kernel<kMode, 16>);
+    k[2] = reinterpret_cast<const void*>(&hc_fused_kernel<kMode, 32>);
+}
+
+int prepare_device(int* ctas) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -7;
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DeviceState& st = g_dev[dev];
     if (!st.ready) {
-        const void* kernels[3] = {reinterpret_cast<const void*>(&hc_fused_kernel<kModePre>),
-                                  reinterpret_cast<const void*>(&hc_fused_kernel<kModePost>),
-                                  reinterpret_cast<const void*>(&hc_fused_kernel<kModeExpand>)};
+        const void* kernels[9];
+        kernels_of_mode<kModePre>(kernels);
+        kernels_of_mode<kModePost>(kernels + 3);
+        kernels_of_mode<kModeExpand>(kernels + 6);
         int per_sm = 1 << 30;
         for (const void* k : kernels) {
             if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
@@ -888,67 +890,64 @@ int prepare_device(int* groups) {
         int sms = 0, coop = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -7;
         if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) return -3;
-        st.groups = std::min(kMaxGroups, sms * per_sm / kGroup);
-        if (st.groups < 1) return -3;
+        st.ctas = std::min(kMaxCtas, sms * per_sm);
+        if (st.ctas < 8) return -3;
         st.ready = true;
     }
-    *groups = st.groups;
+    *ctas = st.ctas;
     return 0;
 }
 
 }  // namespace
 
-void plan_tiles(int64_t n, int groups, int* tile_m, int64_t* num_tiles) {
-    if (n <= 0) {
-        *tile_m = kTileMax;
-        *num_tiles = 0;
-        return;
-    }
-    if (groups < 1) groups = 1;
-    if (n <= kTileMax) {
-        // one tile per group at most; spread small batches over groups in 32-token tiles
-        int64_t best_tiles = 1;
-        int best_m = static_cast<int>(n);
-        for (int m = 32; m < n && m <= kTileMax; m += 32) {
+// Launch plan: for each group size g (d a multiple of 32 g) and tile height m (32..128, or n when
+// n < 32), groups = ctas / g groups run at once; a launch takes ceil(tiles / groups) waves of S =
+// d / (32 g) column stages each, plus a per-tile cost (group exchange, y_normed epilogue tail).
+// A stage costs the larger of its latency floor and a fixed part plus a part per token row; the
+// constants were measured on GB300 (2.1 us per 128-token stage of the prefill step, about 0.8 us
+// for a stage of a small batch, about 4 us per tile).
+void plan_tiles(int64_t n, int d, int ctas, int* group, int* tile_m, int64_t* num_tiles) {
+    *group = 8;
+    *tile_m = kTileMax;
+    *num_tiles = 0;
+    if (n <= 0) return;
+    constexpr double kStageFloorUs = 0.8, kStageFixedUs = 0.5, kStagePerRowUs = 1.6 / kTileMax, kTileUs = 4.0;
+    double best = -1.0;
+    const int gs[3] = {8, 16, 32};
+    for (int g : gs) {
+        if (d % (kChunk * g) != 0) continue;
+        const int groups = ctas / g;
+        if (groups < 1) continue;
+        const int S = d / (kChunk * g);
+        // tile heights, largest first (ties keep the larger tile and the smaller group)
+        const int ms[5] = {128, 96, 64, 32, n < 32 ? static_cast<int>(n) : 0};
+        for (int m : ms) {
+            if (m < 1) continue;
             const int64_t tiles = (n + m - 1) / m;
-            if (tiles <= groups) {
-                best_m = m;
-                best_tiles = tiles;
-                break;
+            const int64_t waves = (tiles + groups - 1) / groups;
+            const double stage = std::max(kStageFloorUs, kStageFixedUs + m * kStagePerRowUs);
+            const double cost = static_cast<double>(waves) * (S * stage + kTileUs);
+            if (best < 0.0 || cost < best - 1e-9) {
+                best = cost;
+                *group = g;
+                *tile_m = m;
+                *num_tiles = tiles;
             }
         }
-        *tile_m = best_m;
-        *num_tiles = best_tiles;
-        return;
     }
-    // cost of a choice: waves x (tokens per tile + fixed per-tile overhead in token-equivalents)
-    const int64_t overhead = 32;
-    int64_t best_cost = -1;
-    int best_m = kTileMax;
-    for (int m = kTileMax; m >= 32; m -= 32) {
-        const int64_t tiles = (n + m - 1) / m;
-        const int64_t waves = (tiles + groups - 1) / groups;
-        const int64_t cost = waves * (m + overhead);
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best_m = m;
-        }
-    }
-    *tile_m = best_m;
-    *num_tiles = (n + best_m - 1) / best_m;
 }
 
-int fused_active_groups(int* groups) { return prepare_device(groups); }
+int fused_ctas(int* ctas) { return prepare_device(ctas); }
 
 size_t workspace_bytes() { return kWorkspaceBytes; }
 
 int launch_fused(const FusedArgs& a, cudaStream_t stream) {
-    int groups = 0;
-    const int st = prepare_device(&groups);
+    int ctas = 0;
+    const int st = prepare_device(&ctas);
     if (st != 0) return st;
-    int tile_m = 0;
+    int group = 8, tile_m = 0;
     int64_t num_tiles = 0;
-    plan_tiles(a.n, groups, &tile_m, &num_tiles);
+    plan_tiles(a.n, a.d, ctas, &group, &tile_m, &num_tiles);
     if (num_tiles == 0) return 0;
 
     const uint64_t n = static_cast<uint64_t>(a.n), d = static_cast<uint64_t>(a.d);
@@ -999,38 +998,46 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     p.num_tiles = num_tiles;
     p.write_y = a.y_normed != nullptr;
     p.d = a.d;
-    p.d_slice = a.d / kGroup;
+    p.d_slice = a.d / group;
     p.stages_per_tile = p.d_slice / kChunk;
     p.tile_m = tile_m;
     p.iters = a.iters;
     p.hc_eps = a.hc_eps;
     p.norm_eps = a.norm_eps;
 
-    const int64_t grid_groups = std::min<int64_t>(num_tiles, groups);
+    const int64_t grid_groups = std::min<int64_t>(num_tiles, ctas / group);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident together: the group flags can be awaited
     attr[0].val.cooperative = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(grid_groups * kGroup), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_groups * group), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e;
-    if (a.mode == kModePost)
-        e = cudaLaunchKernelEx(&cfg, hc_fused_kernel<kModePost>, tmX, tmD, tmB, tmXo, p);
-    else if (a.mode == kModeExpand)
-        e = cudaLaunchKernelEx(&cfg, hc_fused_kernel<kModeExpand>, tmX, tmD, tmB, tmXo, p);
-    else
-        e = cudaLaunchKernelEx(&cfg, hc_fused_kernel<kModePre>, tmX, tmD, tmB, tmXo, p);
+    cudaError_t e = cudaErrorInvalidValue;
+    auto go = [&](auto kernel) { e = cudaLaunchKernelEx(&cfg, kernel, tmX, tmD, tmB, tmXo, p); };
+    if (a.mode == kModePost) {
+        if (group == 8) go(hc_fused_kernel<kModePost, 8>);
+        else if (group == 16) go(hc_fused_kernel<kModePost, 16>);
+        else go(hc_fused_kernel<kModePost, 32>);
+    } else if (a.mode == kModeExpand) {
+        if (group == 8) go(hc_fused_kernel<kModeExpand, 8>);
+        else if (group == 16) go(hc_fused_kernel<kModeExpand, 16>);
+        else go(hc_fused_kernel<kModeExpand, 32>);
+    } else {
+        if (group == 8) go(hc_fused_kernel<kModePre, 8>);
+        else if (group == 16) go(hc_fused_kernel<kModePre, 16>);
+        else go(hc_fused_kernel<kModePre, 32>);
+    }
     return e == cudaSuccess ? 0 : -7;
 }
 
 // ---- scratch that needs no allocation ------------------------------------------------------------
 // The workspace of hc_post_then_pre_noalloc: a fixed array in the library's device image, one per
 // GPU that loads the library, zero at load and kept until the process exits. Its size is the same
-// kWorkspaceBytes (7,344,384 bytes: room for 32 groups of 8 CTAs) that hc_workspace_size reports.
+// kWorkspaceBytes (7,356,672 bytes: room for 256 co-resident CTAs) that hc_workspace_size reports.
 static __device__ __align__(256) unsigned char g_noalloc_workspace[kWorkspaceBytes];
 
 namespace {

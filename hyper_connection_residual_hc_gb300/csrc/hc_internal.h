@@ -42,9 +42,9 @@ struct FusedArgs {
     float norm_eps;
 };
 
-// Tile plan of the fused kernel: tokens per tile and number of tiles for n tokens when
-// `groups` groups of 8 CTAs run concurrently.
-void plan_tiles(int64_t n, int groups, int* tile_m, int64_t* num_tiles);
+// Launch plan of the fused kernel for n tokens of width d when `ctas` CTAs can be resident at once:
+// CTAs per token tile (8, 16 or 32), tokens per tile and number of tiles.
+void plan_tiles(int64_t n, int d, int ctas, int* group, int* tile_m, int64_t* num_tiles);
 
 // Launches the fused kernel; returns 0, -7 (CUDA failure) or -3 (no cooperative launch).
 int launch_fused(const FusedArgs& a, cudaStream_t stream);
@@ -71,8 +71,8 @@ int launch_final(const FinalArgs& a, cudaStream_t stream);
 // Reads (and optionally clears) the device error word of the current device.
 int read_device_error(unsigned int* word, int clear, cudaStream_t stream);
 
-// Co-resident groups of 8 CTAs of the fused kernel on the current device (cached per device).
-int fused_active_groups(int* groups);
+// CTAs of the fused kernel that can be resident at once on the current device (cached per device).
+int fused_ctas(int* ctas);
 
 // Bytes of the workspace the fused kernel exchanges partial sums through.
 size_t workspace_bytes();

@@ -313,6 +313,21 @@ __device__ __forceinline__ float4 ld_cg_f4(const float* p) {
     return v;
 }
 
+// Hardware approximate reciprocal (rcp.approx.ftz.f32: at most 1 ulp from 1/x, subnormal inputs
+// and results flushed to zero).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// 4-byte load cached in L2 only (as ld_cg_f4).
+__device__ __forceinline__ float ld_cg_f32(const float* p) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // Named barrier `id` expecting `count` threads (whole warps): bar.sync waits for all of them,

@@ -141,7 +141,7 @@ int hc_post_then_pre(const void* delta, const void* X, const float* post, const 
  * engine that owns all device memory and hands it no workspace, a runtime whose memory plan is
  * frozen after start-up, or a program that must not risk an allocation failing mid-run. This
  * entry point takes the same arguments as hc_post_then_pre minus the workspace, and computes the
- * same results: its scratch is a fixed array inside the library's device image, 7,344,384 bytes
+ * same results: its scratch is a fixed array inside the library's device image, 7,356,672 bytes
  * (the hc_workspace_size figure), which every GPU that loads the library keeps until the process
  * exits. It allocates nothing and calls no allocating routine.
  *   - The first call on a device looks up that device's copy of the array (a runtime query, no
@@ -211,13 +211,17 @@ int hc_post_then_final(const void* delta, const void* X, const float* post, cons
 int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float* mixes,
                    void* workspace, hc_stream_t stream);
 
-/* Tile plan of the fused calls for n tokens when `groups` groups of 8 CTAs run at once: tokens per
- * tile (a multiple of 32 unless one tile holds all n <= 128 tokens) and the number of tiles.
- * Host-only, no CUDA call. Returns HC_ERR_NULL / HC_ERR_SHAPE on bad arguments. */
-int hc_plan_tiles(int64_t n, int groups, int* tile_m, int64_t* num_tiles);
+/* Launch plan of the fused calls for n tokens of stream width d when `ctas` CTAs of the fused
+ * kernel can be resident at once (hc_fused_ctas): the CTAs that share one token tile (`group`: 8,
+ * 16 or 32, each taking d/group columns; small batches use larger groups, so each CTA has fewer
+ * column stages), the tokens per tile (32, 64, 96 or 128; n itself when n < 32) and the number of
+ * tiles. Host-only, no CUDA call. Returns HC_ERR_NULL / HC_ERR_SHAPE (n < 0, d not a positive
+ * multiple of 256, ctas < 8) on bad arguments. */
+int hc_plan_tiles(int64_t n, int d, int ctas, int* group, int* tile_m, int64_t* num_tiles);
 
-/* How many groups of 8 CTAs of the fused kernel fit on the current device at once. */
-int hc_fused_groups(int* groups);
+/* How many CTAs of the fused kernel can be resident on the current device at once (one per SM on
+ * GB300: 152), capped at 256. */
+int hc_fused_ctas(int* ctas);
 
 /* Read the device-side error word of the current device: nonzero when a kernel gave up a
  * bounded wait (it then returned early and its outputs are not valid). Synchronises `stream`.

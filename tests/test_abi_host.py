@@ -69,8 +69,9 @@ def _expect(status, fn, *args):
 
 
 def test_workspace_size(lib):
-    # partial sums [32 groups][2 parities][8 CTAs][28][128] fp32, flags [32][2][8] u64, counters [32] u64
-    assert hc.hc_workspace_size() == 32 * 2 * 8 * 28 * 128 * 4 + 32 * 2 * 8 * 8 + 32 * 8
+    # partial sums [256 CTAs][2 parities][28][128] fp32, flags [32 group slots][2][32 ranks] u64,
+    # launch counters [32] u64
+    assert hc.hc_workspace_size() == 256 * 2 * 28 * 128 * 4 + 32 * 2 * 32 * 8 + 32 * 8
 
 
 def test_pre_step_validation(lib):
@@ -212,18 +213,24 @@ def test_post_then_final_validation(lib):
 
 
 def test_plan_tiles(lib):
-    for groups in (1, 7, 16, 18, 19):
-        for n in [1, 2, 31, 32, 33, 64, 100, 127, 128, 129, 255, 256, 1000, 4096, 16384, 16385, 65536, 100003]:
-            tm, nt = hc.hc_plan_tiles(n, groups)
-            assert 1 <= tm <= 128
-            assert nt * tm >= n and (nt - 1) * tm < n
-            if nt > 1:
-                assert tm % 32 == 0
-    # the prefill batch spreads evenly enough: waves * tile within 10% of the ideal per-cluster share
-    tm, nt = hc.hc_plan_tiles(16384, 19)
-    waves = -(-nt // 19)
-    assert waves * tm <= 1.1 * 16384 / 19
-    # decode batches use small tiles so that many groups work
-    tm, nt = hc.hc_plan_tiles(256, 19)
-    assert tm == 32 and nt == 8
-    assert hc.hc_plan_tiles(0, 19) == (128, 0)
+    for ctas in (8, 56, 128, 152, 256):
+        for d in (256, 512, 1024, 5120):
+            for n in [1, 2, 31, 32, 33, 64, 100, 127, 128, 129, 255, 256, 1000, 4096, 16384, 16385, 65536, 100003]:
+                g, tm, nt = hc.hc_plan_tiles(n, d, ctas)
+                assert g in (8, 16, 32) and d % (32 * g) == 0 and g <= ctas
+                assert 1 <= tm <= 128
+                assert nt * tm >= n and (nt - 1) * tm < n
+                if nt > 1:
+                    assert tm % 32 == 0
+    # the prefill batch: 128-token tiles over 19 groups of 8 (all 152 SMs of a GB300)
+    assert hc.hc_plan_tiles(16384, 5120, 152) == (8, 128, 128)
+    # a decode batch spreads each tile over more CTAs: fewer column stages per CTA
+    g, tm, nt = hc.hc_plan_tiles(256, 5120, 152)
+    assert g == 32 and g * nt <= 152
+    g, tm, nt = hc.hc_plan_tiles(64, 5120, 152)
+    assert g == 32 and g * nt <= 152
+    # d = 256 only divides into groups of 8
+    assert hc.hc_plan_tiles(64, 256, 152)[0] == 8
+    assert hc.hc_plan_tiles(0, 5120, 152)[2] == 0
+    _expect(hc.HC_ERR_SHAPE, hc.hc_plan_tiles, 16, 5000, 152)
+    _expect(hc.HC_ERR_SHAPE, hc.hc_plan_tiles, 16, 5120, 4)

@@ -150,6 +150,28 @@ def test_many_tiles_per_group_short_rows(d):
     gu.device_error_clear()
 
 
+@pytest.mark.parametrize("n,d,group,waves", [(100, 1024, 32, 1), (257, 5120, 32, 1), (544, 1024, 16, 1),
+                                             (2468, 2048, 16, 3), (2468, 1024, 8, 2)])
+def test_group_sizes(n, d, group, waves):
+    """Every group size the launch plan uses (8, 16 or 32 CTAs per token tile), single and multi-wave,
+    with ragged last tiles."""
+    g, tm, nt = hc.hc_plan_tiles(n, d, hc.hc_fused_ctas())
+    assert g == group and -(-nt // (hc.hc_fused_ctas() // g)) == waves, (g, tm, nt)
+    w = synth.small("step_b1_t64", 1, n, d, seed=900 + n + d)
+    inp = _inputs(w)
+    prm = synth.params(w, 0)
+    P = gu.DevParams(prm, d)
+    dev = {k: (gu.dev_bf16(v) if v.dtype == np.uint16 else gu.dev_f32(v)) for k, v in inp.items()}
+    out = gu.run_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, _shape(w), n)
+    idx = np.arange(n) if n <= 600 else gu.sample_tokens(n, 400, np.random.default_rng(n), tile=tm)
+    gu.check_sampled(w, 0, dev, out, prm, idx, True, "group %d n=%d d=%d" % (g, n, d))
+    # the reading half alone on the same streams
+    o2 = gu.run_pre_step(dev["X"], dev["pre_mix"], P, _shape(w), n)
+    gu.check_sampled(w, 0, dict(X=dev["X"], pre_mix=dev["pre_mix"]), o2, prm, idx, False,
+                     "pre_step group %d n=%d d=%d" % (g, n, d))
+    gu.device_error_clear()
+
+
 # ---- special cases with closed forms ------------------------------------------------------------
 
 def test_identity_comb_returns_streams_bit_exact():
