@@ -13,7 +13,8 @@ Under torchrun every rank runs its own batch (weak scaling, no data-path collect
 `--impl reference` times the CPU oracle itself as the reference arm.
 `--op` times another entry point on the same batch, against its own algorithmic bytes:
 post_then_pre (the default step), pre_step, expand_pre_step (head of the stack), post_then_final
-and final (tail of the stack, eps 1e-20), post (writing half alone).
+and final (tail of the stack, eps 1e-20), post (writing half alone), decode_chain (80 sublayers on 256
+tokens captured in one CUDA graph).
 """
 
 from __future__ import annotations
@@ -202,10 +203,13 @@ def run_reference(args):
         return
     import oracle as orc
     from hyper_connection_residual_hc_gb300 import synth
-    w = synth.WORKLOADS[WORKLOAD]
+    wname, op, unit, metric = WORKLOAD, args.op, "tokens/s", _metric(args.op)
+    if args.op == "decode_chain":  # the chain's sublayer steps, one hc_post_then_pre per sublayer
+        wname, op, unit = DECODE, "post_then_pre", "sublayer-tokens/s"
+        metric = "HC decode chain sublayer-tokens/s (80 sublayers x 256 tokens, one CUDA graph)"
+    w = synth.WORKLOADS[wname]
     threads = orc.hardware_threads()
     # size each step so that warmup + steps take about two minutes at most
-    op = args.op
     rate = _oracle_sample_rate(w, 4 * threads, threads, op)
     per_step = max(threads, min(w.n, int(rate * 120.0 / max(1, args.steps + args.warmup))))
     fn = _oracle_call(w, per_step, threads, op)  # the same sample every step, drawn once
@@ -216,14 +220,14 @@ def run_reference(args):
         fn()
     el = time.perf_counter() - t0
     value = per_step * args.steps / el
-    sample = "first %d of the %d tokens of %s per step (hc_%s, float64 oracle)" % (per_step, w.n, WORKLOAD, op)
-    line = {"impl": "reference", "metric": _metric(op), "value": value, "unit": "tokens/s", "n_gpus": world,
+    sample = "first %d of the %d tokens of %s per step (hc_%s, float64 oracle)" % (per_step, w.n, wname, op)
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "entry_point": "hc_" + op, "tokens": w.n, "hc": w.hc, "d": w.d,
+            "config": {"workload": wname, "entry_point": "hc_" + op, "tokens": w.n, "hc": w.hc, "d": w.d,
                        "sinkhorn_iters": w.iters},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
-            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
 
@@ -419,6 +423,173 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+DECODE = "decode_chain_b256_80steps"
+
+
+def run_decode_chain(args):
+    """The decode chain: 80 sublayers on 256 tokens, the whole stack as one CUDA graph of the
+    library's calls (hc_expand_pre_step, 79 x hc_post_then_pre, hc_post_then_final). The sublayers'
+    outputs Delta are drawn beforehand (the sublayer itself is not part of the path), so the graph
+    holds only the library's 81 launches. Timed by CUDA events around graph replays."""
+    import dataclasses
+
+    import numpy as np
+    import torch
+
+    import hyper_connection_residual_hc_gb300 as hc
+    from hyper_connection_residual_hc_gb300 import synth
+    from hyper_connection_residual_hc_gb300.synth import T_DELTA, T_EMBED
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    hc.load()
+    w0 = synth.WORKLOADS[DECODE]
+    w = dataclasses.replace(w0, seed=w0.seed + 17 * rank) if rank else w0
+    n, d, L = w.n, w.d, w.steps
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    def f32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+
+    params = []
+    for l in range(L):
+        prm = synth.params(w, l)
+        planes = torch.empty(hc.hc_prepare_params_size(4, d) // 2, dtype=torch.bfloat16, device="cuda")
+        fn = f32(prm["hc_fn"]).cuda()
+        hc.hc_prepare_params(fn, 4, d, planes)
+        keep = (planes, f32(prm["hc_scale"]).cuda(), f32(prm["hc_base"]).cuda(), f32(prm["norm_w"]).cuda())
+        params.append((hc.params(*keep), keep))
+    fw = f32(synth.final_norm_w(w)).cuda()
+    h_host = bf(synth.tokens(w, T_EMBED, 0)).pin_memory()
+    h = h_host.cuda()
+    delta = torch.stack([bf(synth.tokens(w, T_DELTA, l)) for l in range(L)]).cuda()
+    s = hc.shape(d=d, sinkhorn_iters=w.iters, hc_eps=w.hc_eps, norm_eps=w.norm_eps)
+    sf = hc.shape(d=d, norm_eps=FINAL_EPS)
+    X = [torch.empty((n, 4, d), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    y = torch.empty((n, d), dtype=torch.bfloat16, device="cuda")
+    coef = [dict(pre=torch.empty((n, 4), device="cuda"), post=torch.empty((n, 4), device="cuda"),
+                 comb=torch.empty((n, 4, 4), device="cuda")) for _ in range(2)]
+    z = torch.empty((n, d), dtype=torch.bfloat16, device="cuda")
+    ws = hc.new_workspace()
+
+    def chain():
+        c = coef[0]
+        hc.hc_expand_pre_step(h, params[0][0], n, s, X[0], y, c["pre"], c["post"], c["comb"], ws)
+        for l in range(1, L):
+            a, b = coef[(l - 1) % 2], coef[l % 2]
+            hc.hc_post_then_pre(delta[l - 1], X[(l - 1) % 2], a["post"], a["comb"], a["pre"], params[l][0], n, s,
+                                X[l % 2], y, b["pre"], b["post"], b["comb"], ws)
+        last = coef[(L - 1) % 2]
+        hc.hc_post_then_final(delta[L - 1], X[(L - 1) % 2], last["post"], last["comb"], last["pre"], fw, n, sf, None,
+                              z)
+
+    for _ in range(max(3, args.warmup)):
+        chain()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        chain()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        chain()
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    werr = hc.hc_device_error(clear=True)
+    stream = torch.cuda.current_stream()
+    steps = max(1, args.steps)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    el_ms = t0.elapsed_time(t1)
+    if dist is not None:
+        t = torch.tensor([el_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        el_ms = float(t.item())
+    derr = hc.hc_device_error(clear=True)
+
+    # end to end: the embedding in from pinned host memory and z out, every chain
+    z_host = torch.empty(z.shape, dtype=z.dtype, pin_memory=True)
+    e2e_steps = max(3, min(50, steps))
+    torch.cuda.synchronize()
+    w0t = time.perf_counter()
+    for _ in range(e2e_steps):
+        h.copy_(h_host, non_blocking=True)
+        graph.replay()
+        z_host.copy_(z, non_blocking=True)
+        stream.synchronize()
+    e2e_s = time.perf_counter() - w0t
+
+    chain_ms = el_ms / steps
+    sub_tokens = n * L * world
+    # algorithmic bytes of one chain: head (h in; streams, y_normed, coefficients out), 79 middle
+    # steps, tail (streams, Delta, coefficients in; z out); each sublayer's parameters once
+    alg = (n * 61536 + PARAM_BYTES) + (L - 1) * (n * BYTES_PER_TOKEN + PARAM_BYTES) + (n * 61536 + 20480)
+    peak, peak_kind = _peaks()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle as orc
+        threads = orc.hardware_threads()
+        k = 32  # tokens of the sample, every sublayer
+        prm0 = synth.params(w, 0)
+        sub = lambda t: synth.tokens(w, t, 0, 0, k)  # noqa: E731
+        from hyper_connection_residual_hc_gb300.synth import T_COMB, T_POST, T_PREMIX, T_X
+        args_ = (sub(T_DELTA), sub(T_X), sub(T_POST), sub(T_COMB), sub(T_PREMIX))
+        ts = time.perf_counter()
+        for _ in range(8):
+            orc.hc_post_then_pre(*args_, prm0["hc_fn"], prm0["hc_scale"], prm0["hc_base"], prm0["norm_w"], w.iters,
+                                 w.hc_eps, w.norm_eps, threads=threads)
+        rate = 8 * k / (time.perf_counter() - ts)
+        cpu = {"value": rate, "unit": "sublayer-tokens/s", "cores": threads, "kind": "oracle",
+               "sample": "8 sublayer steps (hc_post_then_pre) on %d of the %d tokens, float64 oracle" % (k, n)}
+    if rank == 0:
+        line = {
+            "metric": "HC decode chain sublayer-tokens/s (80 sublayers x 256 tokens, one CUDA graph)",
+            "value": sub_tokens / (chain_ms / 1e3), "unit": "sublayer-tokens/s", "n_gpus": world, "steps": steps,
+            "warmup": max(3, args.warmup), "ms_per_step": chain_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": DECODE, "entry_point": "graph of hc_expand_pre_step, 79 x hc_post_then_pre, "
+                       "hc_post_then_final", "tokens_per_gpu": n, "sublayers": L, "hc": 4, "d": d,
+                       "us_per_sublayer": chain_ms * 1e3 / L,
+                       "plan": dict(zip(("ctas_per_tile", "tile_tokens", "tiles"),
+                                        hc.hc_plan_tiles(n, d, hc.hc_fused_ctas()))),
+                       "l2": "no flush: the 80 parameter sets (236 MB of weight planes) exceed the 129 MB L2, "
+                             "the 10 MB of streams stay resident between sublayers as in a real decode step"},
+            "roofline": {"bound": "latency (launch chain)", "achieved": alg / (chain_ms / 1e3) / 1e9, "peak": peak,
+                         "unit": "GB/s", "frac": alg / (chain_ms / 1e3) / 1e9 / peak, "peak_kind": peak_kind,
+                         "traffic": None, "algorithmic_bytes": alg},
+            "cpu_baseline": cpu,
+            "e2e": {"value": sub_tokens * e2e_steps / e2e_s, "unit": "sublayer-tokens/s",
+                    "h2d_bytes_per_step": h.numel() * 2, "d2h_bytes_per_step": z.numel() * 2},
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                       "samples": clk["samples"]},
+            "gpu_launches": (L + 1) * steps,
+            "device_error": werr | derr,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -426,10 +597,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="post_then_pre", choices=sorted(OPS))
+    ap.add_argument("--op", default="post_then_pre", choices=sorted(OPS) + ["decode_chain"])
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "decode_chain":
+        run_decode_chain(args)
     else:
         run_ours(args)
 
