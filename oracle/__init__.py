@@ -68,6 +68,7 @@ def _declare(lib):
     lib.oracle_hc_expand_pre_step.argtypes = [_I64, _I, _I, _P, _P, _P, _P, _P, _I, _D, _D, _P, _P, _P, _P, _P, _I]
     lib.oracle_hc_final.argtypes = [_I64, _I, _I, _P, _P, _P, _D, _P, _P, _P, _I]
     lib.oracle_hc_post_then_final.argtypes = [_I64, _I, _I, _P, _P, _P, _P, _P, _P, _D, _P, _P, _I]
+    lib.oracle_stream_mean.argtypes = [_I64, _I, _I, _P, _P, _P, _I]
     lib.oracle_hardware_threads.restype = _I
     lib.oracle_hardware_threads.argtypes = []
 
@@ -282,3 +283,14 @@ def hc_post_then_final(delta, X, post, comb, pre_mix, norm_w, norm_eps, threads=
     lib.oracle_hc_post_then_final(n, hc, d, _p(delta), _p(X), _p(post), _p(comb), _p(pre_mix), _p(norm_w),
                                   float(norm_eps), _p(out["X_out"]), _p(out["z"]), threads)
     return out
+
+
+def stream_mean(X, threads=0, lib=None):
+    """The mean over the hc streams of X [n,hc,d] (u16), rounded to bf16: (out [n,d] u16, exact)."""
+    lib = lib or load()
+    X = _c(X, np.uint16)
+    n, hc, d = X.shape
+    out = np.empty((n, d), np.uint16)
+    ex = np.empty((n, d), np.float64)
+    lib.oracle_stream_mean(n, hc, d, _p(X), _p(out), _p(ex), threads)
+    return out, ex

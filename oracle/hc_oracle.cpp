@@ -387,6 +387,21 @@ void oracle_hc_post_then_final(int64_t n, int hc, int d, const uint16_t* delta, 
     oracle_hc_final(n, hc, d, X_out, pre_mix, norm_w, norm_eps, z, nullptr, nullptr, threads);
 }
 
+// [FN] Transformer.forward excerpt: at the multi-token-prediction head's target layers the model
+// keeps h.mean over the hc streams entering the layer (the streams after the previous sublayer's
+// hc_post), cast to the stream dtype. out [n, d] bf16 = bf16(mean_j X[t, j, :]).
+void oracle_stream_mean(int64_t n, int hc, int d, const uint16_t* X, uint16_t* out, double* exact, int threads) {
+    parallel_for(n, threads, [&](int64_t t) {
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < hc; ++j) acc += bf16_to_double(X[(t * hc + j) * d + i]);
+            const double m = acc / hc;
+            if (exact) exact[t * d + i] = m;
+            out[t * d + i] = double_to_bf16(m);
+        }
+    });
+}
+
 int oracle_hardware_threads() {
     return static_cast<int>(std::max(1u, std::thread::hardware_concurrency()));
 }

@@ -560,4 +560,29 @@ def pin_post_then_final_hand_case(lib):
     assert np.allclose(want[:2], b["y_normed_exact_first_two"], rtol=1e-6)
 
 
+def pin_stream_mean(lib):
+    """The tap of the multi-token-prediction head: mean over the streams. Identical streams give the
+    value itself; (a, -a, b, -b) gives 0; dyadic streams give their exact mean; random streams match
+    numpy's float64 mean rounded once; the mean is over the stream axis, not the columns."""
+    d = 16
+    a = _bf(np.arange(-8, 8) * 0.375)
+    X = np.stack([a, a, a, a])[None]
+    out, ex = orc.stream_mean(X, lib=lib)
+    assert np.array_equal(out[0], a)
+    b = _bf(np.arange(1, d + 1) * 0.125)
+    neg = lambda v: (v ^ 0x8000).astype(np.uint16)  # noqa: E731
+    out, ex = orc.stream_mean(np.stack([a, neg(a), b, neg(b)])[None], lib=lib)
+    assert np.all(ex == 0)
+    c = np.array([1.0, 0.5, 0.25, 2.0])
+    X = _bf(np.repeat(c[:, None], d, axis=1))[None]
+    _, ex = orc.stream_mean(X, lib=lib)
+    assert np.all(ex == c.mean())
+    rng = np.random.default_rng(30)
+    X = _rand_bf16(rng, (3, 4, d))
+    out, ex = orc.stream_mean(X, lib=lib)
+    want = orc.bf16_to_double(X).mean(axis=1)
+    assert np.allclose(ex, want, rtol=1e-15, atol=0)
+    assert np.array_equal(out, orc.double_to_bf16(want, lib=lib))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -74,6 +74,9 @@ MUTANTS = {
     "post_then_final_skips_post": ("oracle_hc_post(n, hc, d, X, delta, post, comb, X_out, threads);\n"
                                    "    oracle_hc_final(",
                                    "std::copy(X, X + n * hc * d, X_out);\n    oracle_hc_final("),
+    "stream_mean_over_columns": ("for (int j = 0; j < hc; ++j) acc += bf16_to_double(X[(t * hc + j) * d + i]);",
+                                 "for (int j = 0; j < hc; ++j) acc += bf16_to_double(X[t * hc * d + i * hc + j]);"),
+    "stream_mean_sum_not_mean": ("const double m = acc / hc;", "const double m = acc;"),
 }
 
 
