@@ -46,6 +46,10 @@ FINAL_SOURCES = [CSRC + "hc_final.cu"]
 OPS = {
     "post_then_pre": dict(bytes_per_token=BYTES_PER_TOKEN, param_bytes=PARAM_BYTES, kernel="hc_fused_kernel<1>",
                           sources=FUSED_SOURCES, traffic="hc_fused_prefill_b4_t4096_traffic.json"),
+    # the step plus the mean of the 4 new streams: + 10240 written
+    "post_then_pre_tap": dict(bytes_per_token=BYTES_PER_TOKEN + 10240, param_bytes=PARAM_BYTES,
+                              kernel="hc_fused_kernel<1>", sources=FUSED_SOURCES,
+                              traffic="hc_fused_tap_prefill_b4_t4096_traffic.json"),
     # read X 40960 + pre_mix 16; write y_normed 10240 + pre/post/comb 96
     "pre_step": dict(bytes_per_token=51312, param_bytes=PARAM_BYTES, kernel="hc_fused_kernel<0>",
                      sources=FUSED_SOURCES, traffic="hc_fused_pre_step_prefill_b4_t4096_traffic.json"),
@@ -167,9 +171,14 @@ def _oracle_call(w, tokens, threads, op="post_then_pre"):
         return synth.tokens(w, t, 0, 0, tokens)
 
     coef = (prm["hc_fn"], prm["hc_scale"], prm["hc_base"], prm["norm_w"], w.iters, w.hc_eps, w.norm_eps)
-    if op == "post_then_pre":
+    if op in ("post_then_pre", "post_then_pre_tap"):
         args = (tk(T_DELTA), tk(T_X), tk(T_POST), tk(T_COMB), tk(T_PREMIX))
-        fn = lambda: orc.hc_post_then_pre(*args, *coef, threads=threads)  # noqa: E731
+        if op == "post_then_pre":
+            fn = lambda: orc.hc_post_then_pre(*args, *coef, threads=threads)  # noqa: E731
+        else:
+            def fn():
+                out = orc.hc_post_then_pre(*args, *coef, threads=threads)
+                orc.stream_mean(out["X_out"], threads=threads)
     elif op == "pre_step":
         args = (tk(T_X), tk(T_PREMIX))
         fn = lambda: orc.hc_pre_step(*args, *coef, threads=threads)  # noqa: E731
@@ -264,6 +273,7 @@ def run_ours(args):
 
     # per-token inputs of the op (copied host -> device every step of the e2e run)
     names = {"post_then_pre": ("delta", "X", "post", "comb", "pre_mix"), "pre_step": ("X", "pre_mix"),
+             "post_then_pre_tap": ("delta", "X", "post", "comb", "pre_mix"),
              "expand_pre_step": ("h",), "post_then_final": ("delta", "X", "post", "comb", "pre_mix"),
              "final": ("X", "pre_mix"), "post": ("delta", "X", "post", "comb")}[op]
     draw = dict(delta=lambda: bf(synth.tokens(w, T_DELTA, 0)), X=lambda: bf(synth.tokens(w, T_X, 0)),
@@ -287,6 +297,8 @@ def run_ours(args):
                         comb=empty(n, 4, 4, dt=torch.float32))
     if op in ("post_then_pre", "expand_pre_step"):
         out = dict(X_out=empty(n, 4, d), y_normed=empty(n, d), **coef())
+    elif op == "post_then_pre_tap":
+        out = dict(X_out=empty(n, 4, d), y_normed=empty(n, d), stream_mean=empty(n, d), **coef())
     elif op == "pre_step":
         out = dict(y_normed=empty(n, d), **coef())
     elif op in ("post_then_final", "final"):
@@ -300,6 +312,10 @@ def run_ours(args):
         if op == "post_then_pre":
             hc.hc_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, n, s,
                                 out["X_out"], out["y_normed"], out["pre"], out["post"], out["comb"], ws, stream)
+        elif op == "post_then_pre_tap":
+            hc.hc_post_then_pre_tap(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, n, s,
+                                    out["X_out"], out["y_normed"], out["pre"], out["post"], out["comb"],
+                                    out["stream_mean"], ws, stream)
         elif op == "pre_step":
             hc.hc_pre_step(dev["X"], dev["pre_mix"], P, n, s, out["y_normed"], out["pre"], out["post"], out["comb"],
                            ws, stream)

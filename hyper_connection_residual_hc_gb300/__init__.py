@@ -31,7 +31,7 @@ HC_ERR_DEVICE = -8
 # every symbol include/hc.h declares
 SYMBOLS = (
     "hc_prepare_params_size", "hc_prepare_params", "hc_workspace_size", "hc_pre_step", "hc_post_then_pre",
-    "hc_post_then_pre_noalloc", "hc_post", "hc_expand_pre_step", "hc_final", "hc_post_then_final", "hc_debug_mixes",
+    "hc_post_then_pre_tap", "hc_post_then_pre_noalloc", "hc_post", "hc_expand_pre_step", "hc_final", "hc_post_then_final", "hc_debug_mixes",
     "hc_plan_tiles", "hc_fused_ctas", "hc_device_error", "hc_status_string",
 )
 
@@ -70,6 +70,7 @@ def load(path: str = LIB_PATH):
     lib.hc_workspace_size.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
     lib.hc_pre_step.argtypes = [P, P, hc_params_t, I64, hc_shape_t, P, P, P, P, P, P]
     lib.hc_post_then_pre.argtypes = [P, P, P, P, P, hc_params_t, I64, hc_shape_t, P, P, P, P, P, P, P]
+    lib.hc_post_then_pre_tap.argtypes = [P, P, P, P, P, hc_params_t, I64, hc_shape_t, P, P, P, P, P, P, P, P]
     lib.hc_post_then_pre_noalloc.argtypes = [P, P, P, P, P, hc_params_t, I64, hc_shape_t, P, P, P, P, P, P]
     lib.hc_post.argtypes = [P, P, P, P, I64, hc_shape_t, P, P]
     lib.hc_expand_pre_step.argtypes = [P, hc_params_t, I64, hc_shape_t, P, P, P, P, P, P, P]
@@ -157,6 +158,14 @@ def hc_post_then_pre(delta, X, post, comb, pre_mix, nxt: hc_params_t, n: int, s:
     _check("hc_post_then_pre", load().hc_post_then_pre(
         _ptr(delta), _ptr(X), _ptr(post), _ptr(comb), _ptr(pre_mix), nxt, n, s, _ptr(X_out), _ptr(y_normed),
         _ptr(pre_out), _ptr(post_out), _ptr(comb_out), _ptr(workspace), _stream(stream)))
+
+
+def hc_post_then_pre_tap(delta, X, post, comb, pre_mix, nxt: hc_params_t, n: int, s: hc_shape_t, X_out, y_normed,
+                         pre_out, post_out, comb_out, stream_mean, workspace, stream=None) -> None:
+    """hc_post_then_pre that also writes bf16(mean over the 4 new streams) to stream_mean [n, d]."""
+    _check("hc_post_then_pre_tap", load().hc_post_then_pre_tap(
+        _ptr(delta), _ptr(X), _ptr(post), _ptr(comb), _ptr(pre_mix), nxt, n, s, _ptr(X_out), _ptr(y_normed),
+        _ptr(pre_out), _ptr(post_out), _ptr(comb_out), _ptr(stream_mean), _ptr(workspace), _stream(stream)))
 
 
 def hc_post_then_pre_noalloc(delta, X, post, comb, pre_mix, nxt: hc_params_t, n: int, s: hc_shape_t, X_out,

@@ -165,6 +165,56 @@ int launch_status(int internal) { return internal == 0 ? HC_OK : internal == -3 
 
 using namespace hc;
 
+static int post_then_pre_impl(const void* delta, const void* X, const float* post, const float* comb,
+                              const float* pre_mix, hc_params_t next, int64_t n, hc_shape_t s, void* X_out,
+                              void* y_normed, float* pre_out, float* post_out, float* comb_out, void* stream_mean,
+                              void* workspace, hc_stream_t stream) {
+    if (!delta || !X || !post || !comb || !pre_mix || !X_out || !y_normed || !pre_out || !post_out || !comb_out ||
+        !workspace)
+        return HC_ERR_NULL;
+    int st = check_params(next);
+    if (st != HC_OK) return st;
+    st = check_shape_fused(n, s);
+    if (st != HC_OK) return st;
+    const void* ptrs[11] = {delta, X, post, comb, pre_mix, X_out, y_normed, pre_out, post_out, comb_out, workspace};
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return HC_ERR_ALIGN;
+    const size_t N = static_cast<size_t>(n);
+    const size_t xb = N * kHC * s.d * 2, yb = N * s.d * 2, cb = N * 16, kb = N * 64;
+    const void* ins[5] = {delta, X, post, comb, pre_mix};
+    const size_t isz[5] = {yb, xb, cb, kb, cb};
+    if (stream_mean && !aligned16(stream_mean)) return HC_ERR_ALIGN;
+    const void* outs[7] = {X_out, y_normed, pre_out, post_out, comb_out, workspace, stream_mean};
+    const size_t osz[7] = {xb, yb, cb, cb, kb, workspace_bytes(), yb};
+    if (any_overlap(outs, osz, 7, ins, isz, 5)) return HC_ERR_ALIAS;
+    if (n == 0) return HC_OK;
+    FusedArgs a = {};
+    a.mode = kModePost;
+    a.X = X;
+    a.delta = delta;
+    a.post = post;
+    a.comb = comb;
+    a.pre_mix = pre_mix;
+    a.planes = next.hc_fn_planes;
+    a.hc_scale = next.hc_scale;
+    a.hc_base = next.hc_base;
+    a.norm_w = next.norm_w;
+    a.X_out = X_out;
+    a.y_normed = y_normed;
+    a.pre_out = pre_out;
+    a.post_out = post_out;
+    a.comb_out = comb_out;
+    a.stream_mean = stream_mean;
+    a.workspace = workspace;
+    a.n = n;
+    a.d = s.d;
+    a.iters = s.sinkhorn_iters;
+    a.hc_eps = s.hc_eps;
+    a.norm_eps = s.norm_eps;
+    return launch_status(launch_fused(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+
 extern "C" {
 
 const char* hc_status_string(int status) {
@@ -276,52 +326,17 @@ int hc_pre_step(const void* X, const float* pre_mix, hc_params_t p, int64_t n, h
 int hc_post_then_pre(const void* delta, const void* X, const float* post, const float* comb, const float* pre_mix,
                      hc_params_t next, int64_t n, hc_shape_t s, void* X_out, void* y_normed, float* pre_out,
                      float* post_out, float* comb_out, void* workspace, hc_stream_t stream) {
-    if (!delta || !X || !post || !comb || !pre_mix || !X_out || !y_normed || !pre_out || !post_out || !comb_out ||
-        !workspace)
-        return HC_ERR_NULL;
-    int st = check_params(next);
-    if (st != HC_OK) return st;
-    st = check_shape_fused(n, s);
-    if (st != HC_OK) return st;
-    const void* ptrs[11] = {delta, X, post, comb, pre_mix, X_out, y_normed, pre_out, post_out, comb_out, workspace};
-    for (const void* q : ptrs)
-        if (!aligned16(q)) return HC_ERR_ALIGN;
-    const size_t N = static_cast<size_t>(n);
-    const size_t xb = N * kHC * s.d * 2, yb = N * s.d * 2, cb = N * 16, kb = N * 64;
-    const void* ins[5] = {delta, X, post, comb, pre_mix};
-    const size_t isz[5] = {yb, xb, cb, kb, cb};
-    const void* outs[6] = {X_out, y_normed, pre_out, post_out, comb_out, workspace};
-    const size_t osz[6] = {xb, yb, cb, cb, kb, workspace_bytes()};
-    for (int i = 0; i < 6; ++i) {
-        for (int j = 0; j < 5; ++j)
-            if (overlap(outs[i], osz[i], ins[j], isz[j])) return HC_ERR_ALIAS;
-        for (int j = i + 1; j < 6; ++j)
-            if (overlap(outs[i], osz[i], outs[j], osz[j])) return HC_ERR_ALIAS;
-    }
-    if (n == 0) return HC_OK;
-    FusedArgs a = {};
-    a.mode = kModePost;
-    a.X = X;
-    a.delta = delta;
-    a.post = post;
-    a.comb = comb;
-    a.pre_mix = pre_mix;
-    a.planes = next.hc_fn_planes;
-    a.hc_scale = next.hc_scale;
-    a.hc_base = next.hc_base;
-    a.norm_w = next.norm_w;
-    a.X_out = X_out;
-    a.y_normed = y_normed;
-    a.pre_out = pre_out;
-    a.post_out = post_out;
-    a.comb_out = comb_out;
-    a.workspace = workspace;
-    a.n = n;
-    a.d = s.d;
-    a.iters = s.sinkhorn_iters;
-    a.hc_eps = s.hc_eps;
-    a.norm_eps = s.norm_eps;
-    return launch_status(launch_fused(a, reinterpret_cast<cudaStream_t>(stream)));
+    return post_then_pre_impl(delta, X, post, comb, pre_mix, next, n, s, X_out, y_normed, pre_out, post_out,
+                              comb_out, nullptr, workspace, stream);
+}
+
+int hc_post_then_pre_tap(const void* delta, const void* X, const float* post, const float* comb,
+                         const float* pre_mix, hc_params_t next, int64_t n, hc_shape_t s, void* X_out,
+                         void* y_normed, float* pre_out, float* post_out, float* comb_out, void* stream_mean,
+                         void* workspace, hc_stream_t stream) {
+    if (!stream_mean) return HC_ERR_NULL;
+    return post_then_pre_impl(delta, X, post, comb, pre_mix, next, n, s, X_out, y_normed, pre_out, post_out,
+                              comb_out, stream_mean, workspace, stream);
 }
 
 int hc_post_then_pre_noalloc(const void* delta, const void* X, const float* post, const float* comb,

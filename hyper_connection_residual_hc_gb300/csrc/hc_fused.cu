@@ -174,6 +174,7 @@ struct FusedParams {
     float* post_out;
     float* comb_out;
     float* mixes_out;
+    void* stream_mean;              // bf16 [n, d] mean of the 4 new streams, or null
     void* y_normed;
     float* ws_part;                 // workspace partial-sum blocks
     unsigned long long* ws_flags;   // workspace flags
@@ -504,6 +505,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
                             st_smem_v4(sb + kOffX + k * kXTileBytes + off, ov);
                             unpack4(ov, xr[k]);
+                        }
+                        if (p.stream_mean && valid) {
+                            // the multi-token-prediction tap: bf16(mean_j X'_j), summed in fp32
+                            uint32_t o[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                float2 t = __fadd2_rn(__fadd2_rn(__fadd2_rn(xr[0][e], xr[1][e]), xr[2][e]), xr[3][e]);
+                                o[e] = pack_bf16(__fmul2_rn(t, bcast(0.25f)));
+                            }
+                            uint16_t* mrow = static_cast<uint16_t*>(p.stream_mean) + tok * p.d;
+                            *reinterpret_cast<uint4*>(mrow + stage_col(s) + c * 8) = make_uint4(o[0], o[1], o[2], o[3]);
                         }
                     } else {
 #pragma unroll
@@ -989,6 +1001,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     p.post_out = a.post_out;
     p.comb_out = a.comb_out;
     p.mixes_out = a.mixes_out;
+    p.stream_mean = a.stream_mean;
     p.y_normed = a.y_normed;
     p.ws_part = reinterpret_cast<float*>(a.workspace);
     p.ws_flags = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(a.workspace) + kWsPartBytes);

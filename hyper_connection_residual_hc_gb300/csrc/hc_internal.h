@@ -34,6 +34,7 @@ struct FusedArgs {
     float* post_out;         // fp32 [n, 4]
     float* comb_out;         // fp32 [n, 4, 4]
     float* mixes_out;        // fp32 [n, 24]           (null: not written)
+    void* stream_mean;       // bf16 [n, d]            (post mode; null: not written)
     void* workspace;         // workspace_bytes(), zero-filled before its first use
     int64_t n;
     int d;

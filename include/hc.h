@@ -136,6 +136,19 @@ int hc_post_then_pre(const void* delta, const void* X, const float* post, const 
                      void* y_normed, float* pre_out, float* post_out, float* comb_out,
                      void* workspace, hc_stream_t stream);
 
+/* hc_post_then_pre that also writes the mean of the four new streams, the input of the
+ * multi-token-prediction head ("Final RMSNorm" page, Transformer.forward excerpt: at the head's
+ * target layers, 37-39 of the "Router" page's config.json, the model keeps the mean over the hc
+ * streams entering the layer, cast to the stream dtype):
+ *   stream_mean [device] bf16 [n, d] = bf16(mean_j X_out[:, j, :])   (summed in fp32)
+ * computed from the X' values the call already holds, so it costs only its own 2*d bytes of writes
+ * per token. stream_mean must not overlap any other argument (HC_ERR_ALIAS); everything else as
+ * hc_post_then_pre. */
+int hc_post_then_pre_tap(const void* delta, const void* X, const float* post, const float* comb,
+                         const float* pre_mix, hc_params_t next, int64_t n, hc_shape_t s, void* X_out,
+                         void* y_normed, float* pre_out, float* post_out, float* comb_out, void* stream_mean,
+                         void* workspace, hc_stream_t stream);
+
 /* hc_post_then_pre for callers that cannot allocate device memory. Some callers can never call
  * cudaMalloc (or any allocator) at the point where they run this step: a plugin hosted by an
  * engine that owns all device memory and hands it no workspace, a runtime whose memory plan is

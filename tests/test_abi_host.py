@@ -130,6 +130,27 @@ def test_post_then_pre_validation(lib):
     hc.hc_post_then_pre(*bad)
 
 
+def test_post_then_pre_tap_validation(lib):
+    s = hc.shape()
+    st = 0
+    args = [A[0], A[1], A[2], A[3], A[4], _p(), 8, s, A[5], A[6], A[7], A[8], A[9], A[15], A[14], st]
+    bad = list(args)
+    bad[13] = None  # the tap is this call's point
+    _expect(hc.HC_ERR_NULL, hc.hc_post_then_pre_tap, *bad)
+    bad = list(args)
+    bad[13] = A[6] + 512  # stream_mean inside y_normed
+    _expect(hc.HC_ERR_ALIAS, hc.hc_post_then_pre_tap, *bad)
+    bad = list(args)
+    bad[13] = A[1]  # on X
+    _expect(hc.HC_ERR_ALIAS, hc.hc_post_then_pre_tap, *bad)
+    bad = list(args)
+    bad[13] = A[15] + 2
+    _expect(hc.HC_ERR_ALIGN, hc.hc_post_then_pre_tap, *bad)
+    bad = list(args)
+    bad[6] = 0
+    hc.hc_post_then_pre_tap(*bad)
+
+
 def test_post_validation(lib):
     s = hc.shape(d=24)  # hc_post only needs d % 8 == 0
     _expect(hc.HC_ERR_SHAPE, hc.hc_post, A[0], A[1], A[2], A[3], 4, hc.shape(d=20), A[4], 0)
