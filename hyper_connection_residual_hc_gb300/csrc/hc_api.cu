@@ -14,8 +14,9 @@
 namespace hc {
 namespace {
 
-constexpr int kHC = 4;
-constexpr int kMix = (2 + kHC) * kHC;
+constexpr int kHC = 4;         // the fused kernel's number of streams
+constexpr int kMaxHc = 8;      // the generic path's limits
+constexpr int kMaxD = 65536;
 
 // ---- writing half: X' = bf16(post_k * delta + sum_j comb[j,k] X_j) ---------------------------
 // "Write the streams" page, formula for X'_{n,k}; "Source layer, pairs pooled" page, Block.hc_post
@@ -74,11 +75,12 @@ __global__ void __launch_bounds__(256) hc_post_kernel(const uint4* __restrict__ 
 }
 
 // ---- weight split: hc_fn = hi + mid + lo, three bf16 planes ----------------------------------
-// Plane rows are grouped for the fused kernel's accumulator drain: row 36*h + 12*p + i holds
-// plane p (0 hi, 1 mid, 2 lo) of mix 12*h + i.
+// Plane rows follow plane_row(): grouped for the fused kernel's accumulator drain at hc = 4 (row
+// 36*h + 12*p + i holds plane p (0 hi, 1 mid, 2 lo) of mix 12*h + i), plane-major otherwise.
 __global__ void __launch_bounds__(256) hc_prepare_kernel(const float* __restrict__ fn, __nv_bfloat16* planes,
-                                                         long long D) {
-    const long long total = static_cast<long long>(kMix) * D;
+                                                         int hc, long long D) {
+    const int M = (2 + hc) * hc;
+    const long long total = static_cast<long long>(M) * D;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
         const long long m = idx / D;
@@ -89,10 +91,10 @@ __global__ void __launch_bounds__(256) hc_prepare_kernel(const float* __restrict
         const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
         const float r2 = r1 - __bfloat162float(mid);  // exact; at most 8 significant bits remain
         const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
-        const long long hh = m / 12, i = m % 12;
-        planes[(36 * hh + 0 + i) * D + c] = hi;
-        planes[(36 * hh + 12 + i) * D + c] = mid;
-        planes[(36 * hh + 24 + i) * D + c] = lo;
+        const int mm = static_cast<int>(m);
+        planes[plane_row(hc, M, 0, mm) * D + c] = hi;
+        planes[plane_row(hc, M, 1, mm) * D + c] = mid;
+        planes[plane_row(hc, M, 2, mm) * D + c] = lo;
     }
 }
 
@@ -115,26 +117,31 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
     return na && nb && x < y + nb && y < x + na;
 }
 
-int check_shape_fused(int64_t n, const hc_shape_t& s) {
-    if (n < 0) return HC_ERR_SHAPE;
-    if (s.hc < 1 || s.d < 1) return HC_ERR_SHAPE;
-    if (s.d % 256 != 0) return HC_ERR_SHAPE;
-    if (n > 0x7FFFFFFFLL) return HC_ERR_SHAPE;
-    if (s.hc != kHC) return HC_ERR_UNSUPPORTED;
-    if (s.d > 5120) return HC_ERR_UNSUPPORTED;
-    if (s.sinkhorn_iters < 1) return HC_ERR_ARG;
-    if (!std::isfinite(s.hc_eps) || s.hc_eps < 0.f || !std::isfinite(s.norm_eps) || s.norm_eps < 0.f)
-        return HC_ERR_ARG;
-    return HC_OK;
-}
-
-// shape rules of the tail-of-stack calls: d a multiple of 8 up to 5120, only norm_eps is used
-int check_shape_final(int64_t n, const hc_shape_t& s) {
-    if (n < 0 || s.hc < 1 || s.d < 1 || s.d % 8 != 0 || n > 0x7FFFFFFFLL) return HC_ERR_SHAPE;
-    if (s.hc != kHC || s.d > kFinalMaxD) return HC_ERR_UNSUPPORTED;
+// Shape rules of every call: hc in 1..8 and d a positive multiple of 8 up to 65536 (the fused
+// kernel takes hc = 4 with d a multiple of 256 up to 5120, the generic kernels the rest).
+int check_shape(int64_t n, const hc_shape_t& s, bool reading) {
+    if (n < 0 || n > 0x7FFFFFFFLL) return HC_ERR_SHAPE;
+    if (s.hc < 1 || s.d < 1 || s.d % 8 != 0) return HC_ERR_SHAPE;
+    if (s.hc > kMaxHc || s.d > kMaxD) return HC_ERR_UNSUPPORTED;
+    if (reading && s.sinkhorn_iters < 1) return HC_ERR_ARG;
+    if (reading && (!std::isfinite(s.hc_eps) || s.hc_eps < 0.f)) return HC_ERR_ARG;
     if (!std::isfinite(s.norm_eps) || s.norm_eps < 0.f) return HC_ERR_ARG;
     return HC_OK;
 }
+
+bool fused_shape(const hc_shape_t& s) { return s.hc == kHC && s.d % 256 == 0 && s.d <= 5120; }
+
+// byte sizes of the per-token arrays of n tokens
+struct Sizes {
+    size_t x, y, c, k;  // streams [n, hc, d] bf16, rows [n, d] bf16, [n, hc] fp32, [n, hc, hc] fp32
+    Sizes(int64_t n, const hc_shape_t& s) {
+        const size_t N = static_cast<size_t>(n), H = static_cast<size_t>(s.hc), D = static_cast<size_t>(s.d);
+        x = N * H * D * 2;
+        y = N * D * 2;
+        c = N * H * 4;
+        k = N * H * H * 4;
+    }
+};
 
 // true if any output overlaps an input or another output (null entries are skipped)
 bool any_overlap(const void* const* outs, const size_t* osz, int no, const void* const* ins, const size_t* isz,
@@ -165,29 +172,69 @@ int launch_status(int internal) { return internal == 0 ? HC_OK : internal == -3 
 
 using namespace hc;
 
+// the reading half of one sublayer on streams X (hc_pre_step; the second half of the post calls)
+static int reading_half(const void* X, const float* pre_mix, bool identity, const hc_params_t& p, int64_t n,
+                        const hc_shape_t& s, void* y_normed, float* pre, float* post, float* comb, float* mixes,
+                        void* workspace, cudaStream_t stream) {
+    GenericArgs g = {};
+    g.X = X;
+    g.pre_mix = pre_mix;
+    g.identity = identity ? 1 : 0;
+    g.planes = p.hc_fn_planes;
+    g.hc_scale = p.hc_scale;
+    g.hc_base = p.hc_base;
+    g.norm_w = p.norm_w;
+    g.y_normed = y_normed;
+    g.pre_out = pre;
+    g.post_out = post;
+    g.comb_out = comb;
+    g.mixes_out = mixes;
+    g.workspace = workspace;
+    g.n = n;
+    g.hc = s.hc;
+    g.d = s.d;
+    g.iters = s.sinkhorn_iters;
+    g.hc_eps = s.hc_eps;
+    g.norm_eps = s.norm_eps;
+    return launch_generic_reading(g, stream);
+}
+
 static int post_then_pre_impl(const void* delta, const void* X, const float* post, const float* comb,
                               const float* pre_mix, hc_params_t next, int64_t n, hc_shape_t s, void* X_out,
                               void* y_normed, float* pre_out, float* post_out, float* comb_out, void* stream_mean,
-                              void* workspace, hc_stream_t stream) {
+                              void* workspace, bool noalloc, hc_stream_t stream) {
     if (!delta || !X || !post || !comb || !pre_mix || !X_out || !y_normed || !pre_out || !post_out || !comb_out ||
-        !workspace)
+        (!workspace && !noalloc))
         return HC_ERR_NULL;
     int st = check_params(next);
     if (st != HC_OK) return st;
-    st = check_shape_fused(n, s);
+    st = check_shape(n, s, true);
     if (st != HC_OK) return st;
-    const void* ptrs[11] = {delta, X, post, comb, pre_mix, X_out, y_normed, pre_out, post_out, comb_out, workspace};
+    const void* ptrs[10] = {delta, X, post, comb, pre_mix, X_out, y_normed, pre_out, post_out, comb_out};
     for (const void* q : ptrs)
         if (!aligned16(q)) return HC_ERR_ALIGN;
-    const size_t N = static_cast<size_t>(n);
-    const size_t xb = N * kHC * s.d * 2, yb = N * s.d * 2, cb = N * 16, kb = N * 64;
+    if ((workspace && !aligned16(workspace)) || (stream_mean && !aligned16(stream_mean))) return HC_ERR_ALIGN;
+    const Sizes z(n, s);
     const void* ins[5] = {delta, X, post, comb, pre_mix};
-    const size_t isz[5] = {yb, xb, cb, kb, cb};
-    if (stream_mean && !aligned16(stream_mean)) return HC_ERR_ALIGN;
+    const size_t isz[5] = {z.y, z.x, z.c, z.k, z.c};
     const void* outs[7] = {X_out, y_normed, pre_out, post_out, comb_out, workspace, stream_mean};
-    const size_t osz[7] = {xb, yb, cb, cb, kb, workspace_bytes(), yb};
+    const size_t osz[7] = {z.x, z.y, z.c, z.c, z.k, workspace_bytes(), z.y};
     if (any_overlap(outs, osz, 7, ins, isz, 5)) return HC_ERR_ALIAS;
     if (n == 0) return HC_OK;
+    if (noalloc) {
+        // the scratch is the library's fixed array: find this device's copy (first call only) and make
+        // sure the launch needs no more of it than it holds
+        size_t capacity = 0;
+        if (noalloc_workspace(&workspace, &capacity) != 0) return HC_ERR_CUDA;
+        if (workspace_bytes() > capacity) return HC_ERR_UNSUPPORTED;
+    }
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (!fused_shape(s)) {
+        st = launch_generic_post(X, delta, post, comb, X_out, stream_mean, n, s.hc, s.d, cs);
+        if (st != 0) return launch_status(st);
+        return launch_status(reading_half(X_out, pre_mix, false, next, n, s, y_normed, pre_out, post_out, comb_out,
+                                          nullptr, workspace, cs));
+    }
     FusedArgs a = {};
     a.mode = kModePost;
     a.X = X;
@@ -211,9 +258,8 @@ static int post_then_pre_impl(const void* delta, const void* X, const float* pos
     a.iters = s.sinkhorn_iters;
     a.hc_eps = s.hc_eps;
     a.norm_eps = s.norm_eps;
-    return launch_status(launch_fused(a, reinterpret_cast<cudaStream_t>(stream)));
+    return launch_status(launch_fused(a, cs));
 }
-
 
 extern "C" {
 
@@ -221,8 +267,8 @@ const char* hc_status_string(int status) {
     switch (status) {
         case HC_OK: return "ok";
         case HC_ERR_NULL: return "a required pointer is NULL";
-        case HC_ERR_SHAPE: return "invalid shape (n < 0, or d not a positive multiple of the required granule)";
-        case HC_ERR_UNSUPPORTED: return "configuration not implemented by the GPU path (hc != 4 or d > 5120)";
+        case HC_ERR_SHAPE: return "invalid shape (n < 0, or hc < 1, or d not a positive multiple of 8)";
+        case HC_ERR_UNSUPPORTED: return "configuration not implemented (hc > 8, d > 65536, or no cooperative launch)";
         case HC_ERR_ALIGN: return "a device pointer is not 16-byte aligned";
         case HC_ERR_ALIAS: return "an output overlaps an input or another output";
         case HC_ERR_ARG: return "invalid scalar argument (sinkhorn_iters < 1, or an eps negative or not finite)";
@@ -243,14 +289,15 @@ int hc_prepare_params_size(int hc, int d, size_t* bytes) {
 int hc_prepare_params(const float* hc_fn, int hc, int d, void* planes, hc_stream_t stream) {
     if (!hc_fn || !planes) return HC_ERR_NULL;
     if (hc < 1 || d < 1 || d % 8 != 0) return HC_ERR_SHAPE;
-    if (hc != kHC) return HC_ERR_UNSUPPORTED;
+    if (hc > kMaxHc || d > kMaxD) return HC_ERR_UNSUPPORTED;
     if (!aligned16(hc_fn) || !aligned16(planes)) return HC_ERR_ALIGN;
     const long long D = static_cast<long long>(hc) * d;
-    if (overlap(hc_fn, static_cast<size_t>(kMix * D) * 4, planes, static_cast<size_t>(3 * kMix * D) * 2))
+    const long long M = static_cast<long long>(2 + hc) * hc;
+    if (overlap(hc_fn, static_cast<size_t>(M * D) * 4, planes, static_cast<size_t>(3 * M * D) * 2))
         return HC_ERR_ALIAS;
-    const long long work = kMix * D;
+    const long long work = M * D;
     hc_prepare_kernel<<<grid_for(work, 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        hc_fn, static_cast<__nv_bfloat16*>(planes), D);
+        hc_fn, static_cast<__nv_bfloat16*>(planes), hc, D);
     return cuda_status(cudaGetLastError());
 }
 
@@ -258,16 +305,18 @@ int hc_post(const void* delta, const void* X, const float* post, const float* co
             void* X_out, hc_stream_t stream) {
     if (!delta || !X || !post || !comb || !X_out) return HC_ERR_NULL;
     if (n < 0 || s.hc < 1 || s.d < 1 || s.d % 8 != 0 || n > (1LL << 40)) return HC_ERR_SHAPE;
-    if (s.hc != kHC) return HC_ERR_UNSUPPORTED;
+    if (s.hc > kMaxHc || s.d > kMaxD) return HC_ERR_UNSUPPORTED;
     if (!aligned16(delta) || !aligned16(X) || !aligned16(post) || !aligned16(comb) || !aligned16(X_out))
         return HC_ERR_ALIGN;
-    const size_t xb = static_cast<size_t>(n) * kHC * s.d * 2, db = static_cast<size_t>(n) * s.d * 2;
-    if ((X_out != X && overlap(X_out, xb, X, xb)) || overlap(X_out, xb, delta, db) ||
-        overlap(X_out, xb, post, static_cast<size_t>(n) * 16) || overlap(X_out, xb, comb, static_cast<size_t>(n) * 64))
+    const Sizes z(n, s);
+    if ((X_out != X && overlap(X_out, z.x, X, z.x)) || overlap(X_out, z.x, delta, z.y) ||
+        overlap(X_out, z.x, post, z.c) || overlap(X_out, z.x, comb, z.k))
         return HC_ERR_ALIAS;
     if (n == 0) return HC_OK;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (s.hc != kHC) return launch_status(launch_generic_post(X, delta, post, comb, X_out, nullptr, n, s.hc, s.d, cs));
     const int dv = s.d / 8;
-    hc_post_kernel<<<grid_for(n * dv, 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+    hc_post_kernel<<<grid_for(n * dv, 256), 256, 0, cs>>>(
         static_cast<const uint4*>(X), static_cast<const uint4*>(delta), reinterpret_cast<const float4*>(post),
         reinterpret_cast<const float4*>(comb), static_cast<uint4*>(X_out), n, dv);
     return cuda_status(cudaGetLastError());
@@ -284,24 +333,21 @@ int hc_pre_step(const void* X, const float* pre_mix, hc_params_t p, int64_t n, h
     if (!X || !pre_mix || !y_normed || !pre || !post || !comb || !workspace) return HC_ERR_NULL;
     int st = check_params(p);
     if (st != HC_OK) return st;
-    st = check_shape_fused(n, s);
+    st = check_shape(n, s, true);
     if (st != HC_OK) return st;
     if (!aligned16(X) || !aligned16(pre_mix) || !aligned16(y_normed) || !aligned16(pre) || !aligned16(post) ||
         !aligned16(comb) || !aligned16(workspace))
         return HC_ERR_ALIGN;
-    const size_t N = static_cast<size_t>(n);
-    const size_t xb = N * kHC * s.d * 2, yb = N * s.d * 2, cb = N * 16, kb = N * 64;
+    const Sizes z(n, s);
     const void* outs[5] = {y_normed, pre, post, comb, workspace};
-    const size_t osz[5] = {yb, cb, cb, kb, workspace_bytes()};
+    const size_t osz[5] = {z.y, z.c, z.c, z.k, workspace_bytes()};
     const void* ins[2] = {X, pre_mix};
-    const size_t isz[2] = {xb, cb};
-    for (int i = 0; i < 5; ++i) {
-        for (int j = 0; j < 2; ++j)
-            if (overlap(outs[i], osz[i], ins[j], isz[j])) return HC_ERR_ALIAS;
-        for (int j = i + 1; j < 5; ++j)
-            if (overlap(outs[i], osz[i], outs[j], osz[j])) return HC_ERR_ALIAS;
-    }
+    const size_t isz[2] = {z.x, z.c};
+    if (any_overlap(outs, osz, 5, ins, isz, 2)) return HC_ERR_ALIAS;
     if (n == 0) return HC_OK;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (!fused_shape(s))
+        return launch_status(reading_half(X, pre_mix, false, p, n, s, y_normed, pre, post, comb, nullptr, workspace, cs));
     FusedArgs a = {};
     a.mode = kModePre;
     a.X = X;
@@ -320,14 +366,14 @@ int hc_pre_step(const void* X, const float* pre_mix, hc_params_t p, int64_t n, h
     a.iters = s.sinkhorn_iters;
     a.hc_eps = s.hc_eps;
     a.norm_eps = s.norm_eps;
-    return launch_status(launch_fused(a, reinterpret_cast<cudaStream_t>(stream)));
+    return launch_status(launch_fused(a, cs));
 }
 
 int hc_post_then_pre(const void* delta, const void* X, const float* post, const float* comb, const float* pre_mix,
                      hc_params_t next, int64_t n, hc_shape_t s, void* X_out, void* y_normed, float* pre_out,
                      float* post_out, float* comb_out, void* workspace, hc_stream_t stream) {
     return post_then_pre_impl(delta, X, post, comb, pre_mix, next, n, s, X_out, y_normed, pre_out, post_out,
-                              comb_out, nullptr, workspace, stream);
+                              comb_out, nullptr, workspace, false, stream);
 }
 
 int hc_post_then_pre_tap(const void* delta, const void* X, const float* post, const float* comb,
@@ -336,64 +382,14 @@ int hc_post_then_pre_tap(const void* delta, const void* X, const float* post, co
                          void* workspace, hc_stream_t stream) {
     if (!stream_mean) return HC_ERR_NULL;
     return post_then_pre_impl(delta, X, post, comb, pre_mix, next, n, s, X_out, y_normed, pre_out, post_out,
-                              comb_out, stream_mean, workspace, stream);
+                              comb_out, stream_mean, workspace, false, stream);
 }
 
 int hc_post_then_pre_noalloc(const void* delta, const void* X, const float* post, const float* comb,
                              const float* pre_mix, hc_params_t next, int64_t n, hc_shape_t s, void* X_out,
                              void* y_normed, float* pre_out, float* post_out, float* comb_out, hc_stream_t stream) {
-    // the same checks as hc_post_then_pre, before anything touches the device
-    if (!delta || !X || !post || !comb || !pre_mix || !X_out || !y_normed || !pre_out || !post_out || !comb_out)
-        return HC_ERR_NULL;
-    int st = check_params(next);
-    if (st != HC_OK) return st;
-    st = check_shape_fused(n, s);
-    if (st != HC_OK) return st;
-    const void* ptrs[10] = {delta, X, post, comb, pre_mix, X_out, y_normed, pre_out, post_out, comb_out};
-    for (const void* q : ptrs)
-        if (!aligned16(q)) return HC_ERR_ALIGN;
-    const size_t N = static_cast<size_t>(n);
-    const size_t xb = N * kHC * s.d * 2, yb = N * s.d * 2, cb = N * 16, kb = N * 64;
-    const void* ins[5] = {delta, X, post, comb, pre_mix};
-    const size_t isz[5] = {yb, xb, cb, kb, cb};
-    const void* outs[5] = {X_out, y_normed, pre_out, post_out, comb_out};
-    const size_t osz[5] = {xb, yb, cb, cb, kb};
-    for (int i = 0; i < 5; ++i) {
-        for (int j = 0; j < 5; ++j)
-            if (overlap(outs[i], osz[i], ins[j], isz[j])) return HC_ERR_ALIAS;
-        for (int j = i + 1; j < 5; ++j)
-            if (overlap(outs[i], osz[i], outs[j], osz[j])) return HC_ERR_ALIAS;
-    }
-    if (n == 0) return HC_OK;
-    // the scratch is the library's fixed array: find this device's copy (first call only) and make
-    // sure the launch needs no more of it than it holds
-    void* ws = nullptr;
-    size_t capacity = 0;
-    if (noalloc_workspace(&ws, &capacity) != 0) return HC_ERR_CUDA;
-    if (workspace_bytes() > capacity) return HC_ERR_UNSUPPORTED;
-    FusedArgs a = {};
-    a.mode = kModePost;
-    a.X = X;
-    a.delta = delta;
-    a.post = post;
-    a.comb = comb;
-    a.pre_mix = pre_mix;
-    a.planes = next.hc_fn_planes;
-    a.hc_scale = next.hc_scale;
-    a.hc_base = next.hc_base;
-    a.norm_w = next.norm_w;
-    a.X_out = X_out;
-    a.y_normed = y_normed;
-    a.pre_out = pre_out;
-    a.post_out = post_out;
-    a.comb_out = comb_out;
-    a.workspace = ws;
-    a.n = n;
-    a.d = s.d;
-    a.iters = s.sinkhorn_iters;
-    a.hc_eps = s.hc_eps;
-    a.norm_eps = s.norm_eps;
-    return launch_status(launch_fused(a, reinterpret_cast<cudaStream_t>(stream)));
+    return post_then_pre_impl(delta, X, post, comb, pre_mix, next, n, s, X_out, y_normed, pre_out, post_out,
+                              comb_out, nullptr, nullptr, true, stream);
 }
 
 int hc_expand_pre_step(const void* h, hc_params_t p, int64_t n, hc_shape_t s, void* X_out, void* y_normed, float* pre,
@@ -401,19 +397,25 @@ int hc_expand_pre_step(const void* h, hc_params_t p, int64_t n, hc_shape_t s, vo
     if (!h || !X_out || !y_normed || !pre || !post || !comb || !workspace) return HC_ERR_NULL;
     int st = check_params(p);
     if (st != HC_OK) return st;
-    st = check_shape_fused(n, s);
+    st = check_shape(n, s, true);
     if (st != HC_OK) return st;
     const void* ptrs[7] = {h, X_out, y_normed, pre, post, comb, workspace};
     for (const void* q : ptrs)
         if (!aligned16(q)) return HC_ERR_ALIGN;
-    const size_t N = static_cast<size_t>(n);
-    const size_t xb = N * kHC * s.d * 2, yb = N * s.d * 2, cb = N * 16, kb = N * 64;
+    const Sizes z(n, s);
     const void* ins[1] = {h};
-    const size_t isz[1] = {yb};
+    const size_t isz[1] = {z.y};
     const void* outs[6] = {X_out, y_normed, pre, post, comb, workspace};
-    const size_t osz[6] = {xb, yb, cb, cb, kb, workspace_bytes()};
+    const size_t osz[6] = {z.x, z.y, z.c, z.c, z.k, workspace_bytes()};
     if (any_overlap(outs, osz, 6, ins, isz, 1)) return HC_ERR_ALIAS;
     if (n == 0) return HC_OK;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (!fused_shape(s)) {
+        st = launch_generic_expand(h, X_out, n, s.hc, s.d, cs);
+        if (st != 0) return launch_status(st);
+        return launch_status(reading_half(X_out, nullptr, true, p, n, s, y_normed, pre, post, comb, nullptr,
+                                          workspace, cs));
+    }
     FusedArgs a = {};
     a.mode = kModeExpand;
     a.embed = h;
@@ -432,50 +434,15 @@ int hc_expand_pre_step(const void* h, hc_params_t p, int64_t n, hc_shape_t s, vo
     a.iters = s.sinkhorn_iters;
     a.hc_eps = s.hc_eps;
     a.norm_eps = s.norm_eps;
-    return launch_status(launch_fused(a, reinterpret_cast<cudaStream_t>(stream)));
+    return launch_status(launch_fused(a, cs));
 }
 
-int hc_final(const void* X, const float* pre_mix, const float* norm_w, int64_t n, hc_shape_t s, void* z,
-             hc_stream_t stream) {
-    if (!X || !pre_mix || !norm_w || !z) return HC_ERR_NULL;
-    int st = check_shape_final(n, s);
-    if (st != HC_OK) return st;
-    if (!aligned16(X) || !aligned16(pre_mix) || !aligned16(norm_w) || !aligned16(z)) return HC_ERR_ALIGN;
-    const size_t N = static_cast<size_t>(n);
-    const void* ins[3] = {X, pre_mix, norm_w};
-    const size_t isz[3] = {N * kHC * s.d * 2, N * 16, static_cast<size_t>(s.d) * 4};
-    const void* outs[1] = {z};
-    const size_t osz[1] = {N * s.d * 2};
-    if (any_overlap(outs, osz, 1, ins, isz, 3)) return HC_ERR_ALIAS;
-    if (n == 0) return HC_OK;
-    FinalArgs a = {};
-    a.X = X;
-    a.pre_mix = pre_mix;
-    a.norm_w = norm_w;
-    a.z = z;
-    a.n = n;
-    a.d = s.d;
-    a.norm_eps = s.norm_eps;
-    return launch_status(launch_final(a, reinterpret_cast<cudaStream_t>(stream)));
-}
-
-int hc_post_then_final(const void* delta, const void* X, const float* post, const float* comb, const float* pre_mix,
-                       const float* norm_w, int64_t n, hc_shape_t s, void* X_out, void* z, hc_stream_t stream) {
-    if (!delta || !X || !post || !comb || !pre_mix || !norm_w || !z) return HC_ERR_NULL;
-    int st = check_shape_final(n, s);
-    if (st != HC_OK) return st;
-    const void* ptrs[7] = {delta, X, post, comb, pre_mix, norm_w, z};
-    for (const void* q : ptrs)
-        if (!aligned16(q)) return HC_ERR_ALIGN;
-    if (X_out && !aligned16(X_out)) return HC_ERR_ALIGN;
-    const size_t N = static_cast<size_t>(n);
-    const size_t xb = N * kHC * s.d * 2, yb = N * s.d * 2;
-    const void* ins[6] = {delta, X, post, comb, pre_mix, norm_w};
-    const size_t isz[6] = {yb, xb, N * 16, N * 64, N * 16, static_cast<size_t>(s.d) * 4};
-    const void* outs[2] = {z, X_out};
-    const size_t osz[2] = {yb, xb};
-    if (any_overlap(outs, osz, 2, ins, isz, 6)) return HC_ERR_ALIAS;
-    if (n == 0) return HC_OK;
+// the tail of the stack: the 4-stream kernel for hc = 4 and d <= 5120, the generic one otherwise
+static int final_impl(const void* delta, const void* X, const float* post, const float* comb, const float* pre_mix,
+                      const float* norm_w, int64_t n, const hc_shape_t& s, void* X_out, void* z, cudaStream_t cs) {
+    if (s.hc != kHC || s.d > kFinalMaxD)
+        return launch_status(launch_generic_final(X, delta, post, comb, pre_mix, norm_w, X_out, z, n, s.hc, s.d,
+                                                  s.norm_eps, cs));
     FinalArgs a = {};
     a.X = X;
     a.delta = delta;
@@ -488,7 +455,43 @@ int hc_post_then_final(const void* delta, const void* X, const float* post, cons
     a.n = n;
     a.d = s.d;
     a.norm_eps = s.norm_eps;
-    return launch_status(launch_final(a, reinterpret_cast<cudaStream_t>(stream)));
+    return launch_status(launch_final(a, cs));
+}
+
+int hc_final(const void* X, const float* pre_mix, const float* norm_w, int64_t n, hc_shape_t s, void* z,
+             hc_stream_t stream) {
+    if (!X || !pre_mix || !norm_w || !z) return HC_ERR_NULL;
+    int st = check_shape(n, s, false);
+    if (st != HC_OK) return st;
+    if (!aligned16(X) || !aligned16(pre_mix) || !aligned16(norm_w) || !aligned16(z)) return HC_ERR_ALIGN;
+    const Sizes q(n, s);
+    const void* ins[3] = {X, pre_mix, norm_w};
+    const size_t isz[3] = {q.x, q.c, static_cast<size_t>(s.d) * 4};
+    const void* outs[1] = {z};
+    const size_t osz[1] = {q.y};
+    if (any_overlap(outs, osz, 1, ins, isz, 3)) return HC_ERR_ALIAS;
+    if (n == 0) return HC_OK;
+    return final_impl(nullptr, X, nullptr, nullptr, pre_mix, norm_w, n, s, nullptr, z,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+int hc_post_then_final(const void* delta, const void* X, const float* post, const float* comb, const float* pre_mix,
+                       const float* norm_w, int64_t n, hc_shape_t s, void* X_out, void* z, hc_stream_t stream) {
+    if (!delta || !X || !post || !comb || !pre_mix || !norm_w || !z) return HC_ERR_NULL;
+    int st = check_shape(n, s, false);
+    if (st != HC_OK) return st;
+    const void* ptrs[7] = {delta, X, post, comb, pre_mix, norm_w, z};
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return HC_ERR_ALIGN;
+    if (X_out && !aligned16(X_out)) return HC_ERR_ALIGN;
+    const Sizes q(n, s);
+    const void* ins[6] = {delta, X, post, comb, pre_mix, norm_w};
+    const size_t isz[6] = {q.y, q.x, q.c, q.k, q.c, static_cast<size_t>(s.d) * 4};
+    const void* outs[2] = {z, X_out};
+    const size_t osz[2] = {q.y, q.x};
+    if (any_overlap(outs, osz, 2, ins, isz, 6)) return HC_ERR_ALIAS;
+    if (n == 0) return HC_OK;
+    return final_impl(delta, X, post, comb, pre_mix, norm_w, n, s, X_out, z, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float* mixes, void* workspace,
@@ -496,16 +499,20 @@ int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float*
     if (!X || !mixes || !p.hc_fn_planes || !workspace) return HC_ERR_NULL;
     hc_shape_t s2 = s;
     if (s2.sinkhorn_iters < 1) s2.sinkhorn_iters = 1;
-    int st = check_shape_fused(n, s2);
+    int st = check_shape(n, s2, true);
     if (st != HC_OK) return st;
     if (!aligned16(X) || !aligned16(mixes) || !aligned16(p.hc_fn_planes) || !aligned16(workspace))
         return HC_ERR_ALIGN;
-    const size_t N = static_cast<size_t>(n);
-    if (overlap(mixes, N * kMix * 4, X, N * kHC * s.d * 2) ||
-        overlap(workspace, workspace_bytes(), X, N * kHC * s.d * 2) ||
-        overlap(workspace, workspace_bytes(), mixes, N * kMix * 4))
+    const Sizes z(n, s);
+    const size_t mb = static_cast<size_t>(n) * (2 + s.hc) * s.hc * 4;
+    if (overlap(mixes, mb, X, z.x) || overlap(workspace, workspace_bytes(), X, z.x) ||
+        overlap(workspace, workspace_bytes(), mixes, mb))
         return HC_ERR_ALIAS;
     if (n == 0) return HC_OK;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (!fused_shape(s2))
+        return launch_status(reading_half(X, nullptr, false, p, n, s2, nullptr, nullptr, nullptr, nullptr, mixes,
+                                          workspace, cs));
     // the kernel reads scale/base/norm_w unconditionally: point them at the planes (never used)
     FusedArgs a = {};
     a.mode = kModePre;
@@ -517,11 +524,11 @@ int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float*
     a.mixes_out = mixes;
     a.workspace = workspace;
     a.n = n;
-    a.d = s.d;
+    a.d = s2.d;
     a.iters = s2.sinkhorn_iters;
     a.hc_eps = s2.hc_eps;
     a.norm_eps = s2.norm_eps;
-    return launch_status(launch_fused(a, reinterpret_cast<cudaStream_t>(stream)));
+    return launch_status(launch_fused(a, cs));
 }
 
 int hc_plan_tiles(int64_t n, int d, int ctas, int* group, int* tile_m, int64_t* num_tiles) {

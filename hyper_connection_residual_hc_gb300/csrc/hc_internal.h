@@ -69,6 +69,46 @@ constexpr int kFinalMaxD = 5120;
 // Launches the tail-of-stack kernel; returns 0 or -7.
 int launch_final(const FinalArgs& a, cudaStream_t stream);
 
+// Row of the prepared weight planes that holds plane pl (0 hi, 1 mid, 2 lo) of mix m, for hc
+// streams and M = (2 + hc) * hc mixes: the fused kernel's grouping at hc = 4 (row 36h + 12 pl + i
+// for mix 12h + i, so that one warp drains one half of the mixes from contiguous accumulator
+// columns), plane-major (row pl * M + m) for any other hc.
+__host__ __device__ inline int plane_row(int hc, int M, int pl, int m) {
+    return hc == 4 ? 36 * (m / 12) + 12 * pl + m % 12 : pl * M + m;
+}
+
+// The generic path (any hc in 1..8, any d multiple of 8): plain CUDA-core kernels for the shapes
+// the fused kernel does not take.
+struct GenericArgs {
+    const void* X;           // bf16 [n, hc, d]: the streams the reading half reads
+    const float* pre_mix;    // fp32 [n, hc], unless identity
+    int identity;            // 1: pre_mix is 1/hc for every stream (head of the stack)
+    const void* planes;      // bf16 planes of hc_prepare_params
+    const float* hc_scale;
+    const float* hc_base;
+    const float* norm_w;
+    void* y_normed;          // bf16 [n, d], or null (debug mixes)
+    float* pre_out;
+    float* post_out;
+    float* comb_out;
+    float* mixes_out;        // fp32 [n, M]: debug mixes instead of the coefficients, or null
+    void* workspace;         // workspace_bytes(): raw mixes and sums of squares, a chunk of tokens at a time
+    int64_t n;
+    int hc;
+    int d;
+    int iters;
+    float hc_eps;
+    float norm_eps;
+};
+size_t generic_tokens_per_chunk(int hc);
+int launch_generic_post(const void* X, const void* delta, const float* post, const float* comb, void* X_out,
+                        void* mean_out, int64_t n, int hc, int d, cudaStream_t stream);
+int launch_generic_expand(const void* h, void* X_out, int64_t n, int hc, int d, cudaStream_t stream);
+int launch_generic_reading(const GenericArgs& a, cudaStream_t stream);
+int launch_generic_final(const void* X, const void* delta, const float* post, const float* comb,
+                         const float* pre_mix, const float* norm_w, void* X_out, void* z, int64_t n, int hc, int d,
+                         float eps, cudaStream_t stream);
+
 // Reads (and optionally clears) the device error word of the current device.
 int read_device_error(unsigned int* word, int clear, cudaStream_t stream);
 

@@ -53,8 +53,8 @@ typedef struct CUstream_st* hc_stream_t; /* identical to cudaStream_t */
 enum {
     HC_OK = 0,
     HC_ERR_NULL = -1,        /* a required pointer is NULL */
-    HC_ERR_SHAPE = -2,       /* n < 0, or d not a positive multiple of the supported granule */
-    HC_ERR_UNSUPPORTED = -3, /* a valid configuration this GPU path does not implement (hc != 4, d > 5120) */
+    HC_ERR_SHAPE = -2,       /* n < 0, or hc < 1, or d not a positive multiple of 8 */
+    HC_ERR_UNSUPPORTED = -3, /* a valid configuration not implemented (hc > 8, d > 65536, no cooperative launch) */
     HC_ERR_ALIGN = -4,       /* a device pointer is not 16-byte aligned */
     HC_ERR_ALIAS = -5,       /* an output overlaps an input or another output (see each call) */
     HC_ERR_ARG = -6,         /* sinkhorn_iters < 1, or an eps negative or not finite */
@@ -65,9 +65,10 @@ enum {
 /* Problem shape and scalar constants. The model's values ("Router" page, config.json excerpt):
  * hc = 4 (hc_mult), d = 5120 (dim), sinkhorn_iters = 20, hc_eps = 1e-6, norm_eps = 1e-20. */
 typedef struct {
-    int hc;             /* streams; the GPU path implements hc == 4 */
-    int d;              /* width of one stream: a multiple of 256, at most 5120, for the fused calls;
-                           a multiple of 8 for hc_post */
+    int hc;             /* streams, 1..8. hc = 4 with d a multiple of 256 up to 5120 (the model's shape)
+                           runs on the fused tensor-core kernel; every other shape on plain CUDA-core
+                           kernels with the same results (slower) */
+    int d;              /* width of one stream: a multiple of 8, at most 65536 */
     int sinkhorn_iters; /* >= 1: one softmax + column normalisation, then iters-1 row+column rounds */
     float hc_eps;       /* >= 0, finite: the eps of pre and of the Sinkhorn normalisations */
     float norm_eps;     /* >= 0, finite: used by both the mixes statistic and the sublayer RMSNorm */
@@ -91,7 +92,7 @@ int hc_prepare_params_size(int hc, int d, size_t* bytes);
  * equals every fp32 weight exactly, laid out for the fused kernels' tensor-core projection,
  * into `planes` [device] (hc_prepare_params_size bytes, 16-byte aligned). Run it once per
  * parameter set (weights are static); the planes stay valid while hc_fn is unchanged.
- * No counterpart on the pages: it is this library's weight packing. hc must be 4. */
+ * No counterpart on the pages: it is this library's weight packing. hc in 1..8. */
 int hc_prepare_params(const float* hc_fn, int hc, int d, void* planes, hc_stream_t stream);
 
 /* Size in bytes of the workspace the fused calls (hc_pre_step, hc_post_then_pre,

@@ -147,7 +147,8 @@ def _uniform_comb(iters, eps, hc=4):
 def pin_uniform_logits_closed_form(lib):
     """mixes == 0 (hc_fn = 0, base = 0): pre = 1/2 + eps, post = 1, comb = the scalar recurrence."""
     for hc, iters, eps in [(4, 20, 1e-6), (4, 50, 1e-6), (4, 1, 1e-3), (2, 7, 1e-2), (3, 5, 0.0),
-                           (4, 6, 0.9), (2, 9, 0.5), (4, 3, 2.0)]:
+                           (4, 6, 0.9), (2, 9, 0.5), (4, 3, 2.0), (8, 20, 1e-6), (8, 4, 0.3), (1, 5, 1e-2),
+                           (5, 11, 1e-4)]:
         M = (2 + hc) * hc
         pre, post, comb = orc.split_sinkhorn(np.zeros((2, M)), np.array([1.3, 0.7, 2.0], np.float32),
                                              np.zeros(M, np.float32), hc, iters, eps, lib=lib)

@@ -82,9 +82,10 @@ def test_pre_step_validation(lib):
     _expect(hc.HC_ERR_NULL, hc.hc_pre_step, A[0], A[1], _p(), 8, s, A[2], A[3], A[4], A[5], None, st)
     _expect(hc.HC_ERR_NULL, hc.hc_pre_step, A[0], A[1], hc.params(None, A[11], A[12], A[13]), 8, s, A[2], A[3], A[4], A[5], W, st)
     _expect(hc.HC_ERR_SHAPE, hc.hc_pre_step, A[0], A[1], _p(), -1, s, A[2], A[3], A[4], A[5], W, st)
-    _expect(hc.HC_ERR_SHAPE, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(d=5000), A[2], A[3], A[4], A[5], W, st)
-    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(hc=2), A[2], A[3], A[4], A[5], W, st)
-    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(d=5376), A[2], A[3], A[4], A[5], W, st)
+    _expect(hc.HC_ERR_SHAPE, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(d=5004), A[2], A[3], A[4], A[5], W, st)
+    _expect(hc.HC_ERR_SHAPE, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(hc=0), A[2], A[3], A[4], A[5], W, st)
+    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(hc=9), A[2], A[3], A[4], A[5], W, st)
+    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(d=65544), A[2], A[3], A[4], A[5], W, st)
     _expect(hc.HC_ERR_ARG, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(sinkhorn_iters=0), A[2], A[3], A[4], A[5], W, st)
     _expect(hc.HC_ERR_ARG, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(hc_eps=float("nan")), A[2], A[3], A[4], A[5], W, st)
     _expect(hc.HC_ERR_ARG, hc.hc_pre_step, A[0], A[1], _p(), 8, hc.shape(norm_eps=-1.0), A[2], A[3], A[4], A[5], W, st)
@@ -180,7 +181,7 @@ def test_expand_pre_step_validation(lib):
     bad[0] = A[0] + 2
     _expect(hc.HC_ERR_ALIGN, hc.hc_expand_pre_step, *bad)
     bad = list(args)
-    bad[3] = hc.shape(d=264)
+    bad[3] = hc.shape(d=260)
     _expect(hc.HC_ERR_SHAPE, hc.hc_expand_pre_step, *bad)
     bad = list(args)
     bad[3] = hc.shape(sinkhorn_iters=0)
@@ -200,8 +201,8 @@ def test_final_validation(lib):
         _expect(hc.HC_ERR_NULL, hc.hc_final, *bad)
     _expect(hc.HC_ERR_SHAPE, hc.hc_final, A[0], A[1], A[2], 8, hc.shape(d=12), A[3], st)
     _expect(hc.HC_ERR_SHAPE, hc.hc_final, A[0], A[1], A[2], -1, s, A[3], st)
-    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_final, A[0], A[1], A[2], 8, hc.shape(d=5128), A[3], st)
-    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_final, A[0], A[1], A[2], 8, hc.shape(hc=8), A[3], st)
+    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_final, A[0], A[1], A[2], 8, hc.shape(d=65544), A[3], st)
+    _expect(hc.HC_ERR_UNSUPPORTED, hc.hc_final, A[0], A[1], A[2], 8, hc.shape(hc=9), A[3], st)
     _expect(hc.HC_ERR_ARG, hc.hc_final, A[0], A[1], A[2], 8, hc.shape(norm_eps=float("inf")), A[3], st)
     _expect(hc.HC_ERR_ALIGN, hc.hc_final, A[0], A[1], A[2] + 4, 8, s, A[3], st)
     _expect(hc.HC_ERR_ALIAS, hc.hc_final, A[0], A[1], A[2], 8, s, A[0] + 16, st)
