@@ -32,7 +32,7 @@ HC_ERR_DEVICE = -8
 SYMBOLS = (
     "hc_prepare_params_size", "hc_prepare_params", "hc_workspace_size", "hc_pre_step", "hc_post_then_pre",
     "hc_post_then_pre_tap", "hc_post_then_pre_noalloc", "hc_post", "hc_expand_pre_step", "hc_final", "hc_post_then_final", "hc_debug_mixes",
-    "hc_plan_tiles", "hc_fused_ctas", "hc_device_error", "hc_status_string",
+    "hc_plan_tiles", "hc_fused_ctas", "hc_debug_wait_flag", "hc_device_error", "hc_status_string",
 )
 
 
@@ -79,6 +79,7 @@ def load(path: str = LIB_PATH):
     lib.hc_debug_mixes.argtypes = [P, hc_params_t, I64, hc_shape_t, P, P, P]
     lib.hc_plan_tiles.argtypes = [I64, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I64)]
     lib.hc_fused_ctas.argtypes = [ctypes.POINTER(I)]
+    lib.hc_debug_wait_flag.argtypes = [P, I, ctypes.c_uint64, I64, P]
     lib.hc_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), I, P]
     lib.hc_status_string.argtypes = [I]
     lib.hc_status_string.restype = ctypes.c_char_p
@@ -217,6 +218,10 @@ def hc_fused_ctas() -> int:
     c = ctypes.c_int(0)
     _check("hc_fused_ctas", load().hc_fused_ctas(ctypes.byref(c)))
     return c.value
+
+
+def hc_debug_wait_flag(flags, count: int, value: int, limit_ns: int, stream=None) -> None:
+    _check("hc_debug_wait_flag", load().hc_debug_wait_flag(_ptr(flags), count, value, limit_ns, _stream(stream)))
 
 
 def hc_device_error(clear: bool = True, stream=None) -> int:

@@ -543,6 +543,16 @@ int hc_fused_ctas(int* ctas) {
     return launch_status(fused_ctas(ctas));
 }
 
+int hc_debug_wait_flag(const unsigned long long* flags, int count, unsigned long long value, int64_t limit_ns,
+                       hc_stream_t stream) {
+    if (!flags) return HC_ERR_NULL;
+    if (count < 1 || count > 32) return HC_ERR_SHAPE;
+    if (limit_ns < 0 || limit_ns > 1000000000LL) return HC_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(flags) & 7u) return HC_ERR_ALIGN;
+    return launch_status(launch_wait_flag(flags, value, count, static_cast<uint64_t>(limit_ns),
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int hc_device_error(unsigned int* word, int clear, hc_stream_t stream) {
     if (!word) return HC_ERR_NULL;
     return read_device_error(word, clear, reinterpret_cast<cudaStream_t>(stream)) == 0 ? HC_OK : HC_ERR_CUDA;

@@ -219,6 +219,7 @@ __device__ __forceinline__ void unpack4(const uint4& v, float2 (&f)[4]) {
 // Bounded mbarrier wait shared by all roles of one CTA.
 struct Waiter {
     volatile uint32_t* abort;
+    uint64_t limit_ns = kWaitLimitNs;
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, unsigned int code) const {
         if (mbar_test(bar, parity)) return true;
         const uint64_t t0 = global_timer_ns();
@@ -226,7 +227,7 @@ struct Waiter {
             for (int i = 0; i < 32; ++i)
                 if (mbar_test(bar, parity)) return true;
             if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 *abort = 1u;
                 atomicOr(&g_hc_error, code);
                 return false;
@@ -242,7 +243,7 @@ struct Waiter {
             if (!mine) mine = ld_acquire_gpu_u64(f + lane) == epoch;
             if (__all_sync(0xffffffffu, mine)) return true;
             const bool aborted = *abort != 0u;
-            const bool late = global_timer_ns() - t0 > kWaitLimitNs;
+            const bool late = global_timer_ns() - t0 > limit_ns;
             if (__any_sync(0xffffffffu, aborted || late)) {  // one decision for the whole warp
                 if (lane == 0 && !aborted) {
                     *abort = 1u;
@@ -257,7 +258,7 @@ struct Waiter {
     __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) const {
         const uint64_t t0 = global_timer_ns();
         while (!mbar_test(bar, parity)) {
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 atomicOr(&g_hc_error, kErrDrain);
                 return;
             }
@@ -320,6 +321,18 @@ __device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const flo
     }
 }
 
+// ---- diagnostic: one bounded wait on an exchange flag ------------------------------------------------
+// One warp waits, exactly as the fused kernel's split warp waits for its group, for flags f[0..g-1]
+// to equal `value`, giving up after limit_ns: it then records kErrExchange in the device error word
+// and returns. Lets a test make a wait run out (on flags nothing sets) and check what the host sees.
+__global__ void hc_wait_flag_kernel(const unsigned long long* f, unsigned long long value, int g, uint64_t limit_ns) {
+    __shared__ uint32_t abort_word;
+    if (threadIdx.x == 0) abort_word = 0u;
+    __syncwarp();
+    const Waiter W{&abort_word, limit_ns};
+    W.wait_flags_warp(f, value, static_cast<int>(threadIdx.x), g, kErrExchange);
+}
+
 // ---- the kernel ---------------------------------------------------------------------------------
 
 template <int kMode, int kG>
@@ -346,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
-    const Waiter W{abort_flag};
+    const Waiter W{abort_flag, kWaitLimitNs};
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -1072,6 +1085,12 @@ int noalloc_workspace(void** ptr, size_t* capacity) {
     *ptr = g_noalloc_ptr[dev];
     *capacity = sizeof(g_noalloc_workspace);
     return 0;
+}
+
+int launch_wait_flag(const unsigned long long* flags, unsigned long long value, int g, uint64_t limit_ns,
+                     cudaStream_t stream) {
+    hc_wait_flag_kernel<<<1, 32, 0, stream>>>(flags, value, g, limit_ns);
+    return cudaGetLastError() == cudaSuccess ? 0 : -7;
 }
 
 int read_device_error(unsigned int* word, int clear, cudaStream_t stream) {

@@ -109,6 +109,10 @@ int launch_generic_final(const void* X, const void* delta, const float* post, co
                          const float* pre_mix, const float* norm_w, void* X_out, void* z, int64_t n, int hc, int d,
                          float eps, cudaStream_t stream);
 
+// Diagnostic: one bounded wait (limit_ns) for flags[0..g-1] to equal value; 0 or -7.
+int launch_wait_flag(const unsigned long long* flags, unsigned long long value, int g, uint64_t limit_ns,
+                     cudaStream_t stream);
+
 // Reads (and optionally clears) the device error word of the current device.
 int read_device_error(unsigned int* word, int clear, cudaStream_t stream);
 

@@ -237,6 +237,14 @@ int hc_plan_tiles(int64_t n, int d, int ctas, int* group, int* tile_m, int64_t* 
  * GB300: 152), capped at 256. */
 int hc_fused_ctas(int* ctas);
 
+/* Diagnostic for the bounded waits: one warp waits, exactly as the fused kernel waits for the other
+ * CTAs of its group, for the 64-bit flags[0..count-1] [device] (8-byte aligned, count 1..32) to
+ * equal `value`, and gives up after limit_ns (0..1e9) nanoseconds: it then sets the exchange bit of
+ * the device error word (hc_device_error) and returns, leaving the context usable. The fused kernel
+ * gives up after one second on every wait in the same way. No counterpart on the pages. */
+int hc_debug_wait_flag(const unsigned long long* flags, int count, unsigned long long value, int64_t limit_ns,
+                       hc_stream_t stream);
+
 /* Read the device-side error word of the current device: nonzero when a kernel gave up a
  * bounded wait (it then returned early and its outputs are not valid). Synchronises `stream`.
  * If `clear` is nonzero the word is reset to 0. Returns HC_OK, HC_ERR_NULL or HC_ERR_CUDA. */

@@ -234,6 +234,15 @@ def test_post_then_final_validation(lib):
     hc.hc_post_then_final(*bad)
 
 
+def test_debug_wait_flag_validation(lib):
+    _expect(hc.HC_ERR_NULL, hc.hc_debug_wait_flag, None, 8, 1, 1000, 0)
+    _expect(hc.HC_ERR_SHAPE, hc.hc_debug_wait_flag, A[0], 0, 1, 1000, 0)
+    _expect(hc.HC_ERR_SHAPE, hc.hc_debug_wait_flag, A[0], 33, 1, 1000, 0)
+    _expect(hc.HC_ERR_ARG, hc.hc_debug_wait_flag, A[0], 8, 1, -1, 0)
+    _expect(hc.HC_ERR_ARG, hc.hc_debug_wait_flag, A[0], 8, 1, 2_000_000_000, 0)
+    _expect(hc.HC_ERR_ALIGN, hc.hc_debug_wait_flag, A[0] + 4, 8, 1, 1000, 0)
+
+
 def test_plan_tiles(lib):
     for ctas in (8, 56, 128, 152, 256):
         for d in (256, 512, 1024, 5120):
