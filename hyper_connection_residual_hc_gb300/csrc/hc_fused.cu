@@ -269,10 +269,11 @@ struct Waiter {
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
 
 // "Reading weights" page, hc_split_sinkhorn kernel excerpt and the formula for p, in fp32. Every
-// normalisation multiplies by the hardware approximate reciprocal of its sum (1 ulp): the sums are
-// at least eps or 1, never subnormal, and the 2 * iters dependent normalisations run about four
-// times faster than with correctly rounded reciprocals (20 rounds: 2.1 us instead of 8.0 us on one
-// thread), which matters when a small batch waits for them.
+// normalisation multiplies by a reciprocal of its sum taken as the hardware approximation refined
+// by one Newton-Raphson step (about 1 ulp; the sums are at least eps or 1, never subnormal): the
+// 2 * iters dependent normalisations run several times faster than with correctly rounded
+// reciprocals, which matters when a small batch waits for them, and the refinement keeps 50 rounds
+// on extreme logits inside the coefficients' 1e-5 tolerance, which the bare approximation did not.
 __device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const float (&sc)[3], const float (&b)[kMix],
                                                int iters, float eps, float (&pre)[4], float (&post)[4],
                                                float (&C)[16]) {
@@ -288,7 +289,7 @@ __device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const flo
         float mx = fmaxf(fmaxf(C[4 * j], C[4 * j + 1]), fmaxf(C[4 * j + 2], C[4 * j + 3]));
         float e0 = expf(C[4 * j] - mx), e1 = expf(C[4 * j + 1] - mx);
         float e2 = expf(C[4 * j + 2] - mx), e3 = expf(C[4 * j + 3] - mx);
-        float inv = rcp_approx((e0 + e1) + (e2 + e3));
+        float inv = rcp_refined((e0 + e1) + (e2 + e3));
         C[4 * j] = e0 * inv + eps;
         C[4 * j + 1] = e1 * inv + eps;
         C[4 * j + 2] = e2 * inv + eps;
@@ -297,7 +298,7 @@ __device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const flo
     auto col_norm = [&]() {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            float inv = rcp_approx(((C[k] + C[4 + k]) + (C[8 + k] + C[12 + k])) + eps);
+            float inv = rcp_refined(((C[k] + C[4 + k]) + (C[8 + k] + C[12 + k])) + eps);
             C[k] *= inv;
             C[4 + k] *= inv;
             C[8 + k] *= inv;
@@ -307,7 +308,7 @@ __device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const flo
     auto row_norm = [&]() {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            float inv = rcp_approx(((C[4 * j] + C[4 * j + 1]) + (C[4 * j + 2] + C[4 * j + 3])) + eps);
+            float inv = rcp_refined(((C[4 * j] + C[4 * j + 1]) + (C[4 * j + 2] + C[4 * j + 3])) + eps);
             C[4 * j] *= inv;
             C[4 * j + 1] *= inv;
             C[4 * j + 2] *= inv;

@@ -186,7 +186,7 @@ __device__ void gen_split_sinkhorn(int hc, const float* m, const float* sc, cons
             C[j * hc + k] = expf(C[j * hc + k] - mx);
             s += C[j * hc + k];
         }
-        const float inv = rcp_approx(s);
+        const float inv = rcp_refined(s);
         for (int k = 0; k < hc; ++k) C[j * hc + k] = C[j * hc + k] * inv + eps;
     }
     for (int it = 0; it < iters; ++it) {
@@ -194,14 +194,14 @@ __device__ void gen_split_sinkhorn(int hc, const float* m, const float* sc, cons
             for (int j = 0; j < hc; ++j) {
                 float s = 0.f;
                 for (int k = 0; k < hc; ++k) s += C[j * hc + k];
-                const float inv = rcp_approx(s + eps);
+                const float inv = rcp_refined(s + eps);
                 for (int k = 0; k < hc; ++k) C[j * hc + k] *= inv;
             }
         }
         for (int k = 0; k < hc; ++k) {
             float s = 0.f;
             for (int j = 0; j < hc; ++j) s += C[j * hc + k];
-            const float inv = rcp_approx(s + eps);
+            const float inv = rcp_refined(s + eps);
             for (int j = 0; j < hc; ++j) C[j * hc + k] *= inv;
         }
     }

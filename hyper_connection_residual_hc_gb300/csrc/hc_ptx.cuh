@@ -321,6 +321,15 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return r;
 }
 
+// 1/x as the hardware approximation refined by one Newton-Raphson step for the reciprocal,
+// r <- r + r (1 - x r) (two FMAs): the approximation's error is squared away and what remains is
+// the rounding of the two FMAs, about 1 ulp, for normal x.
+__device__ __forceinline__ float rcp_refined(float x) {
+    const float r = rcp_approx(x);
+    const float e = fmaf(-x, r, 1.0f);
+    return fmaf(r, e, r);
+}
+
 // 4-byte load cached in L2 only (as ld_cg_f4).
 __device__ __forceinline__ float ld_cg_f32(const float* p) {
     float v;
