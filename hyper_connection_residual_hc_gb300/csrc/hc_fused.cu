@@ -340,6 +340,7 @@ template <int kMode, int kG>
 __global__ void __launch_bounds__(kThreads, 1)
     hc_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmD,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmXo,
+                    const __grid_constant__ CUtensorMap tmM,
                     const FusedParams p) {
     constexpr bool kPost = kMode == kModePost;
     constexpr bool kExpand = kMode == kModeExpand;
@@ -520,16 +521,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             st_smem_v4(sb + kOffX + k * kXTileBytes + off, ov);
                             unpack4(ov, xr[k]);
                         }
-                        if (p.stream_mean && valid) {
-                            // the multi-token-prediction tap: bf16(mean_j X'_j), summed in fp32
+                        if (p.stream_mean) {
+                            // the multi-token-prediction tap: bf16(mean_j X'_j), summed in fp32, written
+                            // over this thread's own (already read) Delta chunk; the store warp sends
+                            // the tile out with the X' tiles
                             uint32_t o[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 float2 t = __fadd2_rn(__fadd2_rn(__fadd2_rn(xr[0][e], xr[1][e]), xr[2][e]), xr[3][e]);
                                 o[e] = pack_bf16(__fmul2_rn(t, bcast(0.25f)));
                             }
-                            uint16_t* mrow = static_cast<uint16_t*>(p.stream_mean) + tok * p.d;
-                            *reinterpret_cast<uint4*>(mrow + stage_col(s) + c * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+                            st_smem_v4(sb + kOffD + off, make_uint4(o[0], o[1], o[2], o[3]));
                         }
                     } else {
 #pragma unroll
@@ -727,6 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         tma_store_3d(&tmXo, sb + kOffX + (kExpand ? 0 : k * kXTileBytes), col, k, t0);
+                    if (kPost && p.stream_mean) tma_store_2d(&tmM, sb + kOffD, col, t0);  // the tap
                     bulk_commit();
                     bulk_wait_read<0>();
                 }
@@ -983,7 +986,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     const bool write_x = a.mode != kModePre;
     const void* x_in = a.mode == kModeExpand ? a.X_out : a.X;
     const void* rows = a.mode == kModePost ? a.delta : a.mode == kModeExpand ? a.embed : a.X;
-    CUtensorMap tmX, tmD, tmB, tmXo;
+    CUtensorMap tmX, tmD, tmB, tmXo, tmM;
     {
         const uint64_t dims[3] = {d, 4, n};
         const uint64_t str[2] = {d * 2, 4 * d * 2};
@@ -996,6 +999,8 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
         const uint64_t str[1] = {d * 2};
         const uint32_t box[2] = {kChunk, static_cast<uint32_t>(tile_m)};
         if (!encode(&tmD, rows, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B, HC_STREAM_PROMOTION)) return -7;
+        // the tap's rows (encoded on the read rows when there is no tap: never used then)
+        if (!encode(&tmM, a.stream_mean ? a.stream_mean : rows, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
     }
     {
         const uint64_t dims[2] = {4 * d, static_cast<uint64_t>(kBRows)};
@@ -1044,7 +1049,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaErrorInvalidValue;
-    auto go = [&](auto kernel) { e = cudaLaunchKernelEx(&cfg, kernel, tmX, tmD, tmB, tmXo, p); };
+    auto go = [&](auto kernel) { e = cudaLaunchKernelEx(&cfg, kernel, tmX, tmD, tmB, tmXo, tmM, p); };
     if (a.mode == kModePost) {
         if (group == 8) go(hc_fused_kernel<kModePost, 8>);
         else if (group == 16) go(hc_fused_kernel<kModePost, 16>);
