@@ -97,7 +97,11 @@ constexpr int kOffNormW = kStages * kStageBytes;
 constexpr int kPartRows = 28;
 constexpr int kPartFloats = kPartRows * kTileMax;
 constexpr int kPartSx = kMix * kTileMax, kPartSy = kPartSx + 2 * kTileMax;
-constexpr int kOffBar = kOffNormW + kMaxDSlice * 4;
+// y_normed staging: per epilogue warp two 32-row x 64-byte tiles (64-byte swizzle) that the warp
+// fills and TMA-stores in turn
+constexpr int kYStageBytes = 32 * kChunk * 2;                              // 2048
+constexpr int kOffYStage = ((kOffNormW + kMaxDSlice * 4 + 1023) / 1024) * 1024;
+constexpr int kOffBar = kOffYStage + 4 * 2 * kYStageBytes;
 constexpr int kBarFull = 0, kBarXReady = 3, kBarEmpty = 6, kBarAccFull = 9, kBarAccEmpty = 10, kBarMmaDone = 11;
 // kBarFlagsSeen[2] (per tile parity): the split warp has seen the group's flags of a tile, so the
 // epilogue warps may read its sums of y^2. kBarEpiRead: the epilogue warps have read them (one
@@ -340,7 +344,7 @@ template <int kMode, int kG>
 __global__ void __launch_bounds__(kThreads, 1)
     hc_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmD,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmXo,
-                    const __grid_constant__ CUtensorMap tmM,
+                    const __grid_constant__ CUtensorMap tmM, const __grid_constant__ CUtensorMap tmY,
                     const FusedParams p) {
     constexpr bool kPost = kMode == kModePost;
     constexpr bool kExpand = kMode == kModeExpand;
@@ -596,6 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* nw = reinterpret_cast<const float*>(smem + kOffNormW);
         const float inv_d = 1.0f / static_cast<float>(p.d);
         long long g = 0;
+        long long ystores = 0;  // TMA stores this warp has issued (staging tiles alternate)
         for (long long it = 0; it < my_tiles; ++it) {
             const int buf = static_cast<int>(it & 1);
             // r_y of this thread's row from the group's sums of y^2 (2 halves of each of the kG
@@ -612,8 +617,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarEpiRead));  // this warp is done with the tile's blocks
             const long long t0 = (cid + it * ncl) * p.tile_m;
-            const bool store = p.write_y && row < p.tile_m && t0 + row < p.n;
-            uint16_t* yrow = static_cast<uint16_t*>(p.y_normed) + (store ? (t0 + row) * p.d : 0);
+            // this warp's 32 rows go out as one TMA tile when they lie in the tile (rows past n are
+            // clipped by the tensor map; rows past tile_m would belong to the next tile)
+            const bool store = p.write_y && 32 * q < p.tile_m;
             for (int s = 0; s < S; ++s, ++g) {
                 const int ys = static_cast<int>(g % kRing);
                 W.wait(bar(kBarYReady + ys), static_cast<uint32_t>((g / kRing) & 1), kErrEpilogue);
@@ -631,14 +637,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t ov[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) ov[e] = pack_bf16(__fmul2_rn(w[e], __fmul2_rn(bf2(yv[e]), ry2)));
-                    uint4* dst = reinterpret_cast<uint4*>(yrow + stage_col(s));
-                    dst[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
-                    dst[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
-                    dst[2] = make_uint4(ov[8], ov[9], ov[10], ov[11]);
-                    dst[3] = make_uint4(ov[12], ov[13], ov[14], ov[15]);
+                    // staging tile (alternating): the store issued from it two stages ago must have read it
+                    const uint32_t st = sbase + kOffYStage + static_cast<uint32_t>((q * 2 + (ystores & 1)) * kYStageBytes);
+                    if (lane == 0 && ystores >= 2) bulk_wait_read<1>();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        st_smem_v4(st + static_cast<uint32_t>(lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)),
+                                   make_uint4(ov[4 * j], ov[4 * j + 1], ov[4 * j + 2], ov[4 * j + 3]));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmY, st, stage_col(s), static_cast<int>(t0 + 32 * q));
+                        bulk_commit();
+                    }
+                    ++ystores;
                 }
             }
         }
+        if (lane == 0) bulk_wait<0>();  // this warp's y_normed stores are complete
+        __syncwarp();
     } else if (warp == kWarpProducer) {
         // ================= TMA producer =========================================================
         uint64_t pol_stream = 0, pol_keep = 0;
@@ -986,7 +1004,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     const bool write_x = a.mode != kModePre;
     const void* x_in = a.mode == kModeExpand ? a.X_out : a.X;
     const void* rows = a.mode == kModePost ? a.delta : a.mode == kModeExpand ? a.embed : a.X;
-    CUtensorMap tmX, tmD, tmB, tmXo, tmM;
+    CUtensorMap tmX, tmD, tmB, tmXo, tmM, tmY;
     {
         const uint64_t dims[3] = {d, 4, n};
         const uint64_t str[2] = {d * 2, 4 * d * 2};
@@ -1001,6 +1019,9 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
         if (!encode(&tmD, rows, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B, HC_STREAM_PROMOTION)) return -7;
         // the tap's rows (encoded on the read rows when there is no tap: never used then)
         if (!encode(&tmM, a.stream_mean ? a.stream_mean : rows, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+        // y_normed in 32-row tiles, one per epilogue warp (encoded on the read rows when it is not written)
+        const uint32_t ybox[2] = {kChunk, 32};
+        if (!encode(&tmY, a.y_normed ? a.y_normed : rows, 2, dims, str, ybox, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
     }
     {
         const uint64_t dims[2] = {4 * d, static_cast<uint64_t>(kBRows)};
@@ -1049,7 +1070,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaErrorInvalidValue;
-    auto go = [&](auto kernel) { e = cudaLaunchKernelEx(&cfg, kernel, tmX, tmD, tmB, tmXo, tmM, p); };
+    auto go = [&](auto kernel) { e = cudaLaunchKernelEx(&cfg, kernel, tmX, tmD, tmB, tmXo, tmM, tmY, p); };
     if (a.mode == kModePost) {
         if (group == 8) go(hc_fused_kernel<kModePost, 8>);
         else if (group == 16) go(hc_fused_kernel<kModePost, 16>);
