@@ -73,7 +73,7 @@ constexpr int kMaxGroups = 32;     // launch counters: group slots (at most 256 
 constexpr int kFlagRanks = 32;     // flags per (group slot, tile parity): the largest group
 constexpr int kTileMax = 128;
 constexpr int kChunk = 32;        // columns per stage: 64-byte rows
-constexpr int kStages = 3;
+constexpr int kMaxStages = 6;
 constexpr int kComputeWarps = 8;
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
@@ -83,41 +83,58 @@ constexpr int kWarpEpi0 = 12;       // warps 12..15: y_normed epilogue, TMEM lan
 constexpr int kThreads = 16 * 32;
 constexpr int kMaxDSlice = 640;   // d <= 5120
 
-// shared memory layout, offsets from a 1024-byte aligned base
 constexpr int kXTileBytes = kTileMax * kChunk * 2;            // 8192: 128 rows x 64 B
 constexpr int kBTileBytes = kBRows * kChunk * 2;              // 4608: 72 rows x 64 B (the MMA reads
                                                               // 80 rows; rows 72..79 are ignored)
-constexpr int kOffX = 0;
-constexpr int kOffD = 4 * kXTileBytes;
-constexpr int kOffB = kOffD + kXTileBytes;
-constexpr int kStageBytes = kOffB + 4 * kBTileBytes;          // 59392
-constexpr int kOffNormW = kStages * kStageBytes;
 // One CTA's partial sums for one tile: mixes [128 tokens][24] (token-major), then
 // sum x^2 [2 column halves][128], then sum y^2 [2][128].
 constexpr int kPartRows = 28;
 constexpr int kPartFloats = kPartRows * kTileMax;
 constexpr int kPartSx = kMix * kTileMax, kPartSy = kPartSx + 2 * kTileMax;
-// y_normed staging: per epilogue warp two 32-row x 64-byte tiles (64-byte swizzle) that the warp
-// fills and TMA-stores in turn
 constexpr int kYStageBytes = 32 * kChunk * 2;                              // 2048
-constexpr int kOffYStage = ((kOffNormW + kMaxDSlice * 4 + 1023) / 1024) * 1024;
-constexpr int kOffBar = kOffYStage + 4 * 2 * kYStageBytes;
-constexpr int kBarFull = 0, kBarXReady = 3, kBarEmpty = 6, kBarAccFull = 9, kBarAccEmpty = 10, kBarMmaDone = 11;
+// mbarriers, numbered for up to kMaxStages shared-memory slots
+constexpr int kBarFull = 0, kBarXReady = 6, kBarEmpty = 12, kBarAccFull = 18, kBarAccEmpty = 19, kBarMmaDone = 20;
 // kBarFlagsSeen[2] (per tile parity): the split warp has seen the group's flags of a tile, so the
 // epilogue warps may read its sums of y^2. kBarEpiRead: the epilogue warps have read them (one
 // arrival per warp per tile); the split warp publishes the next tile only after that.
-constexpr int kBarSplitDone = 12, kBarFlagsSeen = 13, kBarEpiRead = 15, kBarYReady = 17, kBarYFree = 17 + 27;
+constexpr int kBarSplitDone = 21, kBarFlagsSeen = 22, kBarEpiRead = 24, kBarYReady = 25, kBarYFree = 25 + 27;
 // kBarPublish: the compute warps have written the CTA's partial sums of a tile (one arrival per
 // warp), the split warp waits before publishing them. kBarExit: every warp is done (one arrival per
 // warp) before TMEM is freed. The CTA-wide hardware barriers are not used after the set-up: in
 // this kernel, whose warps spend most of their time in mbarrier waits, a block-wide bar.sync at
 // the end was measured releasing warp 0 while other warps had not reached it; mbarriers hold.
-constexpr int kBarPublish = 17 + 2 * 27, kBarExit = kBarPublish + 1;
+constexpr int kBarPublish = 25 + 2 * 27, kBarExit = kBarPublish + 1;
 constexpr int kNumBars = kBarExit + 1;
-constexpr int kOffTmemPtr = kOffBar + kNumBars * 8;
-constexpr int kOffAbort = kOffTmemPtr + 4;
-constexpr int kSmemUsed = kOffAbort + 4;
-constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
+
+// Shared-memory layout of each mode, offsets from a 1024-byte aligned base. A slot holds one column
+// stage: the stream tiles (four, or the one embedding tile in expand mode), the Delta tile (post
+// mode only) and the four weight-plane tiles. The smaller slots of the reading-only modes buy more
+// of them, so more loads are in flight while the stage's MMA holds its slot: post 3 x 59392 B,
+// pre 4 x 51200 B, expand 6 x 26624 B. After the slots: norm_w of the CTA's columns, the epilogue
+// warps' y_normed staging tiles (per warp two 32-row x 64-byte tiles, 64-byte swizzle, filled and
+// TMA-stored in turn), the mbarriers, the TMEM address and the abort word.
+template <int kMode>
+struct Layout {
+    static constexpr int kXTiles = kMode == kModeExpand ? 1 : 4;
+    static constexpr int kOffX = 0;
+    static constexpr int kOffD = kXTiles * kXTileBytes;
+    static constexpr int kOffB = kOffD + (kMode == kModePost ? kXTileBytes : 0);
+    static constexpr int kStage = kOffB + 4 * kBTileBytes;
+    static constexpr int kStages = kMode == kModePost ? 3 : kMode == kModePre ? 4 : 6;
+    static constexpr int kOffNormW = kStages * kStage;
+    static constexpr int kOffYStage = ((kOffNormW + kMaxDSlice * 4 + 1023) / 1024) * 1024;
+    static constexpr int kOffBar = kOffYStage + 4 * 2 * kYStageBytes;
+    static constexpr int kOffTmemPtr = kOffBar + kNumBars * 8;
+    static constexpr int kOffAbort = kOffTmemPtr + 4;
+    static constexpr int kSmemUsed = kOffAbort + 4;
+    static constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
+    static_assert(kStage % 1024 == 0, "stage buffers keep 1024-byte alignment");
+    static_assert(kOffB % 512 == 0 && kBTileBytes % 512 == 0, "B tiles start on 512-byte swizzle atoms");
+    static_assert(kStages <= kMaxStages, "barrier numbering");
+    static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in shared memory of one CTA");
+    // the MMA of the last B tile of the last slot reads 8 rows (512 B) past it: into norm_w, inside the CTA
+    static_assert(kOffB + 3 * kBTileBytes + kUmmaN * 64 + (kStages - 1) * kStage <= kSmemUsed, "B overrun");
+};
 
 // global workspace: partial sums [group][tile parity][rank][28][128] fp32 (a block per CTA and
 // tile parity), then 64-bit flags [group slot][tile parity][32 ranks], then one 64-bit launch
@@ -134,11 +151,6 @@ constexpr size_t kWorkspaceBytes = kWsPartBytes + kWsFlagBytes + kWsCounterBytes
 
 static_assert(kWarpEpi0 + 4 == kThreads / 32 && kWarpEpi0 % 4 == 0, "one epilogue warp per TMEM lane quadrant");
 static_assert(kWarpSplit + 1 == kWarpEpi0, "warp roles: 8 compute, producer, MMA, store, split, 4 epilogue");
-static_assert(kStageBytes % 1024 == 0, "stage buffers keep 1024-byte alignment");
-static_assert(kOffB % 512 == 0 && kBTileBytes % 512 == 0, "B tiles start on 512-byte swizzle atoms");
-static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in shared memory of one CTA");
-// the MMA of the last B tile of the last stage reads 8 rows (512 B) past it: still inside the CTA
-static_assert(kOffB + 3 * kBTileBytes + kUmmaN * 64 + (kStages - 1) * kStageBytes <= kSmemUsed, "B overrun");
 
 // TMEM: one accumulator (N = 80 columns), then a ring of kRing y chunks of 16 columns each
 // (32 rows x 16 bf16 pairs per warp quadrant). A tile has at most 20 stages, so the compute warps
@@ -346,6 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmXo,
                     const __grid_constant__ CUtensorMap tmM, const __grid_constant__ CUtensorMap tmY,
                     const FusedParams p) {
+    using Lay = Layout<kMode>;
+    constexpr int kStages = Lay::kStages, kStageBytes = Lay::kStage;
+    constexpr int kOffX = Lay::kOffX, kOffD = Lay::kOffD, kOffB = Lay::kOffB, kOffNormW = Lay::kOffNormW;
+    constexpr int kOffYStage = Lay::kOffYStage, kOffBar = Lay::kOffBar, kOffTmemPtr = Lay::kOffTmemPtr;
+    constexpr int kOffAbort = Lay::kOffAbort;
     constexpr bool kPost = kMode == kModePost;
     constexpr bool kExpand = kMode == kModeExpand;
     constexpr bool kWriteX = kPost || kExpand;  // X' goes back to the streams
@@ -925,12 +942,18 @@ int prepare_device(int* ctas) {
         kernels_of_mode<kModePre>(kernels);
         kernels_of_mode<kModePost>(kernels + 3);
         kernels_of_mode<kModeExpand>(kernels + 6);
+        const int k_smem[9] = {Layout<kModePre>::kSmemBytes,    Layout<kModePre>::kSmemBytes,
+                               Layout<kModePre>::kSmemBytes,    Layout<kModePost>::kSmemBytes,
+                               Layout<kModePost>::kSmemBytes,   Layout<kModePost>::kSmemBytes,
+                               Layout<kModeExpand>::kSmemBytes, Layout<kModeExpand>::kSmemBytes,
+                               Layout<kModeExpand>::kSmemBytes};
         int per_sm = 1 << 30;
-        for (const void* k : kernels) {
-            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
-                return -7;
+        for (int i = 0; i < 9; ++i) {
+            const void* k = kernels[i];
+            const int smem = k_smem[i];
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -7;
             int b = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k, kThreads, kSmemBytes) != cudaSuccess || b < 1)
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k, kThreads, smem) != cudaSuccess || b < 1)
                 return -7;
             per_sm = std::min(per_sm, b);
         }
@@ -1065,7 +1088,9 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     attr[0].val.cooperative = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(grid_groups * group), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = a.mode == kModePost     ? Layout<kModePost>::kSmemBytes
+                           : a.mode == kModeExpand ? Layout<kModeExpand>::kSmemBytes
+                                                   : Layout<kModePre>::kSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
