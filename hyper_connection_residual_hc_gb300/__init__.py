@@ -33,6 +33,8 @@ SYMBOLS = (
     "hc_prepare_params_size", "hc_prepare_params", "hc_workspace_size", "hc_pre_step", "hc_post_then_pre",
     "hc_post_then_pre_tap", "hc_post_then_pre_noalloc", "hc_post", "hc_expand_pre_step", "hc_final", "hc_post_then_final", "hc_debug_mixes",
     "hc_plan_tiles", "hc_fused_ctas", "hc_debug_wait_flag", "hc_device_error", "hc_status_string",
+    "hc_host_pipeline_create", "hc_host_pipeline_chunk_tokens", "hc_host_pipeline_destroy", "hc_host_chunk_plan",
+    "hc_host_post_then_pre",
 )
 
 
@@ -82,6 +84,12 @@ def load(path: str = LIB_PATH):
     lib.hc_debug_wait_flag.argtypes = [P, I, ctypes.c_uint64, I64, P]
     lib.hc_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), I, P]
     lib.hc_status_string.argtypes = [I]
+    lib.hc_host_pipeline_create.argtypes = [I, I, I64, ctypes.POINTER(P)]
+    lib.hc_host_pipeline_chunk_tokens.argtypes = [P, ctypes.POINTER(I64)]
+    lib.hc_host_pipeline_destroy.argtypes = [P]
+    PI64 = ctypes.POINTER(I64)
+    lib.hc_host_chunk_plan.argtypes = [I64, I64, I64, PI64, PI64, PI64]
+    lib.hc_host_post_then_pre.argtypes = [P, P, P, P, P, P, hc_params_t, I64, hc_shape_t, P, P, P, P, P, P]
     lib.hc_status_string.restype = ctypes.c_char_p
     for name in SYMBOLS:
         if name != "hc_status_string":
@@ -228,3 +236,66 @@ def hc_device_error(clear: bool = True, stream=None) -> int:
     w = ctypes.c_uint(0)
     _check("hc_device_error", load().hc_device_error(ctypes.byref(w), 1 if clear else 0, _stream(stream)))
     return w.value
+
+
+class HostPipeline:
+    """The host-buffer executor (hc_host_pipeline_t): device staging for three chunks of tokens, two
+    copy streams and a workspace, owned until :meth:`close`. Its calls take host tensors (pinned ones
+    let the copies overlap)."""
+
+    def __init__(self, hc: int = 4, d: int = 5120, chunk_tokens: int = 0):
+        h = ctypes.c_void_p()
+        _check("hc_host_pipeline_create", load().hc_host_pipeline_create(hc, d, chunk_tokens, ctypes.byref(h)))
+        self.handle = h.value
+
+    @property
+    def chunk_tokens(self) -> int:
+        c = ctypes.c_int64(0)
+        _check("hc_host_pipeline_chunk_tokens", load().hc_host_pipeline_chunk_tokens(self.handle, ctypes.byref(c)))
+        return c.value
+
+    def close(self) -> None:
+        if self.handle:
+            h, self.handle = self.handle, None
+            _check("hc_host_pipeline_destroy", load().hc_host_pipeline_destroy(h))
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+def hc_host_pipeline_create(hc: int, d: int, chunk_tokens: int = 0) -> HostPipeline:
+    return HostPipeline(hc, d, chunk_tokens)
+
+
+def hc_host_pipeline_chunk_tokens(p: HostPipeline) -> int:
+    return p.chunk_tokens
+
+
+def hc_host_pipeline_destroy(p: HostPipeline) -> None:
+    p.close()
+
+
+def hc_host_chunk_plan(n: int, chunk_tokens: int = 0):
+    """The chunks [(first token, tokens), ...] the executor cuts a call on n tokens into."""
+    L = load()
+    count, t0, m = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+    _check("hc_host_chunk_plan", L.hc_host_chunk_plan(n, chunk_tokens, -1, ctypes.byref(count), None, None))
+    out = []
+    for i in range(count.value):
+        _check("hc_host_chunk_plan", L.hc_host_chunk_plan(n, chunk_tokens, i, ctypes.byref(count), ctypes.byref(t0),
+                                                          ctypes.byref(m)))
+        out.append((t0.value, m.value))
+    return out
+
+
+def hc_host_post_then_pre(p, delta, X, post, comb, pre_mix, nxt: hc_params_t, n: int, s: hc_shape_t, X_out, y_normed,
+                          pre_out, post_out, comb_out, stream=None) -> None:
+    """hc_post_then_pre on HOST tensors through the executor `p` (a HostPipeline, a raw handle or None);
+    the results are in the host tensors once `stream` has passed the call."""
+    handle = p.handle if isinstance(p, HostPipeline) else p
+    _check("hc_host_post_then_pre", load().hc_host_post_then_pre(
+        handle, _ptr(delta), _ptr(X), _ptr(post), _ptr(comb), _ptr(pre_mix), nxt, n, s, _ptr(X_out), _ptr(y_normed),
+        _ptr(pre_out), _ptr(post_out), _ptr(comb_out), _stream(stream)))

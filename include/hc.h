@@ -23,7 +23,8 @@
  * Conventions for every entry point
  *   - Pointers marked [device] are CUDA device pointers in the current device's context; the
  *     caller allocates and owns every buffer. The library never allocates or frees device memory
- *     and never synchronises the stream, except hc_device_error (documented there).
+ *     and never synchronises the stream, except hc_device_error and the host-buffer executor
+ *     (hc_host_pipeline_*, which owns its staging memory; documented there).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).
  *   - All arrays are contiguous row-major; tokens are flattened, n = batch * positions.
  *   - bf16 is IEEE bfloat16 (16-bit storage); fp32 is IEEE binary32.
@@ -218,6 +219,68 @@ int hc_final(const void* X, const float* pre_mix, const float* norm_w, int64_t n
 int hc_post_then_final(const void* delta, const void* X, const float* post, const float* comb,
                        const float* pre_mix, const float* norm_w, int64_t n, hc_shape_t s,
                        void* X_out, void* z, hc_stream_t stream);
+
+/* ---- Host-buffer executor ---------------------------------------------------------------------
+ * For callers whose per-token arrays live in host memory: the executor streams the tokens through
+ * the GPU in chunks, copying one chunk in while the fused step runs on another and a third is
+ * copied back, on its own two copy streams. On a GB300 the host link bounds such a call, so the
+ * overlap of the two copy directions is what it buys. No counterpart on the pages: it is this
+ * library's host-side runtime around hc_post_then_pre. */
+typedef struct hc_host_pipeline hc_host_pipeline_t;
+
+/* Create an executor for calls of shape (hc, d) on the current device. It allocates, and owns
+ * until hc_host_pipeline_destroy: device staging for 3 chunks of `chunk_tokens` tokens of every
+ * input and output of hc_post_then_pre (3 * chunk_tokens * (2*hc*d*2 + 2*d*2 + 3*hc*4 + 2*hc*hc*4)
+ * bytes, plus alignment; 0 = 1024 tokens, at most 1 << 20); when hc is a multiple of 4, two
+ * segment buffers for the coefficient arrays of S = max(chunk_tokens, 65536) tokens each
+ * (2 * S * (4*hc*4 + 2*hc*hc*4) bytes), which then move once per segment of up to S tokens instead
+ * of once per chunk; its own zero-filled workspace; two non-blocking streams and its events. It
+ * synchronises its own copy stream once. Returns HC_ERR_NULL (out NULL), HC_ERR_SHAPE (hc < 1, d
+ * not a positive multiple of 8, chunk_tokens out of range), HC_ERR_UNSUPPORTED (hc > 8,
+ * d > 65536) or HC_ERR_CUDA (an allocation or a stream or event creation failed; nothing is left
+ * allocated). */
+int hc_host_pipeline_create(int hc, int d, int64_t chunk_tokens, hc_host_pipeline_t** out);
+
+/* Tokens per chunk of an executor. */
+int hc_host_pipeline_chunk_tokens(const hc_host_pipeline_t* p, int64_t* chunk_tokens);
+
+/* How a call on n tokens is cut into chunks by an executor of chunk_tokens (0 = the default, see
+ * hc_host_pipeline_create) tokens per chunk, C. Between ramps of halving size at both ends (C/2,
+ * C/4, ... down to the last size of at least max(128, C/32) tokens, five sizes at most) run chunks
+ * of C, the last of them shorter: the first copy-in and the last copy-out, which nothing overlaps,
+ * stay short, and most tokens move in a few large copies. When n is below both ramps plus one
+ * chunk, or C < 256, the tokens are cut into equal chunks of at most C tokens, and into up to 8
+ * when each keeps 32 tokens or more. Writes the number of chunks to *count; for 0 <= index < *count
+ * also the chunk's first token and size. index < 0 asks for the count only (t0 and tokens may then
+ * be NULL). Host-only, no CUDA call. Returns HC_ERR_NULL, HC_ERR_SHAPE (n < 0, chunk_tokens out of
+ * range) or HC_ERR_ARG (index >= count). */
+int hc_host_chunk_plan(int64_t n, int64_t chunk_tokens, int64_t index, int64_t* count, int64_t* t0,
+                       int64_t* tokens);
+
+/* Wait for every call enqueued on the executor to finish (host-side wait), then free what it owns.
+ * NULL is a no-op. Returns HC_ERR_CUDA if that wait reported an error (everything is freed anyway). */
+int hc_host_pipeline_destroy(hc_host_pipeline_t* p);
+
+/* hc_post_then_pre with every per-token array in HOST memory (delta, X, post, comb, pre_mix in;
+ * X_out, y_normed, pre_out, post_out, comb_out out; same layouts as hc_post_then_pre). The results
+ * are those of hc_post_then_pre applied to each chunk of hc_host_chunk_plan: X_out equals a single
+ * call on all n tokens bit for bit (it is per element); y_normed and the coefficients may differ
+ * from it in the last bits, since the order in which the mixes' partial sums meet follows the tile
+ * plan of the chunk's size. `next` holds [device] pointers, as for hc_post_then_pre. Host arrays
+ * need no alignment; page-locked ones (cudaHostAlloc, cudaHostRegister, torch pin_memory) let the
+ * copies run asynchronously and overlap; pageable ones work, but each copy then blocks the calling
+ * thread. The call enqueues everything and returns: the results are in host memory once `stream`
+ * has passed the call (e.g. after cudaStreamSynchronize(stream)); until then the host arrays must
+ * stay allocated and the inputs unchanged. The call starts after the earlier work on `stream` and
+ * after the previous call on the same executor. One executor serves one call at a time: calls on
+ * it from several host threads must be serialised by the caller. s.hc and s.d must be the
+ * executor's (HC_ERR_SHAPE otherwise); the current device must be the executor's (HC_ERR_ARG
+ * otherwise); no output may overlap an input or another output (HC_ERR_ALIAS). A failure part-way
+ * (HC_ERR_CUDA, or a status of the per-chunk hc_post_then_pre) leaves the outputs incomplete. */
+int hc_host_post_then_pre(hc_host_pipeline_t* p, const void* delta, const void* X, const float* post,
+                          const float* comb, const float* pre_mix, hc_params_t next, int64_t n,
+                          hc_shape_t s, void* X_out, void* y_normed, float* pre_out, float* post_out,
+                          float* comb_out, hc_stream_t stream);
 
 /* Diagnostic: the 24 mix numbers r * (X_flat . hc_fn^T) [device] fp32 [n, (2+hc)*hc] exactly as the
  * fused reading half computes them (same kernel, same tensor-core projection), for checking the

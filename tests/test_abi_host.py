@@ -265,3 +265,67 @@ def test_plan_tiles(lib):
     assert hc.hc_plan_tiles(0, 5120, 152)[2] == 0
     _expect(hc.HC_ERR_SHAPE, hc.hc_plan_tiles, 16, 5000, 152)
     _expect(hc.HC_ERR_SHAPE, hc.hc_plan_tiles, 16, 5120, 4)
+
+
+def test_host_pipeline_validation(lib):
+    """The host-buffer executor's checks that come before any CUDA call (creating a real executor
+    needs a GPU: tests/test_gpu_host_pipeline.py)."""
+    import ctypes
+    h = ctypes.c_void_p()
+    assert lib.hc_host_pipeline_create(4, 5120, 0, None) == hc.HC_ERR_NULL
+    for hcn, d, chunk, status in [(0, 5120, 0, hc.HC_ERR_SHAPE), (4, 0, 0, hc.HC_ERR_SHAPE),
+                                  (4, 5004, 0, hc.HC_ERR_SHAPE), (4, 5120, -1, hc.HC_ERR_SHAPE),
+                                  (4, 5120, (1 << 20) + 1, hc.HC_ERR_SHAPE), (9, 5120, 0, hc.HC_ERR_UNSUPPORTED),
+                                  (4, 65544, 0, hc.HC_ERR_UNSUPPORTED)]:
+        assert lib.hc_host_pipeline_create(hcn, d, chunk, ctypes.byref(h)) == status, (hcn, d, chunk)
+        assert h.value is None
+    assert lib.hc_host_pipeline_destroy(None) == hc.HC_OK
+    c = ctypes.c_int64(0)
+    assert lib.hc_host_pipeline_chunk_tokens(None, ctypes.byref(c)) == hc.HC_ERR_NULL
+    # a NULL executor or host array is refused before anything is dereferenced
+    s = hc.shape()
+    args = [A[0], A[1], A[2], A[3], A[4], _p(), 8, s, A[5], A[6], A[7], A[8], A[9], 0]
+    _expect(hc.HC_ERR_NULL, hc.hc_host_post_then_pre, None, *args)
+    for i in (0, 1, 2, 3, 4, 8, 9, 10, 11, 12):
+        bad = list(args)
+        bad[i] = None
+        _expect(hc.HC_ERR_NULL, hc.hc_host_post_then_pre, None, *bad)
+
+
+@pytest.mark.parametrize("n,chunk", [(0, 0), (1, 0), (5, 1024), (31, 0), (300, 128), (1000, 384), (2500, 256),
+                                     (5631, 2048), (5632, 2048), (16384, 0), (16384, 4096), (16384, 8192), (65536, 1024),
+                                     (1000, 256), (1152, 256), (4480, 4096), (4479, 4096),
+                                     (100, 1), (1 << 20, 1 << 20), (12345, 7)])
+def test_host_chunk_plan(lib, n, chunk):
+    """The executor's chunks tile [0, n) in order, none above the chunk size; large calls ramp
+    up and down by halving sizes (C/2 down to the last one of at least max(128, C/32) tokens)
+    around full chunks, small ones are cut evenly."""
+    plan = hc.hc_host_chunk_plan(n, chunk)
+    C = chunk or 1024
+    pos = 0
+    for t0, m in plan:
+        assert t0 == pos and 1 <= m <= C
+        pos += m
+    assert pos == n
+    ramp = [C >> j for j in range(1, 6) if (C >> j) >= max(128, C // 32)]
+    sizes = [m for _, m in plan]
+    if ramp and n >= 2 * sum(ramp) + C:
+        r = len(ramp)
+        assert sizes[:r] == ramp[::-1] and sizes[-r:] == ramp
+        assert all(m == C for m in sizes[r:-r - 1]) and 1 <= sizes[-r - 1] <= C
+    elif n:
+        assert max(sizes) - min(sizes) <= 1
+        assert len(plan) == max(-(-n // C), min(8, n // 32), 1)
+
+
+def test_host_chunk_plan_validation(lib):
+    import ctypes
+    c = ctypes.c_int64(0)
+    assert lib.hc_host_chunk_plan(10, 0, -1, None, None, None) == hc.HC_ERR_NULL
+    assert lib.hc_host_chunk_plan(-1, 0, -1, ctypes.byref(c), None, None) == hc.HC_ERR_SHAPE
+    assert lib.hc_host_chunk_plan(10, -1, -1, ctypes.byref(c), None, None) == hc.HC_ERR_SHAPE
+    assert lib.hc_host_chunk_plan(10, (1 << 20) + 1, -1, ctypes.byref(c), None, None) == hc.HC_ERR_SHAPE
+    assert lib.hc_host_chunk_plan(10, 0, 0, ctypes.byref(c), None, None) == hc.HC_ERR_NULL
+    t, m = ctypes.c_int64(0), ctypes.c_int64(0)
+    assert lib.hc_host_chunk_plan(10, 0, 1, ctypes.byref(c), ctypes.byref(t), ctypes.byref(m)) == hc.HC_ERR_ARG
+    assert lib.hc_host_chunk_plan(0, 0, -1, ctypes.byref(c), None, None) == hc.HC_OK and c.value == 0
