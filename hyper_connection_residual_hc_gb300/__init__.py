@@ -78,7 +78,7 @@ def load(path: str = LIB_PATH):
     lib.hc_expand_pre_step.argtypes = [P, hc_params_t, I64, hc_shape_t, P, P, P, P, P, P, P]
     lib.hc_final.argtypes = [P, P, P, I64, hc_shape_t, P, P]
     lib.hc_post_then_final.argtypes = [P, P, P, P, P, P, I64, hc_shape_t, P, P, P]
-    lib.hc_debug_mixes.argtypes = [P, hc_params_t, I64, hc_shape_t, P, P, P]
+    lib.hc_debug_mixes.argtypes = [P, hc_params_t, I64, hc_shape_t, I, P, P, P]
     lib.hc_plan_tiles.argtypes = [I64, I, I, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I64)]
     lib.hc_fused_ctas.argtypes = [ctypes.POINTER(I)]
     lib.hc_debug_wait_flag.argtypes = [P, I, ctypes.c_uint64, I64, P]
@@ -209,8 +209,9 @@ def hc_post_then_final(delta, X, post, comb, pre_mix, norm_w, n: int, s: hc_shap
         _stream(stream)))
 
 
-def hc_debug_mixes(X, p: hc_params_t, n: int, s: hc_shape_t, mixes, workspace, stream=None) -> None:
-    _check("hc_debug_mixes", load().hc_debug_mixes(_ptr(X), p, n, s, _ptr(mixes), _ptr(workspace), _stream(stream)))
+def hc_debug_mixes(X, p: hc_params_t, n: int, s: hc_shape_t, group: int, mixes, workspace, stream=None) -> None:
+    _check("hc_debug_mixes", load().hc_debug_mixes(_ptr(X), p, n, s, group, _ptr(mixes), _ptr(workspace),
+                                                   _stream(stream)))
 
 
 def hc_plan_tiles(n: int, d: int, ctas: int):

@@ -494,13 +494,15 @@ int hc_post_then_final(const void* delta, const void* X, const float* post, cons
     return final_impl(delta, X, post, comb, pre_mix, norm_w, n, s, X_out, z, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float* mixes, void* workspace,
+int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, int group, float* mixes, void* workspace,
                    hc_stream_t stream) {
     if (!X || !mixes || !p.hc_fn_planes || !workspace) return HC_ERR_NULL;
     hc_shape_t s2 = s;
     if (s2.sinkhorn_iters < 1) s2.sinkhorn_iters = 1;
     int st = check_shape(n, s2, true);
     if (st != HC_OK) return st;
+    if (group != 0 && group != 8 && group != 16 && group != 32) return HC_ERR_ARG;
+    if (fused_shape(s2) && group != 0 && s2.d % (32 * group) != 0) return HC_ERR_ARG;
     if (!aligned16(X) || !aligned16(mixes) || !aligned16(p.hc_fn_planes) || !aligned16(workspace))
         return HC_ERR_ALIGN;
     const Sizes z(n, s);
@@ -528,13 +530,14 @@ int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float*
     a.iters = s2.sinkhorn_iters;
     a.hc_eps = s2.hc_eps;
     a.norm_eps = s2.norm_eps;
+    a.group = group;
     return launch_status(launch_fused(a, cs));
 }
 
 int hc_plan_tiles(int64_t n, int d, int ctas, int* group, int* tile_m, int64_t* num_tiles) {
     if (!group || !tile_m || !num_tiles) return HC_ERR_NULL;
     if (n < 0 || d < 1 || d % 256 != 0 || ctas < 8) return HC_ERR_SHAPE;
-    plan_tiles(n, d, ctas, group, tile_m, num_tiles);
+    plan_tiles(n, d, ctas, 0, group, tile_m, num_tiles);
     return HC_OK;
 }
 

@@ -87,7 +87,7 @@ constexpr int kXTileBytes = kTileMax * kChunk * 2;            // 8192: 128 rows 
 constexpr int kBTileBytes = kBRows * kChunk * 2;              // 4608: 72 rows x 64 B (the MMA reads
                                                               // 80 rows; rows 72..79 are ignored)
 // One CTA's partial sums for one tile: mixes [128 tokens][24] (token-major), then
-// sum x^2 [2 column halves][128], then sum y^2 [2][128].
+// sum x^2 [128 tokens][2 column halves], then sum y^2 [128][2] (a token's two halves adjacent).
 constexpr int kPartRows = 28;
 constexpr int kPartFloats = kPartRows * kTileMax;
 constexpr int kPartSx = kMix * kTileMax, kPartSy = kPartSx + 2 * kTileMax;
@@ -603,8 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float2 sxx = __fadd2_rn(__fadd2_rn(sx[0], sx[1]), __fadd2_rn(sx[2], sx[3]));
             const float2 syy = __fadd2_rn(sy[0], sy[1]);
-            P[kPartSx + h * kTileMax + row] = sxx.x + sxx.y;
-            P[kPartSy + h * kTileMax + row] = syy.x + syy.y;
+            P[kPartSx + 2 * row + h] = sxx.x + sxx.y;
+            P[kPartSy + 2 * row + h] = syy.x + syy.y;
             // hand the block to the split warp, which publishes it; no waiting here
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarPublish));
@@ -623,13 +623,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // r_y of this thread's row from the group's sums of y^2 (2 halves of each of the kG
             // column shares), once the split warp has seen all their flags
             W.wait(bar(kBarFlagsSeen + buf), static_cast<uint32_t>((it >> 1) & 1), kErrEpilogue);
-            const float* blk = p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kG) * kPartFloats + kPartSy + row;
+            const float* blk =
+                p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kG) * kPartFloats + kPartSy + 2 * row;
+            // all kG loads in flight at once (one L2 round trip), summed in share order
+            float2 sq[kG];
+#pragma unroll
+            for (int r = 0; r < kG; ++r) sq[r] = ld_cg_f2(blk + static_cast<size_t>(r) * kPartFloats);
             float ssq = 0.f;
-#pragma unroll 8
-            for (int r = 0; r < kG; ++r) {
-                const float* Pr = blk + static_cast<size_t>(r) * kPartFloats;
-                ssq += ld_cg_f32(Pr) + ld_cg_f32(Pr + kTileMax);
-            }
+#pragma unroll
+            for (int r = 0; r < kG; ++r) ssq += sq[r].x + sq[r].y;
             const float ry = 1.0f / sqrtf(ssq * inv_d + p.norm_eps);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarEpiRead));  // this warp is done with the tile's blocks
@@ -806,35 +808,58 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long tile = cid + it * ncl;
             const long long t0 = tile * p.tile_m;
             const float* blk = p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kG) * kPartFloats;
-            // the owned tokens t = rank + kG i (i < kT = 128 / kG): lane = part * kT + i sums mixes
-            // part * kMP .. part * kMP + kMP - 1 of token i over the kG blocks (part 0 also sum x^2);
-            // the parts are then gathered into every lane of the token by shuffles
+            // the owned tokens t = rank + kG i (i < kT = 128 / kG). The kParts = 32 / kT lanes of token
+            // i (lane = part * kT + i) each sum the token's 24 mixes and sum x^2 over kG / kParts = 4
+            // of the group's blocks (shares part, part + kParts, ...: every load in flight at once);
+            // a reduce-scatter across those lanes then leaves lane `part` with mixes part * kMP ..
+            // part * kMP + kMP - 1 summed over all kG blocks, and an all-reduce gives each the sum x^2
             constexpr int kT = kTileMax / kG, kParts = 32 / kT, kMP = kMix / kParts;
+            constexpr int kShares = kG / kParts, kLog = kParts == 8 ? 3 : kParts == 4 ? 2 : 1;
+            static_assert(kShares * kParts == kG && (1 << kLog) == kParts, "gather split");
             const int oi = lane % kT, part = lane / kT;
             const int r_tok = static_cast<int>(rank) + kG * oi;
             const bool mine = r_tok < p.tile_m && t0 + r_tok < p.n;
-            float v[kMP];
+            float c[kMix];
 #pragma unroll
-            for (int i = 0; i < kMP; ++i) v[i] = 0.f;
+            for (int i = 0; i < kMix; ++i) c[i] = 0.f;
             float sxt = 0.f;
             if (mine) {
-#pragma unroll 8
-                for (int r = 0; r < kG; ++r) {
-                    const float* Pr = blk + static_cast<size_t>(r) * kPartFloats;
-                    const float* mp = Pr + r_tok * kMix + kMP * part;
-                    if (kMP % 4 == 0) {
+                float4 u[kShares][kMix / 4];
+                float2 sxr[kShares];
 #pragma unroll
-                        for (int q = 0; q < kMP / 4; ++q) {
-                            const float4 u = ld_cg_f4(mp + 4 * q);
-                            v[4 * q] += u.x; v[4 * q + 1] += u.y; v[4 * q + 2] += u.z; v[4 * q + 3] += u.w;
-                        }
-                    } else {
+                for (int j = 0; j < kShares; ++j) {
+                    const float* Pr = blk + static_cast<size_t>(part + kParts * j) * kPartFloats;
 #pragma unroll
-                        for (int i = 0; i < kMP; ++i) v[i] += ld_cg_f32(mp + i);
+                    for (int q = 0; q < kMix / 4; ++q) u[j][q] = ld_cg_f4(Pr + r_tok * kMix + 4 * q);
+                    sxr[j] = ld_cg_f2(Pr + kPartSx + 2 * r_tok);
+                }
+#pragma unroll
+                for (int j = 0; j < kShares; ++j) {
+#pragma unroll
+                    for (int q = 0; q < kMix / 4; ++q) {
+                        c[4 * q] += u[j][q].x; c[4 * q + 1] += u[j][q].y;
+                        c[4 * q + 2] += u[j][q].z; c[4 * q + 3] += u[j][q].w;
                     }
-                    if (part == 0) sxt += ld_cg_f32(Pr + kPartSx + r_tok) + ld_cg_f32(Pr + kPartSx + kTileMax + r_tok);
+                    sxt += sxr[j].x + sxr[j].y;
                 }
             }
+            // reduce-scatter: at level l the lanes split by bit (kLog - 1 - l) of `part`, each keeping
+            // one half of its current span and adding the partner's copy of that half
+#pragma unroll
+            for (int l = 0; l < kLog; ++l) {
+                const int half = (kMix >> l) / 2;
+                const int mask = kT << (kLog - 1 - l);
+                const bool upper = (lane & mask) != 0;
+#pragma unroll
+                for (int i = 0; i < half; ++i) {
+                    const float send = upper ? c[i] : c[i + half];
+                    const float keep = upper ? c[i + half] : c[i];
+                    c[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+                }
+            }
+#pragma unroll
+            for (int l = 0; l < kLog; ++l) sxt += __shfl_xor_sync(0xffffffffu, sxt, kT << l);
+            const float* v = c;  // this lane's kMP mixes
             float m[kMix];
 #pragma unroll
             for (int q = 0; q < kParts; ++q)
@@ -976,7 +1001,7 @@ int prepare_device(int* ctas) {
 // A stage costs the larger of its latency floor and a fixed part plus a part per token row; the
 // constants were measured on GB300 (2.1 us per 128-token stage of the prefill step, about 0.8 us
 // for a stage of a small batch, about 4 us per tile).
-void plan_tiles(int64_t n, int d, int ctas, int* group, int* tile_m, int64_t* num_tiles) {
+void plan_tiles(int64_t n, int d, int ctas, int only_group, int* group, int* tile_m, int64_t* num_tiles) {
     *group = 8;
     *tile_m = kTileMax;
     *num_tiles = 0;
@@ -985,7 +1010,7 @@ void plan_tiles(int64_t n, int d, int ctas, int* group, int* tile_m, int64_t* nu
     double best = -1.0;
     const int gs[3] = {8, 16, 32};
     for (int g : gs) {
-        if (d % (kChunk * g) != 0) continue;
+        if (d % (kChunk * g) != 0 || (only_group != 0 && g != only_group)) continue;
         const int groups = ctas / g;
         if (groups < 1) continue;
         const int S = d / (kChunk * g);
@@ -1017,7 +1042,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     if (st != 0) return st;
     int group = 8, tile_m = 0;
     int64_t num_tiles = 0;
-    plan_tiles(a.n, a.d, ctas, &group, &tile_m, &num_tiles);
+    plan_tiles(a.n, a.d, ctas, a.group, &group, &tile_m, &num_tiles);
     if (num_tiles == 0) return 0;
 
     const uint64_t n = static_cast<uint64_t>(a.n), d = static_cast<uint64_t>(a.d);

@@ -41,11 +41,13 @@ struct FusedArgs {
     int iters;
     float hc_eps;
     float norm_eps;
+    int group;               // CTAs per token tile: 0 = the launch plan's choice, else 8, 16 or 32
 };
 
 // Launch plan of the fused kernel for n tokens of width d when `ctas` CTAs can be resident at once:
 // CTAs per token tile (8, 16 or 32), tokens per tile and number of tiles.
-void plan_tiles(int64_t n, int d, int ctas, int* group, int* tile_m, int64_t* num_tiles);
+// only_group: 0 = any group size; 8, 16 or 32 = that one only (no tiles if d does not allow it)
+void plan_tiles(int64_t n, int d, int ctas, int only_group, int* group, int* tile_m, int64_t* num_tiles);
 
 // Launches the fused kernel; returns 0, -7 (CUDA failure) or -3 (no cooperative launch).
 int launch_fused(const FusedArgs& a, cudaStream_t stream);

@@ -292,6 +292,14 @@ __device__ __forceinline__ void st_release_gpu_u64(unsigned long long* p, unsign
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// A load that observes other CTAs' writes at GPU scope without ordering later accesses (cheaper
+// to repeat than an acquire; follow the last one with fence_acq_rel_gpu to acquire).
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -328,6 +336,13 @@ __device__ __forceinline__ float rcp_refined(float x) {
     const float r = rcp_approx(x);
     const float e = fmaf(-x, r, 1.0f);
     return fmaf(r, e, r);
+}
+
+// 8-byte load cached in L2 only (as ld_cg_f4).
+__device__ __forceinline__ float2 ld_cg_f2(const float* p) {
+    float2 v;
+    asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p) : "memory");
+    return v;
 }
 
 // 4-byte load cached in L2 only (as ld_cg_f4).

@@ -284,8 +284,14 @@ int hc_host_post_then_pre(hc_host_pipeline_t* p, const void* delta, const void* 
 
 /* Diagnostic: the 24 mix numbers r * (X_flat . hc_fn^T) [device] fp32 [n, (2+hc)*hc] exactly as the
  * fused reading half computes them (same kernel, same tensor-core projection), for checking the
- * projection on its own. p.hc_scale, p.hc_base and p.norm_w are not read. */
-int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, float* mixes,
+ * projection on its own. p.hc_scale, p.hc_base and p.norm_w are not read. A token's mixes depend on
+ * the group size of the launch (how many CTAs split its columns, so in which order their partial
+ * sums meet), not on which other tokens share its tile: `group` 0 takes the launch plan for n
+ * tokens; 8, 16 or 32 forces that group size (d a multiple of 32 * group), so that the mixes of
+ * sampled tokens reproduce bit for bit those of a call on more tokens (its group: hc_plan_tiles).
+ * The generic path (shapes the fused kernel does not take) ignores `group`. HC_ERR_ARG for another
+ * group value. */
+int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, int group, float* mixes,
                    void* workspace, hc_stream_t stream);
 
 /* Launch plan of the fused calls for n tokens of stream width d when `ctas` CTAs of the fused

@@ -96,10 +96,19 @@ def run_post_then_pre(delta, X, post, comb, pre_mix, P: DevParams, s, n):
     return o
 
 
-def debug_mixes(X, P: DevParams, s, n):
+def debug_mixes(X, P: DevParams, s, n, group=0):
+    """The GPU's own mixes of n tokens; `group` as the call being checked used (plan_group)."""
     m = torch.empty((n, (2 + s.hc) * s.hc), dtype=torch.float32, device="cuda")
-    hc.hc_debug_mixes(X, P.c, n, s, m, workspace())
+    hc.hc_debug_mixes(X, P.c, n, s, group, m, workspace())
     return m
+
+
+def plan_group(n, s):
+    """The group size (CTAs per token tile) of a fused call on n tokens of shape s; 0 for the
+    generic path. A token's mixes depend on it, not on its tile's other tokens."""
+    if s.hc != 4 or s.d % 256 or s.d > 5120 or n == 0:
+        return 0
+    return hc.hc_plan_tiles(n, s.d, hc.hc_fused_ctas())[0]
 
 
 def device_error_clear():
@@ -261,8 +270,11 @@ def sample_tokens(n, k, rng, tile=128):
     return np.array(sorted(idx), dtype=np.int64)
 
 
-def check_sampled(w, step, dev_in, out, prm, idx, post_mode, label):
-    """Oracle on the sampled tokens of one step, fed that step's device inputs (teacher-forced)."""
+def check_sampled(w, step, dev_in, out, prm, idx, post_mode, label, groups=None):
+    """Oracle on the sampled tokens of one step, fed that step's device inputs (teacher-forced).
+    The stage-isolated check feeds the oracle split the GPU's own mixes of those tokens, taken with
+    the group size of the call that produced `out` (that of a call on w.n tokens, or `groups[i]`
+    per sampled token), so that they are the very mixes that call used."""
     X = host_u16(dev_in["X"][idx])
     pm = host_f32(dev_in["pre_mix"][idx]).astype(np.float32)
     if post_mode:
@@ -277,5 +289,10 @@ def check_sampled(w, step, dev_in, out, prm, idx, post_mode, label):
     check_y_normed(host_u16(out["y_normed"][idx]), X, pm, prm["norm_w"], w.norm_eps, label + " y_normed")
     sub = {k: out[k][idx] for k in ("pre", "post", "comb")}
     P = DevParams(prm, w.d, w.hc)
-    m_gpu = host_f32(debug_mixes(dev_bf16(X), P, shape_of(w), len(idx)))
+    shp = shape_of(w)
+    gs = np.full(len(idx), plan_group(w.n, shp)) if groups is None else np.asarray(groups)
+    m_gpu = np.empty((len(idx), w.M))
+    for g in np.unique(gs):
+        sel = np.nonzero(gs == g)[0]
+        m_gpu[sel] = host_f32(debug_mixes(dev_bf16(X[sel]), P, shp, len(sel), int(g)))
     check_step(sub, ref, m_gpu, ref["mixes"], ref["S"], prm, w.iters, w.hc_eps, label)

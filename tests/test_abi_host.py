@@ -329,3 +329,15 @@ def test_host_chunk_plan_validation(lib):
     t, m = ctypes.c_int64(0), ctypes.c_int64(0)
     assert lib.hc_host_chunk_plan(10, 0, 1, ctypes.byref(c), ctypes.byref(t), ctypes.byref(m)) == hc.HC_ERR_ARG
     assert lib.hc_host_chunk_plan(0, 0, -1, ctypes.byref(c), None, None) == hc.HC_OK and c.value == 0
+
+
+def test_debug_mixes_group_validation(lib):
+    s = hc.shape()
+    W = A[15]
+    _expect(hc.HC_ERR_NULL, hc.hc_debug_mixes, None, _p(), 8, s, 0, A[1], W, 0)
+    _expect(hc.HC_ERR_ARG, hc.hc_debug_mixes, A[0], _p(), 8, s, 4, A[1], W, 0)
+    _expect(hc.HC_ERR_ARG, hc.hc_debug_mixes, A[0], _p(), 8, s, 64, A[1], W, 0)
+    # d = 256 splits over 8 CTAs only (32 columns each)
+    _expect(hc.HC_ERR_ARG, hc.hc_debug_mixes, A[0], _p(), 8, hc.shape(d=256), 16, A[1], W, 0)
+    _expect(hc.HC_ERR_ALIGN, hc.hc_debug_mixes, A[0] + 4, _p(), 8, s, 32, A[1], W, 0)
+    hc.hc_debug_mixes(A[0], _p(), 0, s, 32, A[1], W, 0)  # n == 0: no-op

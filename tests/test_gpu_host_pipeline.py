@@ -71,6 +71,15 @@ def _per_chunk_reference(dev, P, s, n, chunk):
     return {k: torch.cat(v) for k, v in parts.items()}
 
 
+def _chunk_groups(n, chunk, s, idx):
+    """The group size of the fused call that computed each sampled token (that of its chunk)."""
+    plan = hc.hc_host_chunk_plan(n, chunk)
+    starts = np.array([t0 for t0, _ in plan])
+    sizes = np.array([m for _, m in plan])
+    which = np.searchsorted(starts, idx, side="right") - 1
+    return np.array([gu.plan_group(int(sizes[c]), s) for c in which])
+
+
 def _assert_same(hout, ref, label):
     for k in OUT:
         a, b = hout[k], ref[k]
@@ -102,7 +111,8 @@ def test_host_pipeline_matches_device_chunks_and_oracle(n, chunk, d, hcn):
     dev = {k: hin[k].cuda() for k in IN}
     _assert_same(hout, _per_chunk_reference(dev, P, s, n, chunk), "n=%d chunk=%d" % (n, chunk))
     idx = np.arange(n) if n <= 400 else gu.sample_tokens(n, 300, np.random.default_rng(n))
-    gu.check_sampled(w, 0, dev, hout, prm, idx, True, "host pipeline n=%d d=%d hc=%d" % (n, d, hcn))
+    gu.check_sampled(w, 0, dev, hout, prm, idx, True, "host pipeline n=%d d=%d hc=%d" % (n, d, hcn),
+                     _chunk_groups(n, chunk, s, idx))
     gu.device_error_clear()
 
 
@@ -192,5 +202,5 @@ def test_host_pipeline_prefill_b4_t4096():
     assert torch.equal(hout["X_out"].view(torch.int16), full["X_out"].cpu().view(torch.int16))
     del full
     idx = gu.sample_tokens(n, 400, np.random.default_rng(4096))
-    gu.check_sampled(w, 0, dev, hout, prm, idx, True, "host pipeline prefill")
+    gu.check_sampled(w, 0, dev, hout, prm, idx, True, "host pipeline prefill", _chunk_groups(n, 0, s, idx))
     gu.device_error_clear()

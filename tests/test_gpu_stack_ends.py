@@ -61,7 +61,9 @@ def check_expand(w, h_host, out, prm, idx, label):
     gu.assert_bf16_close(gu.host_u16(out["y_normed"][idx]), yn_h, label + " y_normed vs norm(h)")
     sub = {k: out[k][idx] for k in ("pre", "post", "comb")}
     P = gu.DevParams(prm, w.d)
-    m_gpu = gu.host_f32(gu.debug_mixes(gu.dev_bf16(want), P, gu.shape_of(w), len(idx)))
+    # the GPU's own mixes of these tokens, with the group size of the call on all w.n tokens
+    m_gpu = gu.host_f32(gu.debug_mixes(gu.dev_bf16(want), P, gu.shape_of(w), len(idx),
+                                       gu.plan_group(w.n, gu.shape_of(w))))
     gu.check_step(sub, ref, m_gpu, m_ref, S, prm, w.iters, w.hc_eps, label)
 
 
