@@ -81,6 +81,29 @@ def _dist():
     return rank, world, local
 
 
+def rank_workload(w0, rank: int):
+    """This rank's batch: the workload's shapes and distributions with a seed of its own. Tokens are
+    independent, so each rank steps its own batch and no data crosses ranks (weak scaling)."""
+    import dataclasses
+    return dataclasses.replace(w0, seed=w0.seed + 17 * rank) if rank else w0
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The slowest rank's value of a timing (x itself when there is one process). The only
+    collective of a run: the step has no data-path exchange."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Units all ranks processed per second of the slowest rank."""
+    return units_per_rank * world / seconds
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -259,9 +282,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     hc.load()
 
-    w0 = synth.WORKLOADS[WORKLOAD]
-    import dataclasses
-    w = dataclasses.replace(w0, seed=w0.seed + 17 * rank) if rank else w0  # each rank its own batch
+    w = rank_workload(synth.WORKLOADS[WORKLOAD], rank)
     n, d = w.n, w.d
     prm = synth.params(w, 0)
 
@@ -358,10 +379,7 @@ def run_ours(args):
     clk = clocks.stop()
     el_ms = t_start.elapsed_time(t_end)
     kern_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
-    if dist is not None:
-        t = torch.tensor([el_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        el_ms = float(t.item())
+    el_ms = max_over_ranks(el_ms, dist, "cuda")
     derr = hc.hc_device_error(clear=True)
 
     # end to end through the C ABI: pinned host inputs in, results out, every step
@@ -403,13 +421,9 @@ def run_ours(args):
     e2e_s = time.perf_counter() - t0
     if pipe is not None:
         pipe.close()
-    if dist is not None:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, dist, "cuda")
 
-    tokens_total = n * world
-    value = tokens_total * args.steps / (el_ms / 1e3)
+    value = whole_job_rate(n * args.steps, world, el_ms / 1e3)
     peak, peak_kind = _peaks()
     alg_bytes = n * spec["bytes_per_token"] + spec["param_bytes"]
     achieved = alg_bytes / (kern_ms / 1e3) / 1e9
@@ -443,7 +457,7 @@ def run_ours(args):
                          "traffic": _traffic_per_launch(n, op), "algorithmic_bytes": alg_bytes,
                          "kernel": spec["kernel"], "kernel_ms": kern_ms},
             "cpu_baseline": cpu,
-            "e2e": {"value": tokens_total * e2e_steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": whole_job_rate(n * e2e_steps, world, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "path": e2e_path},
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
@@ -464,8 +478,6 @@ def run_decode_chain(args):
     library's calls (hc_expand_pre_step, 79 x hc_post_then_pre, hc_post_then_final). The sublayers'
     outputs Delta are drawn beforehand (the sublayer itself is not part of the path), so the graph
     holds only the library's 81 launches. Timed by CUDA events around graph replays."""
-    import dataclasses
-
     import numpy as np
     import torch
 
@@ -480,8 +492,7 @@ def run_decode_chain(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     hc.load()
-    w0 = synth.WORKLOADS[DECODE]
-    w = dataclasses.replace(w0, seed=w0.seed + 17 * rank) if rank else w0
+    w = rank_workload(synth.WORKLOADS[DECODE], rank)
     n, d, L = w.n, w.d, w.steps
 
     def bf(a):
@@ -552,11 +563,7 @@ def run_decode_chain(args):
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    el_ms = t0.elapsed_time(t1)
-    if dist is not None:
-        t = torch.tensor([el_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        el_ms = float(t.item())
+    el_ms = max_over_ranks(t0.elapsed_time(t1), dist, "cuda")
     derr = hc.hc_device_error(clear=True)
 
     # end to end: the embedding in from pinned host memory and z out, every chain
@@ -569,7 +576,7 @@ def run_decode_chain(args):
         graph.replay()
         z_host.copy_(z, non_blocking=True)
         stream.synchronize()
-    e2e_s = time.perf_counter() - w0t
+    e2e_s = max_over_ranks(time.perf_counter() - w0t, dist, "cuda")
 
     chain_ms = el_ms / steps
     sub_tokens = n * L * world
