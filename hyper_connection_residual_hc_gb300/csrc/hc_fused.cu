@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     hc_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmD,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmXo,
                     const __grid_constant__ CUtensorMap tmM, const __grid_constant__ CUtensorMap tmY,
-                    const FusedParams p) {
+                    const __grid_constant__ CUtensorMap tmYr, const FusedParams p) {
     using Lay = Layout<kMode>;
     constexpr int kStages = Lay::kStages, kStageBytes = Lay::kStage;
     constexpr int kOffX = Lay::kOffX, kOffD = Lay::kOffD, kOffB = Lay::kOffB, kOffNormW = Lay::kOffNormW;
@@ -495,6 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < S; ++s, ++g) {
                 // the y store of the previous stage has had a stage to complete: hand it over
                 if (s > 0) y_ready(g - 1);
+                // reading-only modes: the MMA of this stage reads the tile as loaded, so it may start
+                // as soon as the data lands; drain the previous stage's accumulator first to let it
+                if (!kPost && s > 0) drain(g - 1);
                 // the ring slot of this stage's y last held the chunk of stage g - kRing
                 const long long yround = g / kRing;
                 if (yround > 0)
@@ -582,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // drain the previous stage's accumulator now: its MMA ran while this stage was
                 // computed, so nothing waits here, and the MMA of this stage (which needs the
                 // accumulator empty) is issued right after
-                if (s > 0) drain(g - 1);
+                if (kPost && s > 0) drain(g - 1);
             }
             drain(g - 1);
             y_ready(g - 1);
@@ -636,9 +639,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarEpiRead));  // this warp is done with the tile's blocks
             const long long t0 = (cid + it * ncl) * p.tile_m;
-            // this warp's 32 rows go out as one TMA tile when they lie in the tile (rows past n are
-            // clipped by the tensor map; rows past tile_m would belong to the next tile)
-            const bool store = p.write_y && 32 * q < p.tile_m;
+            // this warp's rows go out as one TMA tile: 32 rows, or the tile's last tile_m % 32 rows
+            // through the second map (rows past n are clipped by the maps; rows past tile_m belong
+            // to the next tile and are never stored)
+            const int rows_q = p.tile_m - 32 * q;
+            const bool store = p.write_y && rows_q > 0;
+            const CUtensorMap* ymap = rows_q >= 32 ? &tmY : &tmYr;
             for (int s = 0; s < S; ++s, ++g) {
                 const int ys = static_cast<int>(g % kRing);
                 W.wait(bar(kBarYReady + ys), static_cast<uint32_t>((g / kRing) & 1), kErrEpilogue);
@@ -667,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmY, st, stage_col(s), static_cast<int>(t0 + 32 * q));
+                        tma_store_2d(ymap, st, stage_col(s), static_cast<int>(t0 + 32 * q));
                         bulk_commit();
                     }
                     ++ystores;
@@ -726,7 +732,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int slot = static_cast<int>(g % kStages);
                 // the single accumulator must have been drained (stage g - 1)
                 if (g > 0) W.wait(bar(kBarAccEmpty), static_cast<uint32_t>((g - 1) & 1), kErrMma);
-                W.wait(bar(kBarXReady + slot), static_cast<uint32_t>((g / kStages) & 1), kErrMma);
+                // post mode multiplies the X' the compute warps wrote; the other modes the loaded tile
+                W.wait(bar((kPost ? kBarXReady : kBarFull) + slot), static_cast<uint32_t>((g / kStages) & 1), kErrMma);
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t sb = sbase + slot * kStageBytes;
@@ -995,8 +1002,8 @@ int prepare_device(int* ctas) {
 
 }  // namespace
 
-// Launch plan: for each group size g (d a multiple of 32 g) and tile height m (32..128, or n when
-// n < 32), groups = ctas / g groups run at once; a launch takes ceil(tiles / groups) waves of S =
+// Launch plan: for each group size g (d a multiple of 32 g) and tile height m (32, 64, 96, 128, a
+// balanced height of 96..128 for batches of several waves, or n when n < 32), groups = ctas / g groups run at once; a launch takes ceil(tiles / groups) waves of S =
 // d / (32 g) column stages each, plus a per-tile cost (group exchange, y_normed epilogue tail).
 // A stage costs the larger of its latency floor and a fixed part plus a part per token row; the
 // constants were measured on GB300 (2.1 us per 128-token stage of the prefill step, about 0.8 us
@@ -1014,8 +1021,15 @@ void plan_tiles(int64_t n, int d, int ctas, int only_group, int* group, int* til
         const int groups = ctas / g;
         if (groups < 1) continue;
         const int S = d / (kChunk * g);
-        // tile heights, largest first (ties keep the larger tile and the smaller group)
-        const int ms[5] = {128, 96, 64, 32, n < 32 ? static_cast<int>(n) : 0};
+        // tile heights, largest first (ties keep the larger tile and the smaller group), then for
+        // batches of several waves the height that spreads the tokens evenly over the waves
+        // 128-token tiles would take (16,384 tokens: 133 tiles of 124 fill 7 waves of 19 groups,
+        // where 128 tiles of 128 leave 5 groups idle in the last); only from 96 rows up, where a
+        // stage's time still follows its rows (shorter balanced tiles measured slower)
+        const int64_t waves128 = ((n + kTileMax - 1) / kTileMax + groups - 1) / groups;
+        const int m_even = static_cast<int>((n + groups * waves128 - 1) / (groups * waves128));
+        const int ms[6] = {128, 96, 64, 32, n < 32 ? static_cast<int>(n) : 0,
+                           waves128 > 1 && m_even >= 96 ? m_even : 0};
         for (int m : ms) {
             if (m < 1) continue;
             const int64_t tiles = (n + m - 1) / m;
@@ -1052,7 +1066,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     const bool write_x = a.mode != kModePre;
     const void* x_in = a.mode == kModeExpand ? a.X_out : a.X;
     const void* rows = a.mode == kModePost ? a.delta : a.mode == kModeExpand ? a.embed : a.X;
-    CUtensorMap tmX, tmD, tmB, tmXo, tmM, tmY;
+    CUtensorMap tmX, tmD, tmB, tmXo, tmM, tmY, tmYr;
     {
         const uint64_t dims[3] = {d, 4, n};
         const uint64_t str[2] = {d * 2, 4 * d * 2};
@@ -1070,6 +1084,9 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
         // y_normed in 32-row tiles, one per epilogue warp (encoded on the read rows when it is not written)
         const uint32_t ybox[2] = {kChunk, 32};
         if (!encode(&tmY, a.y_normed ? a.y_normed : rows, 2, dims, str, ybox, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+        // and the last rows of a tile whose height is not a multiple of 32
+        const uint32_t yrbox[2] = {kChunk, static_cast<uint32_t>(tile_m % 32 ? tile_m % 32 : 32)};
+        if (!encode(&tmYr, a.y_normed ? a.y_normed : rows, 2, dims, str, yrbox, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
     }
     {
         const uint64_t dims[2] = {4 * d, static_cast<uint64_t>(kBRows)};
@@ -1120,7 +1137,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaErrorInvalidValue;
-    auto go = [&](auto kernel) { e = cudaLaunchKernelEx(&cfg, kernel, tmX, tmD, tmB, tmXo, tmM, tmY, p); };
+    auto go = [&](auto kernel) { e = cudaLaunchKernelEx(&cfg, kernel, tmX, tmD, tmB, tmXo, tmM, tmY, tmYr, p); };
     if (a.mode == kModePost) {
         if (group == 8) go(hc_fused_kernel<kModePost, 8>);
         else if (group == 16) go(hc_fused_kernel<kModePost, 16>);

@@ -297,8 +297,9 @@ int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, int gr
 /* Launch plan of the fused calls for n tokens of stream width d when `ctas` CTAs of the fused
  * kernel can be resident at once (hc_fused_ctas): the CTAs that share one token tile (`group`: 8,
  * 16 or 32, each taking d/group columns; small batches use larger groups, so each CTA has fewer
- * column stages), the tokens per tile (32, 64, 96 or 128; n itself when n < 32) and the number of
- * tiles. Host-only, no CUDA call. Returns HC_ERR_NULL / HC_ERR_SHAPE (n < 0, d not a positive
+ * column stages), the tokens per tile (32, 64, 96 or 128; for batches of several waves possibly
+ * the height between 96 and 128 that spreads the tiles evenly over the waves; n itself when
+ * n < 32) and the number of tiles. Host-only, no CUDA call. Returns HC_ERR_NULL / HC_ERR_SHAPE (n < 0, d not a positive
  * multiple of 256, ctas < 8) on bad arguments. */
 int hc_plan_tiles(int64_t n, int d, int ctas, int* group, int* tile_m, int64_t* num_tiles);
 

@@ -252,9 +252,14 @@ def test_plan_tiles(lib):
                 assert 1 <= tm <= 128
                 assert nt * tm >= n and (nt - 1) * tm < n
                 if nt > 1:
-                    assert tm % 32 == 0
-    # the prefill batch: 128-token tiles over 19 groups of 8 (all 152 SMs of a GB300)
-    assert hc.hc_plan_tiles(16384, 5120, 152) == (8, 128, 128)
+                    assert tm % 32 == 0 or 96 <= tm <= 128
+    # the prefill batch over 19 groups of 8 (all 152 SMs of a GB300): 133 tiles of 124 tokens fill
+    # exactly 7 waves, where 128 tiles of 128 would leave 5 groups idle in the last
+    assert hc.hc_plan_tiles(16384, 5120, 152) == (8, 124, 133)
+    # balanced heights only for several waves and only from 96 rows up
+    assert hc.hc_plan_tiles(4096, 5120, 152) == (8, 108, 38)
+    assert hc.hc_plan_tiles(2468, 1024, 152) == (8, 96, 26)
+    assert hc.hc_plan_tiles(65536, 5120, 152) == (8, 128, 512)
     # a decode batch spreads each tile over more CTAs: fewer column stages per CTA
     g, tm, nt = hc.hc_plan_tiles(256, 5120, 152)
     assert g == 32 and g * nt <= 152
