@@ -16,32 +16,36 @@
 // four streams, is written four times to the streams, and the identity pre_mix (1/4 each)
 // collapses the four copies back to h exactly.
 //
-// Decomposition. A group of 8 CTAs owns a tile of up to 128 tokens; CTA `rank` of the group owns
-// d/8 columns of every stream, the 32-column chunks rank, rank+8, rank+16, ... (interleaved, so
-// the group's loads of one stage cover 256 contiguous columns of each row). The 16 warps of a
-// CTA have fixed roles:
-//   producer (warp 8): per 32-column stage, TMA-loads the four X tiles [tokens x 32 cols], the
-//     Delta tile and the four matching slices of the split projection weights (bf16 planes
-//     hi/mid/lo, 72 rows) into one of 3 shared-memory slots, 64-byte swizzled;
+// Decomposition. A group of kG CTAs (8 for large batches; 16 or 32 for small ones, so that each CTA
+// has fewer column stages) owns a tile of up to 128 tokens; CTA `rank` of the group owns d/kG
+// columns of every stream, the 32-column chunks rank, rank+kG, rank+2kG, ... (interleaved, so the
+// group's loads of one stage cover kG*32 contiguous columns of each row). The 16 warps of a CTA
+// have fixed roles:
+//   producer (warp 8): per 32-column stage, TMA-loads the four X tiles [tokens x 32 cols] (expand
+//     mode: the one embedding tile), the Delta tile (post mode) and the four matching slices of
+//     the split projection weights (bf16 planes hi/mid/lo, 72 rows) into a ring of shared-memory
+//     slots, 64-byte swizzled: 3 slots in post mode, 4 in pre mode, 6 in expand mode;
 //   compute (warps 0-7, thread = token, two warps per TMEM lane quadrant, 16 columns each):
-//     compute X' in place, accumulate sum(X'^2), form and round y, accumulate sum(y^2), store the
-//     bf16 y chunk into a ring of 27 chunk slots in tensor memory, and drain the previous
-//     stage's accumulator into 12 per-thread fp32 sums (the three planes added back together);
+//     compute X' in place (post mode; the other modes read the loaded tile), accumulate sum(X'^2),
+//     form and round y, accumulate sum(y^2), store the bf16 y chunk into a ring of 27 chunk slots
+//     in tensor memory, and drain the previous stage's accumulator into 12 per-thread fp32 sums
+//     (the three planes added back together);
 //   MMA (warp 9): one thread issues 8 tcgen05.mma per stage (M=128 tokens, N=80 >= 72 plane
 //     rows, K=16) projecting the bf16 X' tile on the three planes into a TMEM accumulator; the
 //     products are exact in fp32, so the split projection has fp32-FFMA accuracy;
 //   store (warp 10): TMA-stores the X' tile (written once) from the same slot, then frees it;
 //   split (warp 11): at each tile end, publishes the CTA's partial sums (28 per token, in a
-//     caller-provided global workspace) with a release flag, waits (bounded) for the 7 other flags
-//     of the group, turns the sums of y^2 into r_y for all 128 rows, and runs the split and
-//     Sinkhorn for the tokens t with t % 8 == rank;
-//   epilogue (warps 12-15, one per TMEM lane quadrant): read each y chunk back from the ring,
-//     scale it by norm_w and r_y and write y_normed with 64-byte row stores.
-// The ring gives the exchange 7 stages of slack: the compute warps stream on into the next tile
-// while the group finishes the previous one. The groups are formed in software rather than as
-// hardware clusters because only 15 clusters of 8 CTAs fit on a GB300 at once (120 of its 152
-// SMs); the launch is cooperative, so all CTAs are resident together and the flag waits between
-// them cannot deadlock.
+//     caller-provided global workspace) with a release flag, waits (bounded) for the other flags
+//     of the group, gathers the mixes of its own tokens (t % kG == rank) over the group's blocks,
+//     and runs their split and Sinkhorn;
+//   epilogue (warps 12-15, one per TMEM lane quadrant): turn the group's sums of y^2 into r_y of
+//     the warp's rows, read each y chunk back from the ring, scale it by norm_w and r_y into a
+//     32-row swizzled staging tile and TMA-store it to y_normed.
+// The ring holds a tile's y until the exchange gives r_y, with 7 stages of slack at 20 stages a
+// tile: the compute warps stream on into the next tile while the group finishes the previous one.
+// The groups are formed in software rather than as hardware clusters because only 15 clusters of
+// 8 CTAs fit on a GB300 at once (120 of its 152 SMs); the launch is cooperative, so all CTAs are
+// resident together and the flag waits between them cannot deadlock.
 //
 // Every wait on an mbarrier is bounded in time; on expiry the kernel records an error in a
 // device word, stops waiting everywhere, finishes its loops without hanging, frees its tensor
