@@ -19,3 +19,12 @@ def pytest_configure(config):
 def orc_lib():
     import oracle
     return oracle.load()
+
+
+@pytest.fixture(autouse=True)
+def _output_guard_bands():
+    """After every test: no kernel wrote into the guard bands of the outputs it allocated."""
+    yield
+    gu = sys.modules.get("gpu_util")
+    if gu is not None:
+        gu.check_guards()

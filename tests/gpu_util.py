@@ -73,13 +73,60 @@ def workspace():
     return _WS
 
 
+# ---- guard bands around outputs ------------------------------------------------------------------
+# An output allocated through `guarded` sits between two 4 KB bands of 0xA5 bytes. A kernel that writes
+# past either end of the output (a ragged last tile, a wrong row count in a tensor map, an index one
+# row too far) lands in a band, which no parity check of the output itself would see. `check_guards`
+# verifies the bands of every output allocated since the last check; conftest runs it after every
+# test, and `guarded` runs it once the held outputs reach 8 GB, so that long chains stay bounded.
+GUARD_BYTES = 4096
+GUARD_VALUE = 0xA5
+_GUARD_CHECK_BYTES = 8 << 30
+_guarded = []        # (buffer, output bytes) of the outputs allocated since the last check
+_guarded_bytes = 0
+
+
+def guarded(shape, dtype=torch.bfloat16, device="cuda") -> torch.Tensor:
+    """An uninitialised tensor of `shape` and `dtype` with a guard band on each side (its address stays
+    16-byte aligned: the band is 4 KB and the allocator's blocks are aligned further)."""
+    global _guarded_bytes
+    count = 1
+    for e in shape:
+        count *= int(e)
+    nbytes = count * torch.tensor([], dtype=dtype).element_size()
+    if _guarded_bytes + nbytes > _GUARD_CHECK_BYTES:
+        check_guards()
+    buf = torch.empty(2 * GUARD_BYTES + nbytes, dtype=torch.uint8, device=device)
+    buf[:GUARD_BYTES].fill_(GUARD_VALUE)
+    buf[GUARD_BYTES + nbytes:].fill_(GUARD_VALUE)
+    _guarded.append((buf, nbytes))
+    _guarded_bytes += nbytes
+    return buf[GUARD_BYTES:GUARD_BYTES + nbytes].view(dtype).view(tuple(shape))
+
+
+def check_guards():
+    """Raise if any guard band of an output allocated since the last check was written; forget them."""
+    global _guarded, _guarded_bytes
+    held, _guarded, _guarded_bytes = _guarded, [], 0
+    if not held:
+        return
+    if any(b.is_cuda for b, _ in held):
+        torch.cuda.synchronize()
+    for buf, nbytes in held:
+        for side, band in (("before", buf[:GUARD_BYTES]), ("after", buf[GUARD_BYTES + nbytes:])):
+            bad = (band != GUARD_VALUE).nonzero()
+            if bad.numel():
+                raise AssertionError("%d bytes of the guard band %s an output of %d bytes were written (first at "
+                                     "band byte %d)" % (bad.numel(), side, nbytes, int(bad[0])))
+
+
 def alloc_outputs(n: int, d: int, post_mode: bool, hcn: int = 4):
-    o = dict(y_normed=torch.empty((n, d), dtype=torch.bfloat16, device="cuda"),
-             pre=torch.empty((n, hcn), dtype=torch.float32, device="cuda"),
-             post=torch.empty((n, hcn), dtype=torch.float32, device="cuda"),
-             comb=torch.empty((n, hcn, hcn), dtype=torch.float32, device="cuda"))
+    o = dict(y_normed=guarded((n, d), torch.bfloat16),
+             pre=guarded((n, hcn), torch.float32),
+             post=guarded((n, hcn), torch.float32),
+             comb=guarded((n, hcn, hcn), torch.float32))
     if post_mode:
-        o["X_out"] = torch.empty((n, hcn, d), dtype=torch.bfloat16, device="cuda")
+        o["X_out"] = guarded((n, hcn, d), torch.bfloat16)
     return o
 
 
@@ -98,7 +145,7 @@ def run_post_then_pre(delta, X, post, comb, pre_mix, P: DevParams, s, n):
 
 def debug_mixes(X, P: DevParams, s, n, group=0):
     """The GPU's own mixes of n tokens; `group` as the call being checked used (plan_group)."""
-    m = torch.empty((n, (2 + s.hc) * s.hc), dtype=torch.float32, device="cuda")
+    m = guarded((n, (2 + s.hc) * s.hc), torch.float32)
     hc.hc_debug_mixes(X, P.c, n, s, group, m, workspace())
     return m
 

@@ -57,7 +57,7 @@ def test_generic_reading_and_writing(hcn, n, d):
     gu.check_step(out, ref, m_gpu, ref["mixes"], ref["S"], prm, w.iters, w.hc_eps, label + " pre_step")
     # writing half + next reading half, and the tap
     o = gu.alloc_outputs(n, d, True, hcn)
-    mean = torch.empty((n, d), dtype=torch.bfloat16, device="cuda")
+    mean = gu.guarded((n, d), torch.bfloat16)
     hc.hc_post_then_pre_tap(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P.c, n, s, o["X_out"],
                             o["y_normed"], o["pre"], o["post"], o["comb"], mean, gu.workspace())
     xo = gu.host_u16(o["X_out"])
@@ -77,7 +77,7 @@ def test_generic_reading_and_writing(hcn, n, d):
     for k in ("X_out", "y_normed", "pre", "post", "comb"):
         assert torch.equal(o[k], o2[k]), k
     # hc_post alone, also in place
-    Xp = torch.empty_like(dev["X"])
+    Xp = gu.guarded(dev["X"].shape, dev["X"].dtype)
     hc.hc_post(dev["delta"], dev["X"], dev["post"], dev["comb"], n, s, Xp)
     assert torch.equal(Xp, o["X_out"])
     gu.device_error_clear()
@@ -104,17 +104,17 @@ def test_generic_stack_ends(hcn, n, d):
     # tail of the stack
     fw = synth.final_norm_w(w)
     sf = hc.shape(d=d, norm_eps=1e-20, hc=hcn)
-    z = torch.empty((n, d), dtype=torch.bfloat16, device="cuda")
+    z = gu.guarded((n, d), torch.bfloat16)
     hc.hc_final(dev["X"], dev["pre_mix"], gu.dev_f32(fw), n, sf, z)
     gu.check_y_normed(gu.host_u16(z), inp["X"], inp["pre_mix"], fw, 1e-20, label + " final z")
-    Xo = torch.empty_like(dev["X"])
-    z2 = torch.empty_like(z)
+    Xo = gu.guarded(dev["X"].shape, dev["X"].dtype)
+    z2 = gu.guarded(z.shape, z.dtype)
     hc.hc_post_then_final(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], gu.dev_f32(fw), n, sf, Xo,
                           z2)
     xo = gu.host_u16(Xo)
     gu.check_xprime(xo, inp["X"], inp["delta"], inp["post"], inp["comb"], label + " tail X'")
     gu.check_y_normed(gu.host_u16(z2), xo, inp["pre_mix"], fw, 1e-20, label + " tail z")
-    z3 = torch.empty_like(z)
+    z3 = gu.guarded(z.shape, z.dtype)
     hc.hc_post_then_final(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], gu.dev_f32(fw), n, sf,
                           None, z3)
     assert torch.equal(z2, z3)

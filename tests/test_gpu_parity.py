@@ -124,7 +124,7 @@ def test_hc_post_matches_oracle(n, d):
     inp = _inputs(w)
     s = hc.shape(d=d)
     X = gu.dev_bf16(inp["X"])
-    out = torch.empty_like(X)
+    out = gu.guarded(X.shape, X.dtype)
     hc.hc_post(gu.dev_bf16(inp["delta"]), X, gu.dev_f32(inp["post"]), gu.dev_f32(inp["comb"]), n, s, out)
     ex, worst = gu.check_xprime(gu.host_u16(out), inp["X"], inp["delta"], inp["post"], inp["comb"], "hc_post")
     print("n=%d d=%d hc_post bit-exact %.6f, max ulp %d" % (n, d, ex, worst))
@@ -331,7 +331,7 @@ def test_workload_decode_chain_b256_80steps():
     state, worst = _run_chain(w, 256, first_pre_step=True, fresh_delta=False)
     # the chain's tail: the last writing half alone
     delta = gu.dev_bf16(synth.tokens(w, T_DELTA, w.steps))
-    Xf = torch.empty_like(state["X"])
+    Xf = gu.guarded(state["X"].shape, state["X"].dtype)
     hc.hc_post(delta, state["X"], state["post"], state["comb"], w.n, _shape(w), Xf)
     gu.check_xprime(gu.host_u16(Xf), gu.host_u16(state["X"]), gu.host_u16(delta),
                     gu.host_f32(state["post"]).astype(np.float32), gu.host_f32(state["comb"]).astype(np.float32),

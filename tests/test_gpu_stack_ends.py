@@ -128,7 +128,7 @@ def _final_inputs(w, scale=None):
 def test_final_matches_oracle(n, d, eps):
     w = synth.small("step_b1_t64", 1, n, d, seed=700 + n + d)
     X, pm, fw = _final_inputs(w)
-    z = torch.empty((n, d), dtype=torch.bfloat16, device="cuda")
+    z = gu.guarded((n, d), torch.bfloat16)
     hc.hc_final(gu.dev_bf16(X), gu.dev_f32(pm), gu.dev_f32(fw), n, hc.shape(d=d, norm_eps=eps), z)
     exact, worst = gu.check_y_normed(gu.host_u16(z), X, pm, fw, eps, "z")
     ref, _, _ = orc.hc_final(X, pm, fw, eps)
@@ -144,7 +144,7 @@ def test_final_small_values_see_the_eps():
     X, pm, fw = _final_inputs(w, scale=2.0 ** -14)
     zs = {}
     for eps in (FINAL_EPS, 1e-6):
-        z = torch.empty((n, d), dtype=torch.bfloat16, device="cuda")
+        z = gu.guarded((n, d), torch.bfloat16)
         hc.hc_final(gu.dev_bf16(X), gu.dev_f32(pm), gu.dev_f32(fw), n, hc.shape(d=d, norm_eps=eps), z)
         gu.check_y_normed(gu.host_u16(z), X, pm, fw, eps, "z eps=%g" % eps)
         zs[eps] = gu.host_u16(z)
@@ -159,8 +159,8 @@ def test_post_then_final_matches_oracle(n, d):
     pm, fw = synth.tokens(w, T_PREMIX, 0), synth.final_norm_w(w)
     s = hc.shape(d=d, norm_eps=FINAL_EPS)
     dev = [gu.dev_bf16(delta), gu.dev_bf16(X), gu.dev_f32(post), gu.dev_f32(comb), gu.dev_f32(pm), gu.dev_f32(fw)]
-    Xo = torch.empty((n, 4, d), dtype=torch.bfloat16, device="cuda")
-    z = torch.empty((n, d), dtype=torch.bfloat16, device="cuda")
+    Xo = gu.guarded((n, 4, d), torch.bfloat16)
+    z = gu.guarded((n, d), torch.bfloat16)
     hc.hc_post_then_final(*dev, n, s, Xo, z)
     xo = gu.host_u16(Xo)
     ex_x, _ = gu.check_xprime(xo, X, delta, post, comb)
@@ -168,7 +168,7 @@ def test_post_then_final_matches_oracle(n, d):
     free = orc.hc_post_then_final(delta, X, post, comb, pm, fw, FINAL_EPS)
     dd = gu.ulp_diff(gu.host_u16(z), free["z"])
     # without writing the streams: the same z, bit for bit
-    z2 = torch.empty_like(z)
+    z2 = gu.guarded(z.shape, z.dtype)
     hc.hc_post_then_final(*dev, n, s, None, z2)
     assert torch.equal(z, z2)
     print("n=%d d=%d X' bit-exact %.5f, z bit-exact %.5f, free-running z max ulp %d" % (n, d, ex_x, ex_z, int(dd.max())))
@@ -180,8 +180,8 @@ def test_post_then_final_prefill_b4_t4096():
                                                   ("comb", T_COMB), ("pre_mix", T_PREMIX))}
     fw = synth.final_norm_w(w)
     dev = {k: (gu.dev_bf16(v) if v.dtype == np.uint16 else gu.dev_f32(v)) for k, v in inp.items()}
-    Xo = torch.empty_like(dev["X"])
-    z = torch.empty((w.n, w.d), dtype=torch.bfloat16, device="cuda")
+    Xo = gu.guarded(dev["X"].shape, dev["X"].dtype)
+    z = gu.guarded((w.n, w.d), torch.bfloat16)
     hc.hc_post_then_final(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], gu.dev_f32(fw), w.n,
                           hc.shape(d=w.d, norm_eps=FINAL_EPS), Xo, z)
     idx = gu.sample_tokens(w.n, 384, np.random.default_rng(2))
@@ -217,8 +217,8 @@ def test_stack_from_embedding_to_final_norm():
         wd = prm["w_diag"]
     delta = (state["y"].float() * gu.dev_f32(wd)).to(torch.bfloat16)
     fw = synth.final_norm_w(w)
-    Xo = torch.empty_like(state["X"])
-    z = torch.empty((n, w.d), dtype=torch.bfloat16, device="cuda")
+    Xo = gu.guarded(state["X"].shape, state["X"].dtype)
+    z = gu.guarded((n, w.d), torch.bfloat16)
     hc.hc_post_then_final(delta, state["X"], state["post"], state["comb"], state["pre_mix"], gu.dev_f32(fw), n,
                           hc.shape(d=w.d, norm_eps=FINAL_EPS), Xo, z)
     xo = gu.host_u16(Xo)

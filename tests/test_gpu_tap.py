@@ -50,7 +50,7 @@ def test_tap_matches_oracle_and_plain_call(n, d):
     s = gu.shape_of(w)
     ref = gu.run_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, s, n)
     o = gu.alloc_outputs(n, d, True)
-    mean = torch.empty((n, d), dtype=torch.bfloat16, device="cuda")
+    mean = gu.guarded((n, d), torch.bfloat16)
     hc.hc_post_then_pre_tap(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P.c, n, s, o["X_out"],
                             o["y_normed"], o["pre"], o["post"], o["comb"], mean, gu.workspace())
     for k in ("X_out", "y_normed", "pre", "post", "comb"):
