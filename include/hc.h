@@ -97,11 +97,12 @@ int hc_prepare_params_size(int hc, int d, size_t* bytes);
 int hc_prepare_params(const float* hc_fn, int hc, int d, void* planes, hc_stream_t stream);
 
 /* Size in bytes of the workspace the fused calls (hc_pre_step, hc_post_then_pre,
- * hc_expand_pre_step, hc_debug_mixes) need: the 8 CTAs that share a token tile exchange their
- * per-token partial sums through it (about 14 KB per CTA per tile, L2-resident) together with one
- * 64-bit flag per CTA and tile parity, and one 64-bit launch counter per group of 8 CTAs that tags
- * the flags of each launch (kept on the device, so launches replayed from a CUDA graph are tagged
- * afresh too). The caller allocates it once [device], 16-byte aligned, fills it with zeros before
+ * hc_post_then_pre_tap, hc_expand_pre_step, hc_debug_mixes) need: the CTAs that share a token tile
+ * (8, 16 or 32 of them, as the launch plan of hc_plan_tiles chooses) exchange their per-token
+ * partial sums through it (about 14 KB per CTA per tile, L2-resident) together with one 64-bit flag
+ * per CTA and tile parity, and one 64-bit launch counter per group slot that tags the flags of each
+ * launch (kept on the device, so launches replayed from a CUDA graph are tagged afresh too). It has
+ * room for 256 co-resident CTAs: 7,356,672 bytes. The caller allocates it once [device], 16-byte aligned, fills it with zeros before
  * its first use and then keeps passing it unchanged (no re-zeroing needed). Calls that may run at
  * the same time on the GPU must not share a workspace. Host-only, no CUDA call. */
 int hc_workspace_size(size_t* bytes);
