@@ -14,7 +14,9 @@ Under torchrun every rank runs its own batch (weak scaling, no data-path collect
 `--op` times another entry point on the same batch, against its own algorithmic bytes:
 post_then_pre (the default step), pre_step, expand_pre_step (head of the stack), post_then_final
 and final (tail of the stack, eps 1e-20), post (writing half alone), decode_chain (80 sublayers on 256
-tokens captured in one CUDA graph).
+tokens captured in one CUDA graph); or the step on the other single-step workloads: step_b1_t64 (one
+hc_post_then_pre on 64 tokens, each launch timed alone with L2 flushed before it: latency) and
+long_prefill_b1_t65536 (one hc_post_then_pre on 65,536 tokens).
 """
 
 from __future__ import annotations
@@ -33,6 +35,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "HC step tokens/s and achieved HBM GB/s vs peak, prefill B=4 T=4096"
 WORKLOAD = "prefill_b4_t4096"
+SPEC_HBM_GBS = 8000.0         # GB300 HBM3e, nominal
 BYTES_PER_TOKEN = 102592      # read X 40960 + delta 10240 + post 16 + comb 64 + pre_mix 16;
                               # write X' 40960 + y_normed 10240 + pre/post/comb 96
 PARAM_BYTES = 1986668         # hc_fn fp32 1966080 + norm_w 20480 + hc_base 96 + hc_scale 12
@@ -41,8 +44,10 @@ CSRC = "hyper_connection_residual_hc_gb300/csrc/"
 FUSED_SOURCES = [CSRC + "hc_fused.cu", CSRC + "hc_ptx.cuh"]
 FINAL_SOURCES = [CSRC + "hc_final.cu"]
 
-# Per entry point: algorithmic bytes per token and per call (parameters), the kernel it launches,
-# the sources that kernel is built from, and the ncu traffic summary of that kernel on this workload.
+# Per op: algorithmic bytes per token and per call (parameters), the kernel it launches, the sources
+# that kernel is built from, and the ncu summary of that kernel on this workload; `call` is the entry
+# point (default: the op's own name), `workload` the synthetic workload (default: the prefill batch),
+# `flush_l2` times each launch alone after writing a buffer larger than L2.
 OPS = {
     "post_then_pre": dict(bytes_per_token=BYTES_PER_TOKEN, param_bytes=PARAM_BYTES, kernel="hc_fused_kernel<1>",
                           sources=FUSED_SOURCES, traffic="hc_fused_prefill_b4_t4096_traffic.json"),
@@ -65,12 +70,44 @@ OPS = {
     # read X 40960 + delta 10240 + post 16 + comb 64; write X' 40960
     "post": dict(bytes_per_token=92240, param_bytes=0, kernel="hc_post_kernel", sources=[CSRC + "hc_api.cu"],
                  traffic="hc_post_prefill_b4_t4096_traffic.json"),
+    # the step on the single-step workload of 64 tokens: a latency (each launch alone, L2 flushed)
+    "step_b1_t64": dict(bytes_per_token=BYTES_PER_TOKEN, param_bytes=PARAM_BYTES, kernel="hc_fused_kernel<1>",
+                        sources=FUSED_SOURCES, traffic=None, call="post_then_pre", workload="step_b1_t64",
+                        flush_l2=True),
+    # the step on the long-prefill workload's 65,536 tokens (its first step)
+    "long_prefill_b1_t65536": dict(bytes_per_token=BYTES_PER_TOKEN, param_bytes=PARAM_BYTES,
+                                   kernel="hc_fused_kernel<1>", sources=FUSED_SOURCES, traffic=None,
+                                   call="post_then_pre", workload="long_prefill_b1_t65536_4steps"),
 }
+
+
+def _call(op):
+    return OPS[op].get("call", op)
+
+
+def _workload_name(op):
+    return OPS[op].get("workload", WORKLOAD)
+
+
+def workload_config(w, op):
+    """The `config` of a bench line: the workload and the call, nothing measured, so that both arms
+    print the same dict."""
+    spec = OPS[op]
+    alg = w.n * spec["bytes_per_token"] + spec["param_bytes"]
+    l2 = ("flushed before every launch (a 256 MB write); each launch timed alone" if spec.get("flush_l2") else
+          "no flush: every step moves %d MB, far above the 129 MB L2" % (alg // 10 ** 6))
+    return {"workload": w.name, "entry_point": "hc_" + _call(op), "tokens_per_gpu": w.n, "B": w.B, "T": w.T,
+            "hc": w.hc, "d": w.d, "sinkhorn_iters": w.iters, "hc_eps": w.hc_eps, "norm_eps": w.norm_eps,
+            "stream_dtype": "bf16", "coefficient_dtype": "f32", "l2": l2}
 
 
 def _metric(op):
     if op == "post_then_pre":
         return METRIC
+    if op == "step_b1_t64":
+        return "HC step latency and tokens/s, single step B=1 T=64"
+    if op == "long_prefill_b1_t65536":
+        return "HC step tokens/s and achieved HBM GB/s vs peak, long prefill B=1 T=65536"
     return "HC %s tokens/s and achieved HBM GB/s vs peak, prefill B=4 T=4096" % op
 
 
@@ -121,16 +158,27 @@ def _source_hash(sources=FUSED_SOURCES):
     return h.hexdigest()[:16]
 
 
-def _traffic_per_launch(n_tokens, op="post_then_pre"):
-    """DRAM bytes per launch of the op's kernel from the committed ncu summary, scaled to this
-    launch's token count; None when absent or taken on another version of the kernel."""
+def _profile(op="post_then_pre"):
+    """The committed ncu summary of the op's kernel on its workload (DRAM bytes of one launch, and pipe
+    utilisations where captured); None when absent or taken on another version of the kernel."""
     spec = OPS[op]
+    if not spec.get("traffic"):
+        return None
     try:
         with open(os.path.join(ROOT, "profiles", spec["traffic"])) as f:
             t = json.load(f)
     except Exception:
         return None
     if t.get("source_sha256_16") != _source_hash(spec["sources"]):
+        return None
+    return t
+
+
+def _traffic_per_launch(n_tokens, op="post_then_pre"):
+    """DRAM bytes per launch of the op's kernel from the committed ncu summary, scaled to this
+    launch's token count; None when absent or taken on another version of the kernel."""
+    t = _profile(op)
+    if t is None:
         return None
     return float(t["dram_bytes_per_launch"]) * n_tokens / float(t["tokens"])
 
@@ -194,6 +242,7 @@ def _oracle_call(w, tokens, threads, op="post_then_pre"):
         return synth.tokens(w, t, 0, 0, tokens)
 
     coef = (prm["hc_fn"], prm["hc_scale"], prm["hc_base"], prm["norm_w"], w.iters, w.hc_eps, w.norm_eps)
+    op = _call(op) if op in OPS else op
     if op in ("post_then_pre", "post_then_pre_tap"):
         args = (tk(T_DELTA), tk(T_X), tk(T_POST), tk(T_COMB), tk(T_PREMIX))
         if op == "post_then_pre":
@@ -235,15 +284,19 @@ def run_reference(args):
         return
     import oracle as orc
     from hyper_connection_residual_hc_gb300 import synth
-    wname, op, unit, metric = WORKLOAD, args.op, "tokens/s", _metric(args.op)
+    op, unit, metric = args.op, "tokens/s", _metric(args.op)
     if args.op == "decode_chain":  # the chain's sublayer steps, one hc_post_then_pre per sublayer
         wname, op, unit = DECODE, "post_then_pre", "sublayer-tokens/s"
-        metric = "HC decode chain sublayer-tokens/s (80 sublayers x 256 tokens, one CUDA graph)"
+        metric = DECODE_METRIC
+        config = decode_config(synth.WORKLOADS[DECODE])
+    else:
+        wname = _workload_name(op)
+        config = workload_config(synth.WORKLOADS[wname], op)
     w = synth.WORKLOADS[wname]
     threads = orc.hardware_threads()
     # size each step so that warmup + steps take about two minutes at most
-    rate = _oracle_sample_rate(w, 4 * threads, threads, op)
-    per_step = max(threads, min(w.n, int(rate * 120.0 / max(1, args.steps + args.warmup))))
+    rate = _oracle_sample_rate(w, min(w.n, 4 * threads), threads, op)
+    per_step = min(w.n, max(threads, int(rate * 120.0 / max(1, args.steps + args.warmup))))
     fn = _oracle_call(w, per_step, threads, op)  # the same sample every step, drawn once
     for _ in range(args.warmup):
         fn()
@@ -252,12 +305,12 @@ def run_reference(args):
         fn()
     el = time.perf_counter() - t0
     value = per_step * args.steps / el
-    sample = "first %d of the %d tokens of %s per step (hc_%s, float64 oracle)" % (per_step, w.n, wname, op)
+    sample = "first %d of the %d tokens of %s per step (hc_%s, float64 oracle)" % (per_step, w.n, wname,
+                                                                                    _call(op) if op in OPS else op)
     line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wname, "entry_point": "hc_" + op, "tokens": w.n, "hc": w.hc, "d": w.d,
-                       "sinkhorn_iters": w.iters},
+            "config": config,
             "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -274,6 +327,7 @@ def run_ours(args):
 
     op = args.op
     spec = OPS[op]
+    call = _call(op)
     rank, world, local = _dist()
     torch.cuda.set_device(local)
     dist = None
@@ -282,7 +336,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     hc.load()
 
-    w = rank_workload(synth.WORKLOADS[WORKLOAD], rank)
+    w = rank_workload(synth.WORKLOADS[_workload_name(op)], rank)
     n, d = w.n, w.d
     prm = synth.params(w, 0)
 
@@ -296,7 +350,7 @@ def run_ours(args):
     names = {"post_then_pre": ("delta", "X", "post", "comb", "pre_mix"), "pre_step": ("X", "pre_mix"),
              "post_then_pre_tap": ("delta", "X", "post", "comb", "pre_mix"),
              "expand_pre_step": ("h",), "post_then_final": ("delta", "X", "post", "comb", "pre_mix"),
-             "final": ("X", "pre_mix"), "post": ("delta", "X", "post", "comb")}[op]
+             "final": ("X", "pre_mix"), "post": ("delta", "X", "post", "comb")}[call]
     draw = dict(delta=lambda: bf(synth.tokens(w, T_DELTA, 0)), X=lambda: bf(synth.tokens(w, T_X, 0)),
                 post=lambda: f32(synth.tokens(w, T_POST, 0)), comb=lambda: f32(synth.tokens(w, T_COMB, 0)),
                 pre_mix=lambda: f32(synth.tokens(w, T_PREMIX, 0)), h=lambda: bf(synth.tokens(w, T_EMBED, 0)))
@@ -316,13 +370,13 @@ def run_ours(args):
 
     coef = lambda: dict(pre=empty(n, 4, dt=torch.float32), post=empty(n, 4, dt=torch.float32),  # noqa: E731
                         comb=empty(n, 4, 4, dt=torch.float32))
-    if op in ("post_then_pre", "expand_pre_step"):
+    if call in ("post_then_pre", "expand_pre_step"):
         out = dict(X_out=empty(n, 4, d), y_normed=empty(n, d), **coef())
-    elif op == "post_then_pre_tap":
+    elif call == "post_then_pre_tap":
         out = dict(X_out=empty(n, 4, d), y_normed=empty(n, d), stream_mean=empty(n, d), **coef())
-    elif op == "pre_step":
+    elif call == "pre_step":
         out = dict(y_normed=empty(n, d), **coef())
-    elif op in ("post_then_final", "final"):
+    elif call in ("post_then_final", "final"):
         out = dict(z=empty(n, d))
     else:
         out = dict(X_out=empty(n, 4, d))
@@ -330,23 +384,23 @@ def run_ours(args):
     ws = hc.new_workspace()
 
     def step():
-        if op == "post_then_pre":
+        if call == "post_then_pre":
             hc.hc_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, n, s,
                                 out["X_out"], out["y_normed"], out["pre"], out["post"], out["comb"], ws, stream)
-        elif op == "post_then_pre_tap":
+        elif call == "post_then_pre_tap":
             hc.hc_post_then_pre_tap(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, n, s,
                                     out["X_out"], out["y_normed"], out["pre"], out["post"], out["comb"],
                                     out["stream_mean"], ws, stream)
-        elif op == "pre_step":
+        elif call == "pre_step":
             hc.hc_pre_step(dev["X"], dev["pre_mix"], P, n, s, out["y_normed"], out["pre"], out["post"], out["comb"],
                            ws, stream)
-        elif op == "expand_pre_step":
+        elif call == "expand_pre_step":
             hc.hc_expand_pre_step(dev["h"], P, n, s, out["X_out"], out["y_normed"], out["pre"], out["post"],
                                   out["comb"], ws, stream)
-        elif op == "post_then_final":
+        elif call == "post_then_final":
             hc.hc_post_then_final(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], fw, n, sf, None,
                                   out["z"], stream)
-        elif op == "final":
+        elif call == "final":
             hc.hc_final(dev["X"], dev["pre_mix"], fw, n, sf, out["z"], stream)
         else:
             hc.hc_post(dev["delta"], dev["X"], dev["post"], dev["comb"], n, s, out["X_out"], stream)
@@ -362,7 +416,10 @@ def run_ours(args):
     barrier()
     werr = hc.hc_device_error(clear=True)
 
-    # timed region: one fused launch per step, CUDA events on the launching stream around each launch
+    # timed region: one fused launch per step, CUDA events on the launching stream around each launch;
+    # with flush_l2, a 256 MB write before every launch (outside its events), and the steps' time is
+    # the sum of the launches' own times
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if spec.get("flush_l2") else None
     clocks = ClockSampler(local)
     clocks.start()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -371,14 +428,17 @@ def run_ours(args):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
     t_end.record(stream)
     barrier()
     clk = clocks.stop()
-    el_ms = t_start.elapsed_time(t_end)
-    kern_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    per_launch = sorted(a.elapsed_time(b) for a, b in ev)
+    kern_ms = sum(per_launch) / args.steps
+    el_ms = sum(per_launch) if flush is not None else t_start.elapsed_time(t_end)
     el_ms = max_over_ranks(el_ms, dist, "cuda")
     derr = hc.hc_device_error(clear=True)
 
@@ -390,7 +450,7 @@ def run_ours(args):
     d2h = sum(v.numel() * v.element_size() for v in pin_out.values())
 
     pipe = None
-    if op == "post_then_pre":
+    if call == "post_then_pre":
         # the library's host-buffer executor: chunks of tokens copied in, stepped and copied out on
         # overlapping streams, all behind one C-ABI call on host arrays
         pipe = hc.HostPipeline(4, d, args.e2e_chunk)
@@ -427,34 +487,39 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     alg_bytes = n * spec["bytes_per_token"] + spec["param_bytes"]
     achieved = alg_bytes / (kern_ms / 1e3) / 1e9
+    med_ms = statistics.median(per_launch)
     ctas = hc.hc_fused_ctas()
     group, tile_m, tiles = hc.hc_plan_tiles(n, d, ctas)
+    prof = _profile(op)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle as orc
         threads = orc.hardware_threads()
-        r0 = _oracle_sample_rate(w, 2 * threads, threads, op)
+        r0 = _oracle_sample_rate(w, min(n, 2 * threads), threads, op)
         sample_tokens = int(max(threads, min(n, r0 * 15.0)))  # about 15 s of wall time at most
         rate = _oracle_sample_rate(w, sample_tokens, threads, op)
         cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": "hc_%s on the first %d of the %d tokens of %s, float64 oracle, %d threads"
-                         % (op, sample_tokens, n, WORKLOAD, threads)}
+                         % (call, sample_tokens, n, w.name, threads)}
 
     if rank == 0:
         line = {
             "metric": _metric(op), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": el_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "entry_point": "hc_" + op, "tokens_per_gpu": n, "B": w.B, "T": w.T, "hc": w.hc, "d": d,
-                       "sinkhorn_iters": w.iters, "hc_eps": w.hc_eps, "norm_eps": w.norm_eps,
-                       "stream_dtype": "bf16", "coefficient_dtype": "f32",
-                       "l2": "no flush: every step moves %d MB, far above the 129 MB L2" % (alg_bytes // 10 ** 6),
-                       "tile_tokens": tile_m, "tiles": tiles, "ctas_per_tile": group, "resident_ctas": ctas,
-                       "hbm_gb_per_s": alg_bytes * args.steps / (el_ms / 1e3) / 1e9},
+            "config": workload_config(w, op),
+            "plan": {"tile_tokens": tile_m, "tiles": tiles, "ctas_per_tile": group, "resident_ctas": ctas},
+            "latency_us": {"median": 1e3 * med_ms, "best": 1e3 * per_launch[0], "mean": 1e3 * kern_ms,
+                           "launches": args.steps},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
+                         "frac_spec": achieved / SPEC_HBM_GBS, "spec_peak": SPEC_HBM_GBS,
+                         "achieved_median": alg_bytes / (med_ms / 1e3) / 1e9,
+                         "achieved_best": alg_bytes / (per_launch[0] / 1e3) / 1e9,
+                         "region_gb_per_s": alg_bytes * args.steps / (el_ms / 1e3) / 1e9,
                          "traffic": _traffic_per_launch(n, op), "algorithmic_bytes": alg_bytes,
+                         "pipes": prof.get("pipes") if prof else None,
                          "kernel": spec["kernel"], "kernel_ms": kern_ms},
             "cpu_baseline": cpu,
             "e2e": {"value": whole_job_rate(n * e2e_steps, world, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -471,6 +536,16 @@ def run_ours(args):
 
 
 DECODE = "decode_chain_b256_80steps"
+DECODE_METRIC = "HC decode chain sublayer-tokens/s (80 sublayers x 256 tokens, one CUDA graph)"
+
+
+def decode_config(w):
+    """The decode chain's `config`, the same in both arms."""
+    return {"workload": w.name, "entry_point": "graph of hc_expand_pre_step, 79 x hc_post_then_pre, "
+            "hc_post_then_final", "tokens_per_gpu": w.n, "sublayers": w.steps, "hc": w.hc, "d": w.d,
+            "sinkhorn_iters": w.iters, "hc_eps": w.hc_eps, "norm_eps": w.norm_eps, "final_norm_eps": FINAL_EPS,
+            "l2": "no flush: the 80 parameter sets (236 MB of weight planes) exceed the 129 MB L2, the 10 MB of "
+                  "streams stay resident between sublayers as in a real decode step"}
 
 
 def run_decode_chain(args):
@@ -557,12 +632,16 @@ def run_decode_chain(args):
         dist.barrier()
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     t0.record(stream)
-    for _ in range(steps):
+    marks[0].record(stream)
+    for i in range(steps):
         graph.replay()
+        marks[i + 1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
+    chain_samples = [marks[i].elapsed_time(marks[i + 1]) for i in range(steps)]
     el_ms = max_over_ranks(t0.elapsed_time(t1), dist, "cuda")
     derr = hc.hc_device_error(clear=True)
 
@@ -602,19 +681,18 @@ def run_decode_chain(args):
                "sample": "8 sublayer steps (hc_post_then_pre) on %d of the %d tokens, float64 oracle" % (k, n)}
     if rank == 0:
         line = {
-            "metric": "HC decode chain sublayer-tokens/s (80 sublayers x 256 tokens, one CUDA graph)",
+            "metric": DECODE_METRIC,
             "value": sub_tokens / (chain_ms / 1e3), "unit": "sublayer-tokens/s", "n_gpus": world, "steps": steps,
             "warmup": max(3, args.warmup), "ms_per_step": chain_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": DECODE, "entry_point": "graph of hc_expand_pre_step, 79 x hc_post_then_pre, "
-                       "hc_post_then_final", "tokens_per_gpu": n, "sublayers": L, "hc": 4, "d": d,
-                       "us_per_sublayer": chain_ms * 1e3 / L,
-                       "plan": dict(zip(("ctas_per_tile", "tile_tokens", "tiles"),
-                                        hc.hc_plan_tiles(n, d, hc.hc_fused_ctas()))),
-                       "l2": "no flush: the 80 parameter sets (236 MB of weight planes) exceed the 129 MB L2, "
-                             "the 10 MB of streams stay resident between sublayers as in a real decode step"},
+            "config": decode_config(w),
+            "plan": dict(zip(("ctas_per_tile", "tile_tokens", "tiles"), hc.hc_plan_tiles(n, d, hc.hc_fused_ctas()))),
+            "latency_us": {"per_sublayer": chain_ms * 1e3 / L, "per_chain": chain_ms * 1e3,
+                           "per_sublayer_median": 1e3 * statistics.median(chain_samples) / L,
+                           "per_sublayer_best": 1e3 * min(chain_samples) / L, "chains": len(chain_samples)},
             "roofline": {"bound": "latency (launch chain)", "achieved": alg / (chain_ms / 1e3) / 1e9, "peak": peak,
                          "unit": "GB/s", "frac": alg / (chain_ms / 1e3) / 1e9 / peak, "peak_kind": peak_kind,
+                         "frac_spec": alg / (chain_ms / 1e3) / 1e9 / SPEC_HBM_GBS, "spec_peak": SPEC_HBM_GBS,
                          "traffic": None, "algorithmic_bytes": alg},
             "cpu_baseline": cpu,
             "e2e": {"value": sub_tokens * e2e_steps / e2e_s, "unit": "sublayer-tokens/s",

@@ -222,11 +222,10 @@ static int post_then_pre_impl(const void* delta, const void* X, const float* pos
     if (any_overlap(outs, osz, 7, ins, isz, 5)) return HC_ERR_ALIAS;
     if (n == 0) return HC_OK;
     if (noalloc) {
-        // the scratch is the library's fixed array: find this device's copy (first call only) and make
-        // sure the launch needs no more of it than it holds
+        // the scratch is the library's fixed array: find this device's copy (first call only); it is
+        // as large as any launch needs (a compile-time check beside the array)
         size_t capacity = 0;
         if (noalloc_workspace(&workspace, &capacity) != 0) return HC_ERR_CUDA;
-        if (workspace_bytes() > capacity) return HC_ERR_UNSUPPORTED;
     }
     const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     if (!fused_shape(s)) {

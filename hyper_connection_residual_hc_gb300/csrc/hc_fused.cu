@@ -1163,6 +1163,12 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
 // GPU that loads the library, zero at load and kept until the process exits. Its size is the same
 // kWorkspaceBytes (7,356,672 bytes: room for 256 co-resident CTAs) that hc_workspace_size reports.
 static __device__ __align__(256) unsigned char g_noalloc_workspace[kWorkspaceBytes];
+// A launch never needs more scratch than this: the fused kernel runs at most kMaxCtas CTAs (the
+// device's resident count is capped there) and the generic path works through its tokens in chunks
+// sized to kWorkspaceBytes, so no call is ever refused for want of room in the array.
+static_assert(sizeof(g_noalloc_workspace) >= kWorkspaceBytes && kWorkspaceBytes >= kWsPartBytes &&
+                  kWsPartBytes == static_cast<size_t>(kMaxCtas) * 2 * kPartFloats * 4,
+              "the fixed scratch holds the partial sums of kMaxCtas CTAs, their flags and counters");
 
 namespace {
 void* g_noalloc_ptr[kMaxDevices] = {};
@@ -1200,6 +1206,20 @@ int read_device_error(unsigned int* word, int clear, cudaStream_t stream) {
         const unsigned int z = 0;
         if (cudaMemcpyToSymbolAsync(g_hc_error, &z, sizeof(z), 0, cudaMemcpyHostToDevice, stream) != cudaSuccess)
             return -7;
+        if (v != 0) {
+            // A kernel gave up a wait: a CTA of its group that had not yet read the group's launch
+            // counter when the counter advanced would tag its flags like the group's next launch. The
+            // library's fixed scratch (hc_post_then_pre_noalloc) therefore starts afresh from zero; a
+            // memset is not an allocation. Caller workspaces are the caller's to zero (hc.h).
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -7;
+            void* scratch = nullptr;
+            {
+                std::lock_guard<std::mutex> lk(g_noalloc_mu);
+                scratch = g_noalloc_ptr[dev];
+            }
+            if (scratch && cudaMemsetAsync(scratch, 0, sizeof(g_noalloc_workspace), stream) != cudaSuccess) return -7;
+        }
         if (cudaStreamSynchronize(stream) != cudaSuccess) return -7;
     }
     *word = v;

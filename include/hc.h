@@ -104,7 +104,10 @@ int hc_prepare_params(const float* hc_fn, int hc, int d, void* planes, hc_stream
  * launch (kept on the device, so launches replayed from a CUDA graph are tagged afresh too). It has
  * room for 256 co-resident CTAs: 7,356,672 bytes. The caller allocates it once [device], 16-byte aligned, fills it with zeros before
  * its first use and then keeps passing it unchanged (no re-zeroing needed). Calls that may run at
- * the same time on the GPU must not share a workspace. Host-only, no CUDA call. */
+ * the same time on the GPU must not share a workspace. One exception to "no re-zeroing": after a
+ * kernel gave up a bounded wait (HC_ERR_DEVICE, a nonzero hc_device_error word), a CTA that started
+ * late may have tagged its flags like the next launch; zero the workspace again before reusing it.
+ * Host-only, no CUDA call. */
 int hc_workspace_size(size_t* bytes);
 
 /* Reading half of one sublayer ("Source layer, pairs pooled" page, Block.forward excerpt, the
@@ -162,12 +165,17 @@ int hc_post_then_pre_tap(const void* delta, const void* X, const float* post, co
  * exits. It allocates nothing and calls no allocating routine.
  *   - The first call on a device looks up that device's copy of the array (a runtime query, no
  *     allocation); make that first call before any stream capture.
- *   - A launch that would need more scratch than the array holds is refused with
- *     HC_ERR_UNSUPPORTED (not possible on GPUs with up to 256 SMs).
+ *   - No call needs more scratch than the array holds: the library launches at most 256 CTAs
+ *     whatever the GPU, and the shapes outside the fused kernel work through their tokens in
+ *     chunks that fit. Sizes are refused only as for hc_post_then_pre (n above 2^31 - 1:
+ *     HC_ERR_SHAPE; hc > 8 or d > 65536: HC_ERR_UNSUPPORTED).
  *   - All calls share the one array. It needs no clearing between calls: it is zero at load and
  *     every call tags its exchange flags with a new launch number. But two calls whose kernels
  *     could run at the same time on the GPU (other streams, other threads) race on it and produce
  *     wrong results; serialise them, or use hc_post_then_pre with separate workspaces.
+ *   - After a kernel gave up a bounded wait (HC_ERR_DEVICE, a nonzero hc_device_error word), the
+ *     array's flags may hold stale tags: hc_device_error with `clear` zeroes the array of the
+ *     current device too, so the next call starts afresh.
  * The pages have no counterpart to this call: it is a packaging of hc_post_then_pre only. */
 int hc_post_then_pre_noalloc(const void* delta, const void* X, const float* post, const float* comb,
                              const float* pre_mix, hc_params_t next, int64_t n, hc_shape_t s,
@@ -318,7 +326,9 @@ int hc_debug_wait_flag(const unsigned long long* flags, int count, unsigned long
 
 /* Read the device-side error word of the current device: nonzero when a kernel gave up a
  * bounded wait (it then returned early and its outputs are not valid). Synchronises `stream`.
- * If `clear` is nonzero the word is reset to 0. Returns HC_OK, HC_ERR_NULL or HC_ERR_CUDA. */
+ * If `clear` is nonzero the word is reset to 0, and, when it was nonzero, the library's own fixed
+ * scratch of hc_post_then_pre_noalloc on this device is zeroed as well (on `stream`; no call using it
+ * may still be running). Returns HC_OK, HC_ERR_NULL or HC_ERR_CUDA. */
 int hc_device_error(unsigned int* word, int clear, hc_stream_t stream);
 
 /* Static description of a status code (never NULL). */

@@ -12,16 +12,18 @@ Tolerances (stated once, used everywhere):
     99.9% of the values within 1 ulp of the oracle's rounding.
   mixes: |gpu - oracle| <= max(1e-5 |m|, 1e-6) + 2 u S, with u = 2^-24 and S = r sum_c |x_c w_mc|:
     a 20,480-term dot product accumulated in fp32 is off by a few u S whatever the order.
-  pre/post/comb given the GPU's own mixes (stage isolated): rel 1e-5 or abs 1e-6; for comb plus the
-    first-order error of an fp32 evaluation of the Sinkhorn iteration, 2 iters normalisations of
-    (hc + 2) u each ((hc - 1) additions, + eps, reciprocal, product), 2 iters (hc + 2) u |comb|: the
-    model runs hc_split_sinkhorn in fp32, and at 50 rounds on near-one-hot rows a faithful fp32
-    evaluation lands up to ~1e-5 from the exact value.
-  pre/post/comb end to end: the same, plus the mixes bound pushed through the split: pre and post
-    through the sigmoid's slope, comb through the oracle split's sensitivities (central differences).
+  pre/post/comb given the GPU's own mixes (stage isolated): rel 1e-5 or abs 1e-6, flat, for every
+    Sinkhorn round count. The model runs hc_split_sinkhorn in fp32; an IEEE fp32 evaluation of the
+    page's steps meets this even at the stress workload's 50 rounds on extreme logits, with less
+    margin than at 20 (tests/test_split_fp32.py).
+  pre/post/comb end to end: the flat tolerance plus the mixes bound pushed through the split: pre and
+    post through the sigmoid's slope, comb through the oracle split's sensitivities (central
+    differences). The elements beyond the flat tolerance are counted and reported (COEF_STATS).
 """
 
 from __future__ import annotations
+
+import collections
 
 import numpy as np
 import torch
@@ -242,18 +244,39 @@ def assert_mixes_close(m_gpu, m_ref, S, what="mixes"):
 
 
 def sinkhorn_fp32_bound(comb_ref, hcn, iters):
-    """First-order error of an fp32 evaluation of the split's Sinkhorn iteration."""
+    """First-order error of an fp32 evaluation of the split's Sinkhorn iteration: 2 iters normalisations
+    of (hc + 2) u each ((hc - 1) additions, + eps, the division). Not a tolerance of the GPU checks; the
+    fp32 evidence test (test_split_fp32) shows an IEEE evaluation stays inside it."""
     return 2 * iters * (hcn + 2) * U * np.abs(comb_ref)
 
 
-def assert_coef_close(gpu, ref, what, extra=None):
-    tol = np.maximum(1e-5 * np.abs(ref), 1e-6)
-    if extra is not None:
-        tol = tol + extra
+# per check kind (e.g. "comb (isolated)"): [elements, beyond the flat tolerance, worst err / flat]
+COEF_STATS = collections.defaultdict(lambda: [0, 0, 0.0])
+
+
+def coef_stats_report(reset=True):
+    """One line per check kind: how many coefficients needed more than the flat rel 1e-5 / abs 1e-6."""
+    lines = ["%-26s %9d elements, %6d beyond flat (%.2e), worst err/flat %.3f"
+             % (k, v[0], v[1], v[1] / max(v[0], 1), v[2]) for k, v in sorted(COEF_STATS.items())]
+    if reset:
+        COEF_STATS.clear()
+    return "\n".join(lines)
+
+
+def assert_coef_close(gpu, ref, what, extra=None, kind=None):
+    """|gpu - ref| <= max(1e-5 |ref|, 1e-6) + extra; the elements beyond the flat part are counted
+    under `kind` in COEF_STATS."""
+    flat = np.maximum(1e-5 * np.abs(ref), 1e-6)
     err = np.abs(gpu - ref)
+    tol = flat if extra is None else flat + extra
     bad = err > tol
     assert not bad.any(), "%s: %d beyond tolerance, worst err %.3g (tol %.3g)" % (
         what, int(bad.sum()), float(err[bad].max()), float(tol[bad][np.argmax(err[bad])]))
+    if kind is not None:
+        st = COEF_STATS[kind]
+        st[0] += err.size
+        st[1] += int((err > flat).sum())
+        st[2] = max(st[2], float((err / flat).max()) if err.size else 0.0)
 
 
 def hc_of(M):
@@ -293,13 +316,13 @@ def check_step(out, ref, m_gpu, m_ref, S, prm, iters, eps, label):
     assert_mixes_close(m_gpu, m_ref, S, label + " mixes")
     h_ = hc_of(m_gpu.shape[1])
     pre_i, post_i, comb_i = orc.split_sinkhorn(m_gpu, prm["hc_scale"], prm["hc_base"], h_, iters, eps)
-    assert_coef_close(pre_g, pre_i, label + " pre (isolated)")
-    assert_coef_close(post_g, post_i, label + " post (isolated)")
-    assert_coef_close(comb_g, comb_i, label + " comb (isolated)", sinkhorn_fp32_bound(comb_i, h_, iters))
+    assert_coef_close(pre_g, pre_i, label + " pre (isolated)", kind="pre (isolated)")
+    assert_coef_close(post_g, post_i, label + " post (isolated)", kind="post (isolated)")
+    assert_coef_close(comb_g, comb_i, label + " comb (isolated)", kind="comb (isolated)")
     bp, bq, bc = split_sensitivity_bound(m_ref, S, prm["hc_scale"], prm["hc_base"], iters, eps)
-    assert_coef_close(pre_g, ref["pre"], label + " pre", bp)
-    assert_coef_close(post_g, ref["post"], label + " post", bq)
-    assert_coef_close(comb_g, ref["comb"], label + " comb", bc + sinkhorn_fp32_bound(ref["comb"], h_, iters))
+    assert_coef_close(pre_g, ref["pre"], label + " pre", bp, kind="pre (end to end)")
+    assert_coef_close(post_g, ref["post"], label + " post", bq, kind="post (end to end)")
+    assert_coef_close(comb_g, ref["comb"], label + " comb", bc, kind="comb (end to end)")
 
 
 # ---- sampled checks of a full-size step -----------------------------------------------------------

@@ -256,7 +256,12 @@ def test_zero_tokens_is_a_noop():
 
 # ---- the five workloads ------------------------------------------------------------------------------
 
+def _report(name):
+    print("%s: coefficients beyond the flat rel 1e-5 / abs 1e-6\n%s" % (name, gu.coef_stats_report()))
+
+
 def test_workload_step_b1_t64():
+    gu.COEF_STATS.clear()
     w = synth.WORKLOADS["step_b1_t64"]
     inp = _inputs(w)
     prm = synth.params(w, 0)
@@ -265,9 +270,11 @@ def test_workload_step_b1_t64():
     out = gu.run_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, _shape(w), w.n)
     gu.check_sampled(w, 0, dev, out, prm, np.arange(w.n), True, "step_b1_t64")
     gu.device_error_clear()
+    _report(w.name)
 
 
 def test_workload_prefill_b4_t4096():
+    gu.COEF_STATS.clear()
     w = synth.WORKLOADS["prefill_b4_t4096"]
     inp = _inputs(w)
     prm = synth.params(w, 0)
@@ -283,10 +290,39 @@ def test_workload_prefill_b4_t4096():
     pre = out["pre"]
     assert float(pre.min()) >= 1e-6 * 0.999 and float(pre.max()) <= 1 + 2e-6
     gu.device_error_clear()
+    _report(w.name)
+
+
+def _extreme_tokens(X_in, out, P, s, n, k=8):
+    """Tokens at the extremes of one step, picked on the device: the largest |X| among the streams read
+    and among those written, the largest |comb logit| (s2 * mix + base, from the GPU's own mixes of
+    every token), the most nearly one-hot comb (largest sum of row maxima), and tokens whose pre or
+    post saturated in fp32 (pre = 1 + eps, post = 2 or 0)."""
+    picks = []
+
+    def top(v):
+        picks.append(torch.topk(v, min(k, n)).indices)
+
+    top(X_in.float().abs().amax(dim=(1, 2)))
+    if "X_out" in out:
+        top(out["X_out"].float().abs().amax(dim=(1, 2)))
+    m = gu.debug_mixes(out["X_out"] if "X_out" in out else X_in, P, s, n, gu.plan_group(n, s))
+    logits = m[:, 2 * s.hc:] * P.hc_scale[2] + P.hc_base[2 * s.hc:]
+    top(logits.abs().amax(dim=1))
+    top(out["comb"].amax(dim=2).sum(dim=1))
+    sat = ((out["pre"] == float(np.float32(1.0 + s.hc_eps))).any(dim=1) | (out["post"] == 2.0).any(dim=1) |
+           (out["post"] == 0.0).any(dim=1)).nonzero().flatten()
+    picks.append(sat[:k])
+    return set(torch.cat(picks).cpu().numpy().tolist())
+
+
+def _with_extremes(idx, X_in, out, P, s, n):
+    return np.array(sorted(set(idx.tolist()) | _extreme_tokens(X_in, out, P, s, n)), dtype=np.int64)
 
 
 def _run_chain(w, sample_k, first_pre_step, fresh_delta):
-    """Steps: [hc_pre_step], then hc_post_then_pre ... ; every step checked teacher-forced on a sample."""
+    """Steps: [hc_pre_step], then hc_post_then_pre ... ; every step checked teacher-forced on a sample:
+    random tokens, the first and last, tile edges, and the step's extreme tokens (_extreme_tokens)."""
     rng = np.random.default_rng(w.seed)
     s = _shape(w)
     n = w.n
@@ -298,7 +334,7 @@ def _run_chain(w, sample_k, first_pre_step, fresh_delta):
         prm = synth.params(w, 0)
         P = gu.DevParams(prm, w.d)
         out = gu.run_pre_step(X, pre_mix, P, s, n)
-        idx = gu.sample_tokens(n, sample_k, rng)
+        idx = _with_extremes(gu.sample_tokens(n, sample_k, rng), X, out, P, s, n)
         gu.check_sampled(w, 0, dict(X=X, pre_mix=pre_mix), out, prm, idx, False, "%s step 0" % w.name)
         state = dict(X=X, post=out["post"], comb=out["comb"], pre_mix=out["pre"], y=out["y_normed"])
         start = 1
@@ -316,7 +352,7 @@ def _run_chain(w, sample_k, first_pre_step, fresh_delta):
         prm = synth.params(w, l)
         P = gu.DevParams(prm, w.d)
         out = gu.run_post_then_pre(delta, state["X"], state["post"], state["comb"], state["pre_mix"], P, s, n)
-        idx = gu.sample_tokens(n, sample_k, rng)
+        idx = _with_extremes(gu.sample_tokens(n, sample_k, rng), state["X"], out, P, s, n)
         dev_in = dict(X=state["X"], delta=delta, post=state["post"], comb=state["comb"], pre_mix=state["pre_mix"])
         gu.check_sampled(w, l, dev_in, out, prm, idx, True, "%s step %d" % (w.name, l))
         state = dict(X=out["X_out"], post=out["post"], comb=out["comb"], pre_mix=out["pre"], y=out["y_normed"])
@@ -327,6 +363,7 @@ def _run_chain(w, sample_k, first_pre_step, fresh_delta):
 
 
 def test_workload_decode_chain_b256_80steps():
+    gu.COEF_STATS.clear()
     w = synth.WORKLOADS["decode_chain_b256_80steps"]
     state, worst = _run_chain(w, 256, first_pre_step=True, fresh_delta=False)
     # the chain's tail: the last writing half alone
@@ -337,15 +374,20 @@ def test_workload_decode_chain_b256_80steps():
                     gu.host_f32(state["post"]).astype(np.float32), gu.host_f32(state["comb"]).astype(np.float32),
                     "decode chain tail")
     print("decode chain: max |X| after 80 steps %.3g" % worst)
+    _report(w.name)
 
 
 @pytest.mark.slow
 def test_workload_long_prefill_b1_t65536_4steps():
+    gu.COEF_STATS.clear()
     w = synth.WORKLOADS["long_prefill_b1_t65536_4steps"]
     _run_chain(w, 256, first_pre_step=False, fresh_delta=True)
+    _report(w.name)
 
 
 @pytest.mark.slow
 def test_workload_stress_b2_t8192_80steps():
+    gu.COEF_STATS.clear()
     w = synth.WORKLOADS["stress_b2_t8192_80steps"]
     _run_chain(w, 48, first_pre_step=True, fresh_delta=True)
+    _report(w.name)
