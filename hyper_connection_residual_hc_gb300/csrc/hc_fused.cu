@@ -17,35 +17,44 @@
 // collapses the four copies back to h exactly.
 //
 // Decomposition. A group of kG CTAs (8 for large batches; 16 or 32 for small ones, so that each CTA
-// has fewer column stages) owns a tile of up to 128 tokens; CTA `rank` of the group owns d/kG
-// columns of every stream, the 32-column chunks rank, rank+kG, rank+2kG, ... (interleaved, so the
-// group's loads of one stage cover kG*32 contiguous columns of each row). The 16 warps of a CTA
-// have fixed roles:
-//   producer (warp 8): per 32-column stage, TMA-loads the four X tiles [tokens x 32 cols] (expand
-//     mode: the one embedding tile), the Delta tile (post mode) and the four matching slices of
-//     the split projection weights (bf16 planes hi/mid/lo, 72 rows) into a ring of shared-memory
-//     slots, 64-byte swizzled: 3 slots in post mode, 4 in pre mode, 6 in expand mode;
-//   compute (warps 0-7, thread = token, two warps per TMEM lane quadrant, 16 columns each):
+// has fewer column stages) owns a tile of up to 128 tokens (groups of 16 and 32: up to 64); CTA
+// `rank` of the group owns d/kG columns of every stream, the 32-column chunks rank, rank+kG,
+// rank+2kG, ... (interleaved, so the group's loads of one stage cover kG*32 contiguous columns of
+// each row). Groups of 8 make one pass per 32-column stage. Groups of 16 and 32 fold their tiles:
+// a pass holds two column stages, the second in rows 64..127 of each tile, so that the 128-row MMA
+// and all compute warps do useful work on small batches. The 16 warps of a CTA have fixed roles:
+//   producer (warp 8): per pass, TMA-loads the four X tiles [tokens x 32 cols] (expand mode: the
+//     one embedding tile), the Delta tile (post mode) and the matching slices of the split
+//     projection weights (bf16 planes hi/mid/lo, 72 rows per stream and stage) into a ring of
+//     shared-memory slots, 64-byte swizzled: 3 slots in post mode, 4 in pre mode, 6 in expand mode
+//     (folded: 2, 2, 4); a folded pass of 64-token tiles takes one box per tensor. The first slots'
+//     loads are issued by thread 0 as soon as the kernel ahead on the stream has completed;
+//   compute (warps 0-7, thread = token row, two warps per TMEM lane quadrant, 16 columns each):
 //     compute X' in place (post mode; the other modes read the loaded tile), accumulate sum(X'^2),
-//     form and round y, accumulate sum(y^2), store the bf16 y chunk into a ring of 27 chunk slots
-//     in tensor memory, and drain the previous stage's accumulator into 12 per-thread fp32 sums
-//     (the three planes added back together);
-//   MMA (warp 9): one thread issues 8 tcgen05.mma per stage (M=128 tokens, N=80 >= 72 plane
-//     rows, K=16) projecting the bf16 X' tile on the three planes into a TMEM accumulator; the
-//     products are exact in fp32, so the split projection has fp32-FFMA accuracy;
+//     form and round y, accumulate sum(y^2), store the bf16 y chunk into a ring of chunk slots in
+//     tensor memory, and drain the previous pass's accumulator into 12 per-thread fp32 sums (the
+//     three planes added back together); folded, the warps of rows 64..127 hand their sums of a
+//     tile to those of rows 0..63 (same tokens) through shared memory;
+//   MMA (warp 9): one thread issues 8 tcgen05.mma per pass (M=128 rows, N=80 >= 72 plane rows, or
+//     N=144 for the two stages of a folded pass, K=16) projecting the bf16 X' tile on the three
+//     planes into a TMEM accumulator; the products are exact in fp32, so the split projection has
+//     fp32-FFMA accuracy;
 //   store (warp 10): TMA-stores the X' tile (written once) from the same slot, then frees it;
 //   split (warp 11): at each tile end, publishes the CTA's partial sums (28 per token, in a
-//     caller-provided global workspace) with a release flag, waits (bounded) for the other flags
-//     of the group, gathers the mixes of its own tokens (t % kG == rank) over the group's blocks,
-//     and runs their split and Sinkhorn;
-//   epilogue (warps 12-15, one per TMEM lane quadrant): turn the group's sums of y^2 into r_y of
-//     the warp's rows, read each y chunk back from the ring, scale it by norm_w and r_y into a
-//     32-row swizzled staging tile and TMA-store it to y_normed.
+//     caller-provided global workspace) by a release add to the group's arrival counter, waits
+//     (bounded) until the counter shows every CTA of the group, gathers the mixes of its own tokens
+//     (t % kG == rank) over the group's blocks, and runs their split and Sinkhorn;
+//   epilogue (warps 12-15, one per TMEM lane quadrant): load norm_w of the CTA's columns, turn the
+//     group's sums of y^2 into r_y of the warp's rows, read each y chunk back from the ring, scale
+//     it by norm_w and r_y into a 32-row swizzled staging tile and TMA-store it to y_normed.
 // The ring holds a tile's y until the exchange gives r_y, with 7 stages of slack at 20 stages a
 // tile: the compute warps stream on into the next tile while the group finishes the previous one.
 // The groups are formed in software rather than as hardware clusters because only 15 clusters of
 // 8 CTAs fit on a GB300 at once (120 of its 152 SMs); the launch is cooperative, so all CTAs are
-// resident together and the flag waits between them cannot deadlock.
+// resident together and the counter waits between them cannot deadlock. It is also a programmatic
+// dependent launch: the set-up (barriers, tensor memory, descriptors, an L2 prefetch of the first
+// weight planes) overlaps the end of the kernel ahead, and every access to global memory follows
+// griddepcontrol.wait.
 //
 // Every wait on an mbarrier is bounded in time; on expiry the kernel records an error in a
 // device word, stops waiting everywhere, finishes its loops without hanging, frees its tensor
@@ -73,8 +82,8 @@ constexpr int kUmmaN = 80;        // smallest legal N >= 72 at M = 128
 // A group of kG CTAs (8, 16 or 32, a template parameter) shares one token tile, each CTA taking
 // d/kG columns; small batches use larger groups so that each CTA has fewer column stages.
 constexpr int kMaxCtas = 256;      // workspace capacity: up to 256 co-resident CTAs
-constexpr int kMaxGroups = 32;     // launch counters: group slots (at most 256 / 8)
-constexpr int kFlagRanks = 32;     // flags per (group slot, tile parity): the largest group
+constexpr int kMaxGroups = 32;     // group slots (at most 256 / 8): one arrival counter and one base each
+constexpr int kCounterStride = 16; // 64-bit words between arrival counters: one 128-byte line each
 constexpr int kTileMax = 128;
 constexpr int kChunk = 32;        // columns per stage: 64-byte rows
 constexpr int kMaxStages = 6;
@@ -90,6 +99,24 @@ constexpr int kMaxDSlice = 640;   // d <= 5120
 constexpr int kXTileBytes = kTileMax * kChunk * 2;            // 8192: 128 rows x 64 B
 constexpr int kBTileBytes = kBRows * kChunk * 2;              // 4608: 72 rows x 64 B (the MMA reads
                                                               // 80 rows; rows 72..79 are ignored)
+// Folded tiles (groups of 16 and 32, tiles of at most 64 tokens): rows 64..127 of every tile in a
+// slot hold the same tokens at the next column stage, so one 128-row MMA and all compute warps
+// serve two stages. The weight-plane tile then holds both stages' planes, rows 0..71 and 72..143,
+// and one MMA of N = 144 gives rows 0..63 their projection in accumulator columns 0..71 and rows
+// 64..127 theirs in columns 72..143 (the other blocks of the product are not read). A pass of two
+// stages on 64-token tiles is loaded with one box per tensor: the four streams' two stages of X
+// [stream][stage][token][32 columns], the two of Delta, the four streams' two stages of planes
+// (4-D and 3-D views whose "stage" dimension steps by the group's column stride), 3 TMA issues
+// instead of 18 (each issue costs a thread about 57 cycles, the first about 390).
+constexpr int kFoldRows = 64;                                 // tokens per folded tile at most
+constexpr int kFoldXHalf = kFoldRows * kChunk * 2;            // 4096: the second stage's rows
+constexpr int kUmmaNFold = 144;
+constexpr int kFoldBRow1 = kBRows;                            // first plane row of the second stage
+constexpr int kBTileBytesFold = kUmmaNFold * kChunk * 2;      // 9216
+// per token row and column half: 12 mixes, sum x^2, sum y^2 (+ 2 pad), handed from the warps of
+// rows 64..127 to those of rows 0..63 at the end of a folded tile
+constexpr int kFoldScratchFloats = 16;
+constexpr int kFoldScratchBytes = kFoldRows * 2 * kFoldScratchFloats * 4;   // 8192
 // One CTA's partial sums for one tile: mixes [128 tokens][24] (token-major), then
 // sum x^2 [128 tokens][2 column halves], then sum y^2 [128][2] (a token's two halves adjacent).
 constexpr int kPartRows = 28;
@@ -108,26 +135,36 @@ constexpr int kBarSplitDone = 21, kBarFlagsSeen = 22, kBarEpiRead = 24, kBarYRea
 // this kernel, whose warps spend most of their time in mbarrier waits, a block-wide bar.sync at
 // the end was measured releasing warp 0 while other warps had not reached it; mbarriers hold.
 constexpr int kBarPublish = 25 + 2 * 27, kBarExit = kBarPublish + 1;
-constexpr int kNumBars = kBarExit + 1;
+// folded tiles: the warps of rows 64..127 have put their partial sums of a tile in the scratch
+// (one arrival per warp), and the warps of rows 0..63 have taken them (one arrival per warp)
+constexpr int kBarFoldFull = kBarExit + 1, kBarFoldEmpty = kBarExit + 2;
+// kBarNormW: the epilogue warps have put norm_w of the CTA's columns in shared memory (one arrival per
+// epilogue warp; only they read it, long after the stage loop has started)
+constexpr int kBarNormW = kBarExit + 3;
+constexpr int kNumBars = kBarExit + 4;
 
 // Shared-memory layout of each mode, offsets from a 1024-byte aligned base. A slot holds one column
-// stage: the stream tiles (four, or the one embedding tile in expand mode), the Delta tile (post
-// mode only) and the four weight-plane tiles. The smaller slots of the reading-only modes buy more
-// of them, so more loads are in flight while the stage's MMA holds its slot: post 3 x 59392 B,
-// pre 4 x 51200 B, expand 6 x 26624 B. After the slots: norm_w of the CTA's columns, the epilogue
-// warps' y_normed staging tiles (per warp two 32-row x 64-byte tiles, 64-byte swizzle, filled and
-// TMA-stored in turn), the mbarriers, the TMEM address and the abort word.
-template <int kMode>
+// stage (a folded slot two): the stream tiles (four, or the one embedding tile in expand mode), the
+// Delta tile (post mode only) and the four weight-plane tiles. The smaller slots of the
+// reading-only modes buy more of them, so more loads are in flight while the stage's MMA holds its
+// slot: post 3 x 59392 B, pre 4 x 51200 B, expand 6 x 26624 B; folded post 2 x 81920 B, pre
+// 2 x 73728 B, expand 4 x 49152 B. After the slots: norm_w of the CTA's columns, the epilogue warps'
+// y_normed staging tiles (per warp two 32-row x 64-byte tiles, 64-byte swizzle, filled and
+// TMA-stored in turn), the folded tiles' scratch, the mbarriers, the TMEM address and the abort word.
+template <int kMode, bool kFold>
 struct Layout {
     static constexpr int kXTiles = kMode == kModeExpand ? 1 : 4;
+    static constexpr int kBTile = kFold ? kBTileBytesFold : kBTileBytes;
     static constexpr int kOffX = 0;
     static constexpr int kOffD = kXTiles * kXTileBytes;
     static constexpr int kOffB = kOffD + (kMode == kModePost ? kXTileBytes : 0);
-    static constexpr int kStage = kOffB + 4 * kBTileBytes;
-    static constexpr int kStages = kMode == kModePost ? 3 : kMode == kModePre ? 4 : 6;
+    static constexpr int kStage = kOffB + 4 * kBTile;
+    static constexpr int kStages = kFold ? (kMode == kModeExpand ? 4 : 2)
+                                         : (kMode == kModePost ? 3 : kMode == kModePre ? 4 : 6);
     static constexpr int kOffNormW = kStages * kStage;
     static constexpr int kOffYStage = ((kOffNormW + kMaxDSlice * 4 + 1023) / 1024) * 1024;
-    static constexpr int kOffBar = kOffYStage + 4 * 2 * kYStageBytes;
+    static constexpr int kOffFold = kOffYStage + 4 * 2 * kYStageBytes;
+    static constexpr int kOffBar = kOffFold + (kFold ? kFoldScratchBytes : 0);
     static constexpr int kOffTmemPtr = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemPtr + 4;
     static constexpr int kSmemUsed = kOffAbort + 4;
@@ -136,20 +173,28 @@ struct Layout {
     static_assert(kOffB % 512 == 0 && kBTileBytes % 512 == 0, "B tiles start on 512-byte swizzle atoms");
     static_assert(kStages <= kMaxStages, "barrier numbering");
     static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in shared memory of one CTA");
-    // the MMA of the last B tile of the last slot reads 8 rows (512 B) past it: into norm_w, inside the CTA
-    static_assert(kOffB + 3 * kBTileBytes + kUmmaN * 64 + (kStages - 1) * kStage <= kSmemUsed, "B overrun");
+    // unfolded: the MMA of the last B tile of the last slot reads 8 rows (512 B) past it: into norm_w,
+    // inside the CTA (a folded B tile is exactly the 160 rows its MMA reads)
+    static_assert(kOffB + 3 * kBTile + (kFold ? kUmmaNFold : kUmmaN) * 64 + (kStages - 1) * kStage <= kSmemUsed,
+                  "B overrun");
+    static_assert(kFoldXHalf % 512 == 0 && (kFoldBRow1 * 64) % 512 == 0, "second stage on swizzle atoms");
 };
 
 // global workspace: partial sums [group][tile parity][rank][28][128] fp32 (a block per CTA and
-// tile parity), then 64-bit flags [group slot][tile parity][32 ranks], then one 64-bit launch
-// counter per group slot. A flag slot is always tagged from the same counter, whatever the group
-// size of the launch that writes it, so tags never repeat on one workspace. A flag holds
-// (launch number of its group) << 32 | (tile index + 1); the launch number is the group's counter
-// + 1, read by every CTA of the group when it starts and stored back by the group's rank-0 CTA
-// after its last exchange, when all 8 have read it. The tags therefore come from the device: a
-// launch replayed from a CUDA graph tags its flags afresh, and a zero-filled workspace holds no tag.
+// tile parity), then one 64-bit arrival counter per group slot (each on its own 128-byte line),
+// then one 64-bit base per group slot. When a CTA has written its block of a tile it adds 1 to its
+// group's arrival counter (release); the tile's exchange is complete when the counter reaches
+// base + kG * (tile index + 1), the base being the counter's value when the launch started. Every
+// CTA of the group reads the base when it starts, and the group's rank-0 CTA stores the counter's
+// final value as the next base after its last exchange, when all its group has read the base and
+// added its last arrival. A group slot keeps counting across launches of any group size, so the
+// targets never repeat on one workspace; they come from the device, so a launch replayed from a
+// CUDA graph waits for its own arrivals, and a zero-filled workspace starts at 0. One counter per
+// group, polled by one lane per CTA, keeps the exchange off a contended line: with one flag per
+// CTA, polled by every lane of every CTA of a group (1024 pollers on two 128-byte lines), some
+// groups of a 256-token launch saw their flags 3-4 us after the last one was published.
 constexpr size_t kWsPartBytes = static_cast<size_t>(kMaxCtas) * 2 * kPartFloats * 4;
-constexpr size_t kWsFlagBytes = static_cast<size_t>(kMaxGroups) * 2 * kFlagRanks * 8;
+constexpr size_t kWsFlagBytes = static_cast<size_t>(kMaxGroups) * kCounterStride * 8;
 constexpr size_t kWsCounterBytes = static_cast<size_t>(kMaxGroups) * 8;
 constexpr size_t kWorkspaceBytes = kWsPartBytes + kWsFlagBytes + kWsCounterBytes;
 
@@ -163,18 +208,13 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0, kYCol = 80;
 constexpr int kRing = 27;
 static_assert(kYCol + kRing * 16 <= kTmemCols, "y ring fits in TMEM");
+// folded tiles: a 144-column accumulator, then 23 ring slots (a tile has at most 10 folded passes)
+constexpr uint32_t kYColFold = 144;
+constexpr int kRingFold = 23;
+static_assert(kYColFold + kRingFold * 16 <= kTmemCols, "folded y ring fits in TMEM");
 static_assert(kBarYFree == kBarYReady + kRing, "one ready and one free barrier per ring slot");
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
-
-// L2 handling of the streamed tiles (X, Delta): cache-hint policy of the loads (0 evict_normal,
-// 1 evict_first, 2 evict_last) and the L2 promotion of their tensor maps.
-#ifndef HC_STREAM_POLICY
-#define HC_STREAM_POLICY 0
-#endif
-#ifndef HC_STREAM_PROMOTION
-#define HC_STREAM_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_L2_128B
-#endif
 
 // device error word: bit set = which wait gave up
 __device__ unsigned int g_hc_error = 0;
@@ -206,6 +246,7 @@ struct FusedParams {
     int d_slice;
     int stages_per_tile;
     int tile_m;
+    int combined;                   // folded 64-token tiles: one box per tensor for a two-stage pass
     int iters;
     float hc_eps;
     float norm_eps;
@@ -254,13 +295,14 @@ struct Waiter {
             }
         }
     }
-    // Whole warp: lanes 0..g-1 each wait for flag f[lane] to equal `epoch`; returns when all g do.
-    __device__ __forceinline__ bool wait_flags_warp(const unsigned long long* f, unsigned long long epoch, int lane,
-                                                    int g, unsigned int code) const {
+    // Whole warp: lanes 0..g-1 each wait for the 64-bit counter c[lane] to reach `target`; returns
+    // when all g do. The fused kernel waits on one counter (g = 1): that of its group.
+    __device__ __forceinline__ bool wait_count(const unsigned long long* c, unsigned long long target, int lane,
+                                               int g, unsigned int code) const {
         const uint64_t t0 = global_timer_ns();
         bool mine = lane >= g;
         while (true) {
-            if (!mine) mine = ld_acquire_gpu_u64(f + lane) == epoch;
+            if (!mine) mine = ld_acquire_gpu_u64(c + lane) >= target;
             if (__all_sync(0xffffffffu, mine)) return true;
             const bool aborted = *abort != 0u;
             const bool late = global_timer_ns() - t0 > limit_ns;
@@ -294,6 +336,16 @@ __device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf
 // 2 * iters dependent normalisations run several times faster than with correctly rounded
 // reciprocals, which matters when a small batch waits for them, and the refinement keeps 50 rounds
 // on extreme logits inside the coefficients' 1e-5 tolerance, which the bare approximation did not.
+// The 4x4 matrix is held as row pairs (C2[2j] = columns 0-1 of row j, C2[2j+1] = columns 2-3), so
+// that the sums, refinements and products run as packed fp32x2 instructions (two IEEE operations
+// each): a column sum adds the four rows' pairs, a row sum adds a row's two pairs and then the two
+// halves, (C[j0] + C[j2]) + (C[j1] + C[j3]).
+__device__ __forceinline__ float2 rcp2_refined(float2 x) {
+    const float2 r = make_float2(rcp_approx(x.x), rcp_approx(x.y));
+    const float2 e = __ffma2_rn(make_float2(-x.x, -x.y), r, make_float2(1.0f, 1.0f));
+    return __ffma2_rn(r, e, r);
+}
+
 __device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const float (&sc)[3], const float (&b)[kMix],
                                                int iters, float eps, float (&pre)[4], float (&post)[4],
                                                float (&C)[16]) {
@@ -301,38 +353,47 @@ __device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const flo
     for (int j = 0; j < 4; ++j) pre[j] = sigmoidf_(m[j] * sc[0] + b[j]) + eps;
 #pragma unroll
     for (int j = 0; j < 4; ++j) post[j] = 2.0f * sigmoidf_(m[4 + j] * sc[1] + b[4 + j]);
-#pragma unroll
-    for (int q = 0; q < 16; ++q) C[q] = m[8 + q] * sc[2] + b[8 + q];
+    float2 C2[8];
+    const float2 e2 = make_float2(eps, eps);
     // softmax over each row (max subtracted), then + eps
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        float mx = fmaxf(fmaxf(C[4 * j], C[4 * j + 1]), fmaxf(C[4 * j + 2], C[4 * j + 3]));
-        float e0 = expf(C[4 * j] - mx), e1 = expf(C[4 * j + 1] - mx);
-        float e2 = expf(C[4 * j + 2] - mx), e3 = expf(C[4 * j + 3] - mx);
-        float inv = rcp_refined((e0 + e1) + (e2 + e3));
-        C[4 * j] = e0 * inv + eps;
-        C[4 * j + 1] = e1 * inv + eps;
-        C[4 * j + 2] = e2 * inv + eps;
-        C[4 * j + 3] = e3 * inv + eps;
+        float l[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) l[k] = m[8 + 4 * j + k] * sc[2] + b[8 + 4 * j + k];
+        const float mx = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
+        const float2 x01 = make_float2(expf(l[0] - mx), expf(l[1] - mx));
+        const float2 x23 = make_float2(expf(l[2] - mx), expf(l[3] - mx));
+        const float inv = rcp_refined((x01.x + x01.y) + (x23.x + x23.y));
+        C2[2 * j] = __ffma2_rn(x01, make_float2(inv, inv), e2);
+        C2[2 * j + 1] = __ffma2_rn(x23, make_float2(inv, inv), e2);
     }
     auto col_norm = [&]() {
+        const float2 s01 = __fadd2_rn(__fadd2_rn(C2[0], C2[2]), __fadd2_rn(C2[4], C2[6]));
+        const float2 s23 = __fadd2_rn(__fadd2_rn(C2[1], C2[3]), __fadd2_rn(C2[5], C2[7]));
+        const float2 i01 = rcp2_refined(__fadd2_rn(s01, e2));
+        const float2 i23 = rcp2_refined(__fadd2_rn(s23, e2));
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            float inv = rcp_refined(((C[k] + C[4 + k]) + (C[8 + k] + C[12 + k])) + eps);
-            C[k] *= inv;
-            C[4 + k] *= inv;
-            C[8 + k] *= inv;
-            C[12 + k] *= inv;
+        for (int j = 0; j < 4; ++j) {
+            C2[2 * j] = __fmul2_rn(C2[2 * j], i01);
+            C2[2 * j + 1] = __fmul2_rn(C2[2 * j + 1], i23);
         }
     };
     auto row_norm = [&]() {
+        float r[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            float inv = rcp_refined(((C[4 * j] + C[4 * j + 1]) + (C[4 * j + 2] + C[4 * j + 3])) + eps);
-            C[4 * j] *= inv;
-            C[4 * j + 1] *= inv;
-            C[4 * j + 2] *= inv;
-            C[4 * j + 3] *= inv;
+            const float2 h = __fadd2_rn(C2[2 * j], C2[2 * j + 1]);
+            r[j] = h.x + h.y;
+        }
+        const float2 i01 = rcp2_refined(__fadd2_rn(make_float2(r[0], r[1]), e2));
+        const float2 i23 = rcp2_refined(__fadd2_rn(make_float2(r[2], r[3]), e2));
+        const float inv[4] = {i01.x, i01.y, i23.x, i23.y};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 v = make_float2(inv[j], inv[j]);
+            C2[2 * j] = __fmul2_rn(C2[2 * j], v);
+            C2[2 * j + 1] = __fmul2_rn(C2[2 * j + 1], v);
         }
     };
     col_norm();
@@ -340,33 +401,47 @@ __device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const flo
         row_norm();
         col_norm();
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        C[4 * j] = C2[2 * j].x;
+        C[4 * j + 1] = C2[2 * j].y;
+        C[4 * j + 2] = C2[2 * j + 1].x;
+        C[4 * j + 3] = C2[2 * j + 1].y;
+    }
 }
 
-// ---- diagnostic: one bounded wait on an exchange flag ------------------------------------------------
-// One warp waits, exactly as the fused kernel's split warp waits for its group, for flags f[0..g-1]
-// to equal `value`, giving up after limit_ns: it then records kErrExchange in the device error word
-// and returns. Lets a test make a wait run out (on flags nothing sets) and check what the host sees.
+// ---- diagnostic: one bounded wait on an exchange counter ---------------------------------------------
+// One warp waits, exactly as the fused kernel's split warp waits for its group, for the counters
+// f[0..g-1] to reach `value`, giving up after limit_ns: it then records kErrExchange in the device
+// error word and returns. Lets a test make a wait run out (on counters nothing advances) and check
+// what the host sees.
 __global__ void hc_wait_flag_kernel(const unsigned long long* f, unsigned long long value, int g, uint64_t limit_ns) {
     __shared__ uint32_t abort_word;
     if (threadIdx.x == 0) abort_word = 0u;
     __syncwarp();
     const Waiter W{&abort_word, limit_ns};
-    W.wait_flags_warp(f, value, static_cast<int>(threadIdx.x), g, kErrExchange);
+    W.wait_count(f, value, static_cast<int>(threadIdx.x), g, kErrExchange);
 }
 
 // ---- the kernel ---------------------------------------------------------------------------------
 
-template <int kMode, int kG>
+template <int kMode, int kG, bool kFold>
 __global__ void __launch_bounds__(kThreads, 1)
     hc_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmD,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmXo,
                     const __grid_constant__ CUtensorMap tmM, const __grid_constant__ CUtensorMap tmY,
-                    const __grid_constant__ CUtensorMap tmYr, const FusedParams p) {
-    using Lay = Layout<kMode>;
-    constexpr int kStages = Lay::kStages, kStageBytes = Lay::kStage;
+                    const __grid_constant__ CUtensorMap tmYr, const __grid_constant__ CUtensorMap tmX4,
+                    const __grid_constant__ CUtensorMap tmXo4, const __grid_constant__ CUtensorMap tmD3,
+                    const __grid_constant__ CUtensorMap tmM3, const __grid_constant__ CUtensorMap tmB4,
+                    const __grid_constant__ CUtensorMap tmX3s, const __grid_constant__ CUtensorMap tmXo3s,
+                    const __grid_constant__ CUtensorMap tmB3, const FusedParams p) {
+    using Lay = Layout<kMode, kFold>;
+    constexpr int kStages = Lay::kStages, kStageBytes = Lay::kStage, kBTile = Lay::kBTile;
+    constexpr int kRingN = kFold ? kRingFold : kRing;
+    constexpr uint32_t kYColN = kFold ? kYColFold : kYCol;
     constexpr int kOffX = Lay::kOffX, kOffD = Lay::kOffD, kOffB = Lay::kOffB, kOffNormW = Lay::kOffNormW;
     constexpr int kOffYStage = Lay::kOffYStage, kOffBar = Lay::kOffBar, kOffTmemPtr = Lay::kOffTmemPtr;
-    constexpr int kOffAbort = Lay::kOffAbort;
+    constexpr int kOffAbort = Lay::kOffAbort, kOffFold = Lay::kOffFold;
     constexpr bool kPost = kMode == kModePost;
     constexpr bool kExpand = kMode == kModeExpand;
     constexpr bool kWriteX = kPost || kExpand;  // X' goes back to the streams
@@ -383,6 +458,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunks, so at any moment they read and write kG * 64 contiguous bytes of each stream row
     auto stage_col = [&](int s) -> int { return (s * kG + static_cast<int>(rank)) * kChunk; };
     const int S = p.stages_per_tile;
+    // passes over a tile: one per column stage, or one per pair of stages when folded (stage 2f in
+    // rows 0..63, stage 2f + 1, if any, in rows 64..127)
+    const int SP = kFold ? (S + 1) / 2 : S;
+    // A folded pass with one stage on 64-token tiles (the last pass of an odd stage count) is loaded
+    // compact, one box per tensor: the four streams' 64 rows 4 KB apart and their plane tiles 4,608
+    // bytes apart, so the 128-row MMA of stream k reads stream k + 1 as its rows 64..127 (products
+    // that land in accumulator cells nobody drains) and all reads stay inside the slot.
+    auto compact = [&](int sp) { return kFold && p.combined && 2 * sp + 1 >= S; };
+    auto x_pitch = [&](int sp) -> uint32_t { return compact(sp) ? static_cast<uint32_t>(kFoldXHalf) : kXTileBytes; };
+    auto b_pitch = [&](int sp) -> uint32_t { return compact(sp) ? static_cast<uint32_t>(kBTileBytes) : kBTile; };
 
     auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
@@ -406,49 +491,126 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(kBarPublish), kComputeWarps);
         mbar_init(bar(kBarExit), kThreads / 32);
+        mbar_init(bar(kBarFoldFull), 4);
+        mbar_init(bar(kBarFoldEmpty), 4);
+        mbar_init(bar(kBarNormW), 4);
         *abort_flag = 0u;
         fence_mbar_init();
     }
+    const long long my_tiles =
+        (static_cast<long long>(cid) < p.num_tiles) ? (p.num_tiles - 1 - cid) / ncl + 1 : 0;
+    // bytes of one column stage; a folded pass loads two (rows 64.. of each tile, plane rows 80..)
+    const uint32_t stage_bytes =
+        static_cast<uint32_t>((kExpand ? 1 : 4) * p.tile_m * 64 + (kPost ? p.tile_m * 64 : 0) + 4 * kBTileBytes);
+    // one thread: the TMA loads of pass s of the tile starting at token t0 into the slot of pass g
+    auto issue_pass = [&](long long g, int s, int t0, uint64_t pol_stream, uint64_t pol_keep) {
+        const int slot = static_cast<int>(g % kStages);
+        const uint32_t sb = sbase + slot * kStageBytes;
+        const uint32_t fb = bar(kBarFull + slot);
+        const int halves = (kFold && 2 * s + 1 < S) ? 2 : 1;
+        mbar_arrive_expect_tx(fb, stage_bytes * static_cast<uint32_t>(halves));
+        if (kFold && halves == 2 && p.combined) {
+            const int col = stage_col(2 * s);
+            if (kExpand)
+                tma_load_3d(sb + kOffX, &tmD3, fb, col, t0, 0, pol_stream);
+            else
+                tma_load_4d(sb + kOffX, &tmX4, fb, col, t0, 0, 0, pol_stream);
+            if (kPost) tma_load_3d(sb + kOffD, &tmD3, fb, col, t0, 0, pol_stream);
+            tma_load_4d(sb + kOffB, &tmB4, fb, col, 0, 0, 0, pol_keep);
+            return;
+        }
+        if (compact(s)) {
+            const int col = stage_col(2 * s);
+            if (kExpand)
+                tma_load_2d(sb + kOffX, &tmD, fb, col, t0, pol_stream);
+            else
+                tma_load_3d(sb + kOffX, &tmX3s, fb, col, t0, 0, pol_stream);
+            if (kPost) tma_load_2d(sb + kOffD, &tmD, fb, col, t0, pol_stream);
+            tma_load_3d(sb + kOffB, &tmB3, fb, col, 0, 0, pol_keep);
+            return;
+        }
+        for (int hf = 0; hf < halves; ++hf) {
+            const int col = stage_col(kFold ? 2 * s + hf : s);
+            const uint32_t xo = static_cast<uint32_t>(hf * kFoldXHalf);
+            const uint32_t bo = static_cast<uint32_t>(hf * kFoldBRow1 * 64);
+            if (kExpand) {
+                tma_load_2d(sb + kOffX + xo, &tmD, fb, col, t0, pol_stream);  // h into the stream-0 tile
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    tma_load_3d(sb + kOffX + j * kXTileBytes + xo, &tmX, fb, col, j, t0, pol_stream);
+            }
+            if (kPost) tma_load_2d(sb + kOffD + xo, &tmD, fb, col, t0, pol_stream);
+            if (!kFold) {
+                tma_load_3d(sb + kOffB, &tmB3, fb, col, 0, 0, pol_keep);  // the four streams' planes, one box
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    tma_load_2d(sb + kOffB + k * kBTile + bo, &tmB, fb, k * p.d + col, 0, pol_keep);
+            }
+        }
+    };
+    // the passes of the first tile that fill the empty slots: issued as soon as the kernel ahead has
+    // completed, by the thread that initialised the barriers and before the CTA-wide barrier below
+    // (the producer warp skips them)
+    const int early = my_tiles > 0 ? (SP < kStages ? SP : kStages) : 0;
     if (warp == kWarpProducer && lane == 0) {
         tma_prefetch_desc(&tmX);
         tma_prefetch_desc(&tmB);
         if (kWriteX) tma_prefetch_desc(&tmD);
-    }
-    {
-        float* nw = reinterpret_cast<float*>(smem + kOffNormW);
-        for (int i = threadIdx.x; i < p.d_slice; i += kThreads) nw[i] = p.norm_w[stage_col(i / kChunk) + i % kChunk];
+        // the weight-plane tiles of the first stages into L2 while the previous kernel may still run
+        // (a prefetch into L2, the point of coherence, returns nothing stale to the loads that follow
+        // the wait below)
+        if (my_tiles > 0)
+            for (int s = 0; s < S && s < (kFold ? 2 : 1) * kStages; ++s)
+                for (int k = 0; k < 4; ++k) tma_prefetch_l2_2d(&tmB, k * p.d + stage_col(s), 0);
     }
     if (warp == 0) {
         tmem_alloc(sbase + kOffTmemPtr, kTmemCols);
         tmem_relinquish();
+    }
+    // Launched with programmatic stream serialization: the set-up above (barriers, tensor memory,
+    // descriptors, L2 prefetch) overlaps the end of the kernel ahead on the stream; every read and
+    // write of global memory comes after this wait for that kernel to complete. The next kernel may
+    // start its own set-up as soon as every CTA of this one has got here.
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    griddep_wait();
+    if (threadIdx.x == 0) {
+        // the streamed tiles (X, Delta) keep the normal L2 policy: evict_first dropped the unused
+        // half of each 128-byte line and re-read it (356 MB more per prefill step)
+        const uint64_t pol_stream = policy_evict_normal(), pol_keep = policy_evict_last();
+        for (int s = 0; s < early; ++s) issue_pass(s, s, static_cast<int>(cid * p.tile_m), pol_stream, pol_keep);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemPtr);
 
-    const long long my_tiles =
-        (static_cast<long long>(cid) < p.num_tiles) ? (p.num_tiles - 1 - cid) / ncl + 1 : 0;
-
     if (warp < kComputeWarps) {
         // ================= compute warps: X', sums, y, accumulator drain ========================
-        const int q = warp & 3;             // TMEM lane quadrant = token rows 32q..32q+31
+        const int q = warp & 3;             // TMEM lane quadrant = tile rows 32q..32q+31
         const int h = warp >> 2;            // column half of each 32-column stage
-        const int row = 32 * q + lane;      // token row inside the tile
+        const int row = 32 * q + lane;      // row of the tile (and TMEM lane)
+        // folded: rows 64..127 (sub = 1) hold the tokens of rows 0..63 at the pass's second stage
+        const int sub = kFold ? (q >> 1) : 0;
+        const int trow = kFold ? (row & (kFoldRows - 1)) : row;  // token row inside the tile
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        long long g = 0;        // global stage counter (same sequence in every role)
-        // tell the epilogue warps that the y chunk of stage gy is in TMEM
+        long long g = 0;        // global pass counter (same sequence in every role)
+        // does pass sp of a tile hold a stage for this warp's rows (folded: not the second half of
+        // the last pass when the stages are odd)
+        auto pass_ok = [&](int sp) { return !kFold || 2 * sp + sub < S; };
+        // tell the epilogue warps that the y chunk of pass gy is in TMEM
         auto y_ready = [&](long long gy) {
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarYReady + static_cast<int>(gy % kRing)));
+            if (lane == 0) mbar_arrive(bar(kBarYReady + static_cast<int>(gy % kRingN)));
         };
         for (long long it = 0; it < my_tiles; ++it) {
             const long long tile = cid + it * ncl;
             const long long t0 = tile * p.tile_m;
-            const long long tok = t0 + row;
-            const bool valid = (row < p.tile_m) && (tok < p.n);
+            const long long tok = t0 + trow;
+            const bool valid = (trow < p.tile_m) && (tok < p.n);
             // this token's coefficients, each broadcast to both lanes of a float2
             float2 cpost[4], ccomb[16], pm[4];
 #pragma unroll
@@ -481,37 +643,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 4; ++i) sx[i] = bcast(0.f);
             sy[0] = sy[1] = bcast(0.f);
 
-            auto drain = [&](long long gd) {
+            // drain pass gd's accumulator (the three planes added back together) into acc; a folded
+            // pass with no stage for these rows is waited for and released but not added
+            auto drain = [&](long long gd, bool add) {
                 W.wait(bar(kBarAccFull), static_cast<uint32_t>(gd & 1), kErrComputeAcc);
                 tc_fence_after();
-                uint32_t v[36];
-                const uint32_t col = kAccCol + 36u * h;
-                tmem_ld36_wait(tl + col, tl + col + 32u, v);
-                auto f2 = [&](int i) { return make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])); };
+                if (add) {
+                    uint32_t v[36];
+                    const uint32_t col = kAccCol + (sub ? static_cast<uint32_t>(kFoldBRow1) : 0u) + 36u * h;
+                    tmem_ld36_wait(tl + col, tl + col + 32u, v);
+                    auto f2 = [&](int i) { return make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])); };
 #pragma unroll
-                for (int i = 0; i < 6; ++i)
-                    acc[i] = __fadd2_rn(acc[i], __fadd2_rn(__fadd2_rn(f2(2 * i), f2(12 + 2 * i)), f2(24 + 2 * i)));
+                    for (int i = 0; i < 6; ++i)
+                        acc[i] = __fadd2_rn(acc[i], __fadd2_rn(__fadd2_rn(f2(2 * i), f2(12 + 2 * i)), f2(24 + 2 * i)));
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarAccEmpty));
             };
 
-            for (int s = 0; s < S; ++s, ++g) {
-                // the y store of the previous stage has had a stage to complete: hand it over
+            for (int s = 0; s < SP; ++s, ++g) {
+                // the y store of the previous pass has had a pass to complete: hand it over
                 if (s > 0) y_ready(g - 1);
-                // reading-only modes: the MMA of this stage reads the tile as loaded, so it may start
-                // as soon as the data lands; drain the previous stage's accumulator first to let it
-                if (!kPost && s > 0) drain(g - 1);
-                // the ring slot of this stage's y last held the chunk of stage g - kRing
-                const long long yround = g / kRing;
+                // reading-only modes: the MMA of this pass reads the tile as loaded, so it may start
+                // as soon as the data lands; drain the previous pass's accumulator first to let it
+                if (!kPost && s > 0) drain(g - 1, pass_ok(s - 1));
+                // the ring slot of this pass's y last held the chunk of pass g - kRingN
+                const long long yround = g / kRingN;
                 if (yround > 0)
-                    W.wait(bar(kBarYFree + static_cast<int>(g % kRing)), static_cast<uint32_t>((yround - 1) & 1),
+                    W.wait(bar(kBarYFree + static_cast<int>(g % kRingN)), static_cast<uint32_t>((yround - 1) & 1),
                            kErrComputeY);
                 const int slot = static_cast<int>(g % kStages);
                 const uint32_t par = static_cast<uint32_t>((g / kStages) & 1);
                 W.wait(bar(kBarFull + slot), par, kErrComputeFull);
                 const uint32_t sb = sbase + slot * kStageBytes;
+                const bool here = pass_ok(s);  // warp-uniform
+                const uint32_t xp = x_pitch(s);  // bytes between the streams' tiles in this pass
                 uint32_t yb[8];
+                if (here) {
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const int c = 2 * h + cc;
@@ -525,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         xv[3] = xv[0];
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) xv[j] = ld_smem_v4(sb + kOffX + j * kXTileBytes + off);
+                        for (int j = 0; j < 4; ++j) xv[j] = ld_smem_v4(sb + kOffX + j * xp + off);
                     }
                     if (kPost) {
                         // X'_k = post_k * Delta + sum_j comb[j,k] X_j, in this order for every column
@@ -546,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 o[e] = pack_bf16(t);
                             }
                             const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
-                            st_smem_v4(sb + kOffX + k * kXTileBytes + off, ov);
+                            st_smem_v4(sb + kOffX + k * xp + off, ov);
                             unpack4(ov, xr[k]);
                         }
                         if (p.stream_mean) {
@@ -582,16 +751,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sy[cc] = __ffma2_rn(a, a, sy[cc]);
                     }
                 }
-                tmem_st8(tl + kYCol + static_cast<uint32_t>((g % kRing) * 16 + h * 8), yb);
+                tmem_st8(tl + kYColN + static_cast<uint32_t>((g % kRingN) * 16 + h * 8), yb);
+                }
                 if (kPost) fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarXReady + slot));
-                // drain the previous stage's accumulator now: its MMA ran while this stage was
-                // computed, so nothing waits here, and the MMA of this stage (which needs the
+                // drain the previous pass's accumulator now: its MMA ran while this pass was
+                // computed, so nothing waits here, and the MMA of this pass (which needs the
                 // accumulator empty) is issued right after
-                if (kPost && s > 0) drain(g - 1);
+                if (kPost && s > 0) drain(g - 1, pass_ok(s - 1));
             }
-            drain(g - 1);
+            drain(g - 1, pass_ok(SP - 1));
             y_ready(g - 1);
 
             // publish this CTA's partial sums of the tile to the group; the split warp collects them.
@@ -599,19 +769,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             // still be reading; each of them publishes tile it - 1 only after it has read tile it - 2,
             // and this CTA's split warp signals split_done(it - 1) only after it has seen all those
             // flags (and read tile it - 1 itself).
+            const float2 sxx = __fadd2_rn(__fadd2_rn(sx[0], sx[1]), __fadd2_rn(sx[2], sx[3]));
+            const float2 syy = __fadd2_rn(sy[0], sy[1]);
+            float sxs = sxx.x + sxx.y, sys = syy.x + syy.y;
+            if (kFold) {
+                // the same tokens' sums of the odd stages (rows 64..127) join those of the even ones
+                float4* fs = reinterpret_cast<float4*>(smem + kOffFold) + (trow * 2 + h) * (kFoldScratchFloats / 4);
+                if (sub) {
+                    if (it > 0) W.wait(bar(kBarFoldEmpty), static_cast<uint32_t>((it - 1) & 1), kErrComputeAcc);
+                    fs[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+                    fs[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+                    fs[2] = make_float4(acc[4].x, acc[4].y, acc[5].x, acc[5].y);
+                    fs[3] = make_float4(sxs, sys, 0.f, 0.f);
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(bar(kBarFoldFull));
+                        mbar_arrive(bar(kBarPublish));  // the block is written by the warp of rows 0..63
+                    }
+                    continue;
+                }
+                W.wait(bar(kBarFoldFull), static_cast<uint32_t>(it & 1), kErrComputeAcc);
+                const float4 f0 = fs[0], f1 = fs[1], f2v = fs[2], f3 = fs[3];
+                acc[0] = __fadd2_rn(acc[0], make_float2(f0.x, f0.y));
+                acc[1] = __fadd2_rn(acc[1], make_float2(f0.z, f0.w));
+                acc[2] = __fadd2_rn(acc[2], make_float2(f1.x, f1.y));
+                acc[3] = __fadd2_rn(acc[3], make_float2(f1.z, f1.w));
+                acc[4] = __fadd2_rn(acc[4], make_float2(f2v.x, f2v.y));
+                acc[5] = __fadd2_rn(acc[5], make_float2(f2v.z, f2v.w));
+                sxs += f3.x;
+                sys += f3.y;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarFoldEmpty));
+            }
             if (it > 0) W.wait(bar(kBarSplitDone), static_cast<uint32_t>((it - 1) & 1), kErrExchange);
             const int buf = static_cast<int>(it & 1);
             float* P = p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kG + rank) * kPartFloats;
             {
-                float4* pm4 = reinterpret_cast<float4*>(P + row * kMix + 12 * h);
+                float4* pm4 = reinterpret_cast<float4*>(P + trow * kMix + 12 * h);
                 pm4[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
                 pm4[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
                 pm4[2] = make_float4(acc[4].x, acc[4].y, acc[5].x, acc[5].y);
             }
-            const float2 sxx = __fadd2_rn(__fadd2_rn(sx[0], sx[1]), __fadd2_rn(sx[2], sx[3]));
-            const float2 syy = __fadd2_rn(sy[0], sy[1]);
-            P[kPartSx + 2 * row + h] = sxx.x + sxx.y;
-            P[kPartSy + 2 * row + h] = syy.x + syy.y;
+            P[kPartSx + 2 * trow + h] = sxs;
+            P[kPartSy + 2 * trow + h] = sys;
             // hand the block to the split warp, which publishes it; no waiting here
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarPublish));
@@ -619,9 +819,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= kWarpEpi0) {
         // ================= epilogue warps: y_normed = bf16(norm_w * y * r_y), one quadrant each ===
         const int q = warp & 3;
-        const int row = 32 * q + lane;
+        // folded: quadrants 2 and 3 hold the tokens of quadrants 0 and 1 at each pass's second stage
+        const int sub = kFold ? (q >> 1) : 0;
+        const int qt = kFold ? (q & 1) : q;   // this warp's 32 token rows: 32 qt .. 32 qt + 31
+        const int trow = 32 * qt + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        const float* nw = reinterpret_cast<const float*>(smem + kOffNormW);
+        float* nw = reinterpret_cast<float*>(smem + kOffNormW);
+        // norm_w of this CTA's columns, loaded by the epilogue warps themselves: off the path to the
+        // first loads, and needed only once a tile's exchange is complete
+        for (int i = threadIdx.x - kWarpEpi0 * 32; i < p.d_slice; i += 4 * 32)
+            nw[i] = p.norm_w[stage_col(i / kChunk) + i % kChunk];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarNormW));
+        W.wait(bar(kBarNormW), 0u, kErrEpilogue);
         const float inv_d = 1.0f / static_cast<float>(p.d);
         long long g = 0;
         long long ystores = 0;  // TMA stores this warp has issued (staging tiles alternate)
@@ -631,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // column shares), once the split warp has seen all their flags
             W.wait(bar(kBarFlagsSeen + buf), static_cast<uint32_t>((it >> 1) & 1), kErrEpilogue);
             const float* blk =
-                p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kG) * kPartFloats + kPartSy + 2 * row;
+                p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kG) * kPartFloats + kPartSy + 2 * trow;
             // all kG loads in flight at once (one L2 round trip), summed in share order
             float2 sq[kG];
 #pragma unroll
@@ -639,29 +849,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             float ssq = 0.f;
 #pragma unroll
             for (int r = 0; r < kG; ++r) ssq += sq[r].x + sq[r].y;
-            const float ry = 1.0f / sqrtf(ssq * inv_d + p.norm_eps);
+            const float ry = rsqrtf(ssq * inv_d + p.norm_eps);  // the norm's rsqrt of mean(y^2) + eps
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarEpiRead));  // this warp is done with the tile's blocks
             const long long t0 = (cid + it * ncl) * p.tile_m;
             // this warp's rows go out as one TMA tile: 32 rows, or the tile's last tile_m % 32 rows
             // through the second map (rows past n are clipped by the maps; rows past tile_m belong
             // to the next tile and are never stored)
-            const int rows_q = p.tile_m - 32 * q;
+            const int rows_q = p.tile_m - 32 * qt;
             const bool store = p.write_y && rows_q > 0;
             const CUtensorMap* ymap = rows_q >= 32 ? &tmY : &tmYr;
-            for (int s = 0; s < S; ++s, ++g) {
-                const int ys = static_cast<int>(g % kRing);
-                W.wait(bar(kBarYReady + ys), static_cast<uint32_t>((g / kRing) & 1), kErrEpilogue);
+            for (int s = 0; s < SP; ++s, ++g) {
+                const int cs = kFold ? 2 * s + sub : s;  // the column stage of this warp's rows
+                const int ys = static_cast<int>(g % kRingN);
+                W.wait(bar(kBarYReady + ys), static_cast<uint32_t>((g / kRingN) & 1), kErrEpilogue);
                 tc_fence_after();
                 uint32_t yv[16];
-                tmem_ld16_wait(tl + kYCol + static_cast<uint32_t>(ys * 16), yv);
+                tmem_ld16_wait(tl + kYColN + static_cast<uint32_t>(ys * 16), yv);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarYFree + ys));
-                if (store) {
+                if (store && cs < S) {
                     // TMEM columns ys*16 + 0..7 hold stage columns 0..15 (half 0), + 8..15 hold 16..31;
                     // y_normed = norm_w * (y * r_y), two columns per instruction
-                    const float2* w = reinterpret_cast<const float2*>(nw + s * 32);
+                    const float2* w = reinterpret_cast<const float2*>(nw + cs * 32);
                     const float2 ry2 = bcast(ry);
                     uint32_t ov[16];
 #pragma unroll
@@ -677,7 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(ymap, st, stage_col(s), static_cast<int>(t0 + 32 * q));
+                        tma_store_2d(ymap, st, stage_col(cs), static_cast<int>(t0 + 32 * qt));
                         bulk_commit();
                     }
                     ++ystores;
@@ -690,36 +901,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= TMA producer =========================================================
         uint64_t pol_stream = 0, pol_keep = 0;
         if (lane == 0) {
-            pol_stream = HC_STREAM_POLICY == 1 ? policy_evict_first()
-                         : HC_STREAM_POLICY == 2 ? policy_evict_last() : policy_evict_normal();
+            pol_stream = policy_evict_normal();
             pol_keep = policy_evict_last();
         }
-        const uint32_t bytes =
-            static_cast<uint32_t>((kExpand ? 1 : 4) * p.tile_m * 64 + (kPost ? p.tile_m * 64 : 0) + 4 * kBTileBytes);
         long long g = 0;
         for (long long it = 0; it < my_tiles; ++it) {
             const long long tile = cid + it * ncl;
             const int t0 = static_cast<int>(tile * p.tile_m);
-            for (int s = 0; s < S; ++s, ++g) {
+            for (int s = 0; s < SP; ++s, ++g) {
+                if (g < early) continue;  // issued at the start
                 const int slot = static_cast<int>(g % kStages);
                 const long long round = g / kStages;
                 if (round > 0) W.wait(bar(kBarEmpty + slot), static_cast<uint32_t>((round - 1) & 1), kErrProducer);
-                if (lane == 0) {
-                    const uint32_t sb = sbase + slot * kStageBytes;
-                    const uint32_t fb = bar(kBarFull + slot);
-                    const int col = stage_col(s);
-                    mbar_arrive_expect_tx(fb, bytes);
-                    if (kExpand) {
-                        tma_load_2d(sb + kOffX, &tmD, fb, col, t0, pol_stream);  // h into the stream-0 tile
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            tma_load_3d(sb + kOffX + j * kXTileBytes, &tmX, fb, col, j, t0, pol_stream);
-                    }
-                    if (kPost) tma_load_2d(sb + kOffD, &tmD, fb, col, t0, pol_stream);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) tma_load_2d(sb + kOffB + k * kBTileBytes, &tmB, fb, k * p.d + col, 0, pol_keep);
-                }
+                if (lane == 0) issue_pass(g, s, t0, pol_stream, pol_keep);
                 __syncwarp();
             }
         }
@@ -729,10 +923,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             W.drain(bar(kBarFull + static_cast<int>(gg % kStages)), static_cast<uint32_t>((gg / kStages) & 1));
     } else if (warp == kWarpMma) {
         // ================= MMA issuer ===========================================================
-        constexpr uint32_t idesc = idesc_bf16_f32(kUmmaM, kUmmaN);
+        constexpr uint32_t idesc = idesc_bf16_f32(kUmmaM, kFold ? kUmmaNFold : kUmmaN);
         long long g = 0;
         for (long long it = 0; it < my_tiles; ++it) {
-            for (int s = 0; s < S; ++s, ++g) {
+            for (int s = 0; s < SP; ++s, ++g) {
                 const int slot = static_cast<int>(g % kStages);
                 // the single accumulator must have been drained (stage g - 1)
                 if (g > 0) W.wait(bar(kBarAccEmpty), static_cast<uint32_t>((g - 1) & 1), kErrMma);
@@ -746,8 +940,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < 4; ++k) {
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
-                            const uint64_t ad = sdesc_kmajor_sw64(sb + kOffX + (kExpand ? 0 : k * kXTileBytes) + kk * 32);
-                            const uint64_t bd = sdesc_kmajor_sw64(sb + kOffB + k * kBTileBytes + kk * 32);
+                            const uint64_t ad = sdesc_kmajor_sw64(sb + kOffX + (kExpand ? 0 : k * x_pitch(s)) + kk * 32);
+                            const uint64_t bd = sdesc_kmajor_sw64(sb + kOffB + k * b_pitch(s) + kk * 32);
                             umma_bf16(dcol, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
                         }
                     }
@@ -768,16 +962,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (long long it = 0; it < my_tiles; ++it) {
             const long long tile = cid + it * ncl;
             const int t0 = static_cast<int>(tile * p.tile_m);
-            for (int s = 0; s < S; ++s, ++g) {
+            for (int s = 0; s < SP; ++s, ++g) {
                 const int slot = static_cast<int>(g % kStages);
                 W.wait(bar(kBarXReady + slot), static_cast<uint32_t>((g / kStages) & 1), kErrStore);
                 if (kWriteX && lane == 0) {
                     const uint32_t sb = sbase + slot * kStageBytes;
-                    const int col = stage_col(s);
+                    const int halves = (kFold && 2 * s + 1 < S) ? 2 : 1;
+                    if (kPost && halves == 2 && p.combined) {
+                        // both stages of the four streams in one box, the tap's two in another
+                        tma_store_4d(&tmXo4, sb + kOffX, stage_col(2 * s), t0, 0, 0);
+                        if (p.stream_mean) tma_store_3d(&tmM3, sb + kOffD, stage_col(2 * s), t0, 0);
+                    } else if (kPost && compact(s)) {
+                        tma_store_3d(&tmXo3s, sb + kOffX, stage_col(2 * s), t0, 0);  // the compact tiles
+                        if (p.stream_mean) tma_store_2d(&tmM, sb + kOffD, stage_col(2 * s), t0);
+                    } else {
+                        for (int hf = 0; hf < halves; ++hf) {
+                            const int col = stage_col(kFold ? 2 * s + hf : s);
+                            const uint32_t xo = static_cast<uint32_t>(hf * kFoldXHalf);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        tma_store_3d(&tmXo, sb + kOffX + (kExpand ? 0 : k * kXTileBytes), col, k, t0);
-                    if (kPost && p.stream_mean) tma_store_2d(&tmM, sb + kOffD, col, t0);  // the tap
+                            for (int k = 0; k < 4; ++k)
+                                tma_store_3d(&tmXo, sb + kOffX + (kExpand ? 0 : k * kXTileBytes) + xo, col, k, t0);
+                            if (kPost && p.stream_mean) tma_store_2d(&tmM, sb + kOffD + xo, col, t0);  // the tap
+                        }
+                    }
                     bulk_commit();
                     bulk_wait_read<0>();
                 }
@@ -793,27 +1000,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 3; ++i) sc[i] = __ldg(p.hc_scale + i);
 #pragma unroll
         for (int i = 0; i < kMix; ++i) bs[i] = __ldg(p.hc_base + i);
-        // this launch's number for the group: its counter + 1 (never 0, which a fresh workspace holds)
-        unsigned long long launch_no = 0;
-        if (lane == 0) launch_no = ld_acquire_gpu_u64(p.ws_launch + cid) + 1ull;
-        launch_no = __shfl_sync(0xffffffffu, launch_no, 0);
-        const unsigned long long epoch_base = launch_no << 32;
+        // the group's arrival counter and its value when this launch started
+        unsigned long long* arrivals = p.ws_flags + static_cast<size_t>(cid) * kCounterStride;
+        unsigned long long base = 0;
+        if (lane == 0) base = ld_acquire_gpu_u64(p.ws_launch + cid);
+        base = __shfl_sync(0xffffffffu, base, 0);
         for (long long it = 0; it < my_tiles; ++it) {
             const int buf = static_cast<int>(it & 1);
             // the compute warps have written this CTA's block of the tile: publish it, then wait for
-            // the group (lanes 0..7 poll one flag each)
+            // the group (lane 0 polls the group's arrival counter)
             W.wait(bar(kBarPublish), static_cast<uint32_t>(it & 1), kErrSplit);
-            // a flag also says that this CTA is done reading the group's blocks of the previous tile
-            // (whose buffer the group reuses after this tile): the split warp read them in its last
-            // iteration, the epilogue warps read the sums of y^2
+            // an arrival also says that this CTA is done reading the group's blocks of the previous
+            // tile (whose buffer the group reuses after this tile): the split warp read them in its
+            // last iteration, the epilogue warps read the sums of y^2
             if (it >= 1) W.wait(bar(kBarEpiRead), static_cast<uint32_t>((it - 1) & 1), kErrSplit);
-            unsigned long long* flg = p.ws_flags + static_cast<size_t>(cid * 2 + buf) * kFlagRanks;
-            const unsigned long long epoch = epoch_base + static_cast<unsigned long long>(it) + 1ull;
-            if (lane == 0) {
-                fence_acq_rel_gpu();  // after the barrier: the compute threads' block writes come first
-                st_release_gpu_u64(flg + rank, epoch);
-            }
-            W.wait_flags_warp(flg, epoch, lane, kG, kErrExchange);
+            // the compute warps' block writes happen before the add (the publish mbarrier orders them
+            // within the CTA, the add's release orders them at GPU scope)
+            if (lane == 0) red_release_gpu_add_u64(arrivals, 1ull);
+            const unsigned long long target = base + static_cast<unsigned long long>(kG) * static_cast<unsigned long long>(it + 1);
+            W.wait_count(arrivals, target, lane, 1, kErrExchange);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarFlagsSeen + buf));  // the epilogue warps may read the sums of y^2
             const long long tile = cid + it * ncl;
@@ -881,7 +1086,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(bar(kBarSplitDone));  // the blocks of this tile may be reused
             if (mine && oh == 0) {
                 const long long tok = t0 + r_tok;
-                const float rr = 1.0f / sqrtf(sxt / static_cast<float>(4 * p.d) + p.norm_eps);
+                const float rr = rsqrtf(sxt / static_cast<float>(4 * p.d) + p.norm_eps);  // rsqrt of mean(x^2) + eps
 #pragma unroll
                 for (int i = 0; i < kMix; ++i) m[i] *= rr;
                 if (p.mixes_out) {
@@ -901,9 +1106,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         }
-        // every CTA of the group has read the counter (each published a flag of the last tile,
-        // which this warp has seen): advance it for the group's next launch
-        if (rank == 0 && lane == 0 && my_tiles > 0) st_release_gpu_u64(p.ws_launch + cid, launch_no);
+        // every CTA of the group has read the base and added its last arrival (the counter reached
+        // the last tile's target, which this warp has seen): store the final count as the next base
+        if (rank == 0 && lane == 0 && my_tiles > 0)
+            st_release_gpu_u64(p.ws_launch + cid,
+                               base + static_cast<unsigned long long>(kG) * static_cast<unsigned long long>(my_tiles));
         __syncwarp();
     }
 
@@ -942,7 +1149,7 @@ bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, co
             CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_128B) {
     auto fn = get_encode();
     if (!fn) return false;
-    uint32_t estr[3] = {1, 1, 1};
+    uint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
                     reinterpret_cast<const cuuint64_t*>(dims), reinterpret_cast<const cuuint64_t*>(strides_bytes),
                     reinterpret_cast<const cuuint32_t*>(box), reinterpret_cast<const cuuint32_t*>(estr),
@@ -960,12 +1167,25 @@ constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-// every instantiation of the fused kernel: [mode][group size 8, 16, 32]
+// every instantiation of the fused kernel: [mode][group size 8, 16, 32]; groups of 16 and 32 always
+// fold their tiles (at most 64 tokens), groups of 8 never, so that a token's mixes (the order in
+// which its partial sums meet) depend on the group size alone
+constexpr bool fold_of(int group) { return group != 8; }
+
 template <int kMode>
-void kernels_of_mode(const void** k) {
-    k[0] = reinterpret_cast<const void*>(&hc_fused_kernel<kMode, 8>);
-    k[1] = reinterpret_cast<const void*>(&hc_fused_kernel<kMode, 16>);
-    k[2] = reinterpret_cast<const void*>(&hc_fused_kernel<kMode, 32>);
+void kernels_of_mode(const void** k, int* smem) {
+    k[0] = reinterpret_cast<const void*>(&hc_fused_kernel<kMode, 8, fold_of(8)>);
+    k[1] = reinterpret_cast<const void*>(&hc_fused_kernel<kMode, 16, fold_of(16)>);
+    k[2] = reinterpret_cast<const void*>(&hc_fused_kernel<kMode, 32, fold_of(32)>);
+    smem[0] = Layout<kMode, fold_of(8)>::kSmemBytes;
+    smem[1] = Layout<kMode, fold_of(16)>::kSmemBytes;
+    smem[2] = Layout<kMode, fold_of(32)>::kSmemBytes;
+}
+
+template <int kMode>
+int smem_of(int group) {
+    return group == 8 ? Layout<kMode, fold_of(8)>::kSmemBytes
+                      : group == 16 ? Layout<kMode, fold_of(16)>::kSmemBytes : Layout<kMode, fold_of(32)>::kSmemBytes;
 }
 
 int prepare_device(int* ctas) {
@@ -975,14 +1195,10 @@ int prepare_device(int* ctas) {
     DeviceState& st = g_dev[dev];
     if (!st.ready) {
         const void* kernels[9];
-        kernels_of_mode<kModePre>(kernels);
-        kernels_of_mode<kModePost>(kernels + 3);
-        kernels_of_mode<kModeExpand>(kernels + 6);
-        const int k_smem[9] = {Layout<kModePre>::kSmemBytes,    Layout<kModePre>::kSmemBytes,
-                               Layout<kModePre>::kSmemBytes,    Layout<kModePost>::kSmemBytes,
-                               Layout<kModePost>::kSmemBytes,   Layout<kModePost>::kSmemBytes,
-                               Layout<kModeExpand>::kSmemBytes, Layout<kModeExpand>::kSmemBytes,
-                               Layout<kModeExpand>::kSmemBytes};
+        int k_smem[9];
+        kernels_of_mode<kModePre>(kernels, k_smem);
+        kernels_of_mode<kModePost>(kernels + 3, k_smem + 3);
+        kernels_of_mode<kModeExpand>(kernels + 6, k_smem + 6);
         int per_sm = 1 << 30;
         for (int i = 0; i < 9; ++i) {
             const void* k = kernels[i];
@@ -1006,40 +1222,47 @@ int prepare_device(int* ctas) {
 
 }  // namespace
 
-// Launch plan: for each group size g (d a multiple of 32 g) and tile height m (32, 64, 96, 128, a
-// balanced height of 96..128 for batches of several waves, or n when n < 32), groups = ctas / g groups run at once; a launch takes ceil(tiles / groups) waves of S =
-// d / (32 g) column stages each, plus a per-tile cost (group exchange, y_normed epilogue tail).
-// A stage costs the larger of its latency floor and a fixed part plus a part per token row; the
-// constants were measured on GB300 (2.1 us per 128-token stage of the prefill step, about 0.8 us
-// for a stage of a small batch, about 4 us per tile).
+// Launch plan: for each group size g (d a multiple of 32 g) and tile height m, groups = ctas / g
+// groups run at once; a launch takes ceil(tiles / groups) waves, each of P passes over a tile plus
+// a per-tile cost (group exchange, y_normed epilogue tail). Groups of 8 take tiles of 32, 64, 96 or
+// 128 tokens (or a balanced height of 96..128 for batches of several waves, or n when n < 32) and
+// make one pass per column stage, P = S = d / (32 g). Groups of 16 and 32 fold: tiles of 32 or 64
+// tokens (or n when n < 32), two column stages per pass in the 128 rows of the MMA, P = ceil(S / 2).
+// A pass costs the larger of its latency floor and a fixed part plus a part per row in use; the
+// constants were measured on GB300 (2.1 us per 128-row pass of the prefill step, about 0.8 us for
+// a pass of a small batch, 1.3 us for a folded pass of a decode batch, about 4 us per tile).
 void plan_tiles(int64_t n, int d, int ctas, int only_group, int* group, int* tile_m, int64_t* num_tiles) {
     *group = 8;
     *tile_m = kTileMax;
     *num_tiles = 0;
     if (n <= 0) return;
-    constexpr double kStageFloorUs = 0.8, kStageFixedUs = 0.5, kStagePerRowUs = 1.6 / kTileMax, kTileUs = 4.0;
+    constexpr double kPassFloorUs = 0.8, kFoldFloorUs = 1.3, kPassFixedUs = 0.5, kPassPerRowUs = 1.6 / kTileMax,
+                     kTileUs = 4.0;
     double best = -1.0;
     const int gs[3] = {8, 16, 32};
     for (int g : gs) {
         if (d % (kChunk * g) != 0 || (only_group != 0 && g != only_group)) continue;
         const int groups = ctas / g;
         if (groups < 1) continue;
+        const bool fold = fold_of(g);
         const int S = d / (kChunk * g);
+        const int P = fold ? (S + 1) / 2 : S;
         // tile heights, largest first (ties keep the larger tile and the smaller group), then for
-        // batches of several waves the height that spreads the tokens evenly over the waves
+        // unfolded batches of several waves the height that spreads the tokens evenly over the waves
         // 128-token tiles would take (16,384 tokens: 133 tiles of 124 fill 7 waves of 19 groups,
         // where 128 tiles of 128 leave 5 groups idle in the last); only from 96 rows up, where a
         // stage's time still follows its rows (shorter balanced tiles measured slower)
         const int64_t waves128 = ((n + kTileMax - 1) / kTileMax + groups - 1) / groups;
         const int m_even = static_cast<int>((n + groups * waves128 - 1) / (groups * waves128));
-        const int ms[6] = {128, 96, 64, 32, n < 32 ? static_cast<int>(n) : 0,
-                           waves128 > 1 && m_even >= 96 ? m_even : 0};
+        const int ms[6] = {fold ? 0 : 128, fold ? 0 : 96, 64, 32, n < 32 ? static_cast<int>(n) : 0,
+                           !fold && waves128 > 1 && m_even >= 96 ? m_even : 0};
         for (int m : ms) {
             if (m < 1) continue;
             const int64_t tiles = (n + m - 1) / m;
             const int64_t waves = (tiles + groups - 1) / groups;
-            const double stage = std::max(kStageFloorUs, kStageFixedUs + m * kStagePerRowUs);
-            const double cost = static_cast<double>(waves) * (S * stage + kTileUs);
+            const int rows = fold && S > 1 ? 2 * m : m;
+            const double pass = std::max(fold ? kFoldFloorUs : kPassFloorUs, kPassFixedUs + rows * kPassPerRowUs);
+            const double cost = static_cast<double>(waves) * (P * pass + kTileUs);
             if (best < 0.0 || cost < best - 1e-9) {
                 best = cost;
                 *group = g;
@@ -1075,14 +1298,14 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
         const uint64_t dims[3] = {d, 4, n};
         const uint64_t str[2] = {d * 2, 4 * d * 2};
         const uint32_t box[3] = {kChunk, 1, static_cast<uint32_t>(tile_m)};
-        if (!encode(&tmX, x_in, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B, HC_STREAM_PROMOTION)) return -7;
+        if (!encode(&tmX, x_in, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
         if (!encode(&tmXo, write_x ? a.X_out : a.X, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
     }
     {
         const uint64_t dims[2] = {d, n};
         const uint64_t str[1] = {d * 2};
         const uint32_t box[2] = {kChunk, static_cast<uint32_t>(tile_m)};
-        if (!encode(&tmD, rows, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B, HC_STREAM_PROMOTION)) return -7;
+        if (!encode(&tmD, rows, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
         // the tap's rows (encoded on the read rows when there is no tap: never used then)
         if (!encode(&tmM, a.stream_mean ? a.stream_mean : rows, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
         // y_normed in 32-row tiles, one per epilogue warp (encoded on the read rows when it is not written)
@@ -1097,6 +1320,52 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
         const uint64_t str[1] = {4 * d * 2};
         const uint32_t box[2] = {kChunk, static_cast<uint32_t>(kBRows)};
         if (!encode(&tmB, a.planes, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+    }
+    // Folded 64-token tiles load a pass of two stages with one box per tensor: views with a "stage"
+    // dimension of 2 whose stride is the group's column step (a CTA's stages are kG * 32 columns
+    // apart); the box lands as [stream][stage][token][32 columns], which is the folded slot's layout.
+    // These maps are used only for passes whose two stages exist, so no box reaches past a row. For
+    // other launches they are placeholders, never read.
+    const bool combined = fold_of(group) && tile_m == kFoldRows;
+    CUtensorMap tmX4 = tmX, tmXo4 = tmXo, tmD3 = tmD, tmM3 = tmM, tmB4 = tmB, tmX3s = tmX, tmXo3s = tmXo, tmB3 = tmB;
+    {
+        // the four streams' plane tiles of one stage in one box, 4,608 bytes apart
+        const uint64_t dims[3] = {d, static_cast<uint64_t>(kBRows), 4};
+        const uint64_t str[2] = {4 * d * 2, d * 2};
+        const uint32_t box[3] = {kChunk, static_cast<uint32_t>(kBRows), 4};
+        if (!encode(&tmB3, a.planes, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+    }
+    if (combined) {
+        {
+            // a compact one-stage pass: the four streams' 64 rows, 4 KB apart
+            const uint64_t dims[3] = {d, n, 4};
+            const uint64_t str[2] = {4 * d * 2, d * 2};
+            const uint32_t box[3] = {kChunk, static_cast<uint32_t>(kFoldRows), 4};
+            if (!encode(&tmX3s, x_in, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+            if (!encode(&tmXo3s, write_x ? a.X_out : a.X, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+        }
+        const uint64_t cs = static_cast<uint64_t>(group) * kChunk * 2;
+        {
+            const uint64_t dims[4] = {d, n, 2, 4};
+            const uint64_t str[3] = {4 * d * 2, cs, d * 2};
+            const uint32_t box[4] = {kChunk, static_cast<uint32_t>(kFoldRows), 2, 4};
+            if (!encode(&tmX4, x_in, 4, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+            if (!encode(&tmXo4, write_x ? a.X_out : a.X, 4, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+        }
+        {
+            const uint64_t dims[3] = {d, n, 2};
+            const uint64_t str[2] = {d * 2, cs};
+            const uint32_t box[3] = {kChunk, static_cast<uint32_t>(kFoldRows), 2};
+            if (!encode(&tmD3, rows, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+            if (!encode(&tmM3, a.stream_mean ? a.stream_mean : rows, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B))
+                return -7;
+        }
+        {
+            const uint64_t dims[4] = {d, static_cast<uint64_t>(kBRows), 2, 4};
+            const uint64_t str[3] = {4 * d * 2, cs, d * 2};
+            const uint32_t box[4] = {kChunk, static_cast<uint32_t>(kBRows), 2, 4};
+            if (!encode(&tmB4, a.planes, 4, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B)) return -7;
+        }
     }
 
     FusedParams p;
@@ -1123,37 +1392,44 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     p.d_slice = a.d / group;
     p.stages_per_tile = p.d_slice / kChunk;
     p.tile_m = tile_m;
+    p.combined = combined ? 1 : 0;
     p.iters = a.iters;
     p.hc_eps = a.hc_eps;
     p.norm_eps = a.norm_eps;
 
     const int64_t grid_groups = std::min<int64_t>(num_tiles, ctas / group);
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident together: the group flags can be awaited
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident together: the group counters can be awaited
     attr[0].val.cooperative = 1;
+    // programmatic dependent launch: the kernel's set-up may overlap the end of the kernel ahead
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(grid_groups * group), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = a.mode == kModePost     ? Layout<kModePost>::kSmemBytes
-                           : a.mode == kModeExpand ? Layout<kModeExpand>::kSmemBytes
-                                                   : Layout<kModePre>::kSmemBytes;
+    cfg.dynamicSmemBytes = a.mode == kModePost     ? smem_of<kModePost>(group)
+                           : a.mode == kModeExpand ? smem_of<kModeExpand>(group)
+                                                   : smem_of<kModePre>(group);
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaErrorInvalidValue;
-    auto go = [&](auto kernel) { e = cudaLaunchKernelEx(&cfg, kernel, tmX, tmD, tmB, tmXo, tmM, tmY, tmYr, p); };
+    auto go = [&](auto kernel) {
+        e = cudaLaunchKernelEx(&cfg, kernel, tmX, tmD, tmB, tmXo, tmM, tmY, tmYr, tmX4, tmXo4, tmD3, tmM3, tmB4, tmX3s,
+                               tmXo3s, tmB3, p);
+    };
     if (a.mode == kModePost) {
-        if (group == 8) go(hc_fused_kernel<kModePost, 8>);
-        else if (group == 16) go(hc_fused_kernel<kModePost, 16>);
-        else go(hc_fused_kernel<kModePost, 32>);
+        if (group == 8) go(hc_fused_kernel<kModePost, 8, fold_of(8)>);
+        else if (group == 16) go(hc_fused_kernel<kModePost, 16, fold_of(16)>);
+        else go(hc_fused_kernel<kModePost, 32, fold_of(32)>);
     } else if (a.mode == kModeExpand) {
-        if (group == 8) go(hc_fused_kernel<kModeExpand, 8>);
-        else if (group == 16) go(hc_fused_kernel<kModeExpand, 16>);
-        else go(hc_fused_kernel<kModeExpand, 32>);
+        if (group == 8) go(hc_fused_kernel<kModeExpand, 8, fold_of(8)>);
+        else if (group == 16) go(hc_fused_kernel<kModeExpand, 16, fold_of(16)>);
+        else go(hc_fused_kernel<kModeExpand, 32, fold_of(32)>);
     } else {
-        if (group == 8) go(hc_fused_kernel<kModePre, 8>);
-        else if (group == 16) go(hc_fused_kernel<kModePre, 16>);
-        else go(hc_fused_kernel<kModePre, 32>);
+        if (group == 8) go(hc_fused_kernel<kModePre, 8, fold_of(8)>);
+        else if (group == 16) go(hc_fused_kernel<kModePre, 16, fold_of(16)>);
+        else go(hc_fused_kernel<kModePre, 32, fold_of(32)>);
     }
     return e == cudaSuccess ? 0 : -7;
 }
@@ -1161,7 +1437,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
 // ---- scratch that needs no allocation ------------------------------------------------------------
 // The workspace of hc_post_then_pre_noalloc: a fixed array in the library's device image, one per
 // GPU that loads the library, zero at load and kept until the process exits. Its size is the same
-// kWorkspaceBytes (7,356,672 bytes: room for 256 co-resident CTAs) that hc_workspace_size reports.
+// kWorkspaceBytes (7,344,384 bytes: room for 256 co-resident CTAs) that hc_workspace_size reports.
 static __device__ __align__(256) unsigned char g_noalloc_workspace[kWorkspaceBytes];
 // A launch never needs more scratch than this: the fused kernel runs at most kMaxCtas CTAs (the
 // device's resident count is capped there) and the generic path works through its tokens in chunks

@@ -99,15 +99,16 @@ int hc_prepare_params(const float* hc_fn, int hc, int d, void* planes, hc_stream
 /* Size in bytes of the workspace the fused calls (hc_pre_step, hc_post_then_pre,
  * hc_post_then_pre_tap, hc_expand_pre_step, hc_debug_mixes) need: the CTAs that share a token tile
  * (8, 16 or 32 of them, as the launch plan of hc_plan_tiles chooses) exchange their per-token
- * partial sums through it (about 14 KB per CTA per tile, L2-resident) together with one 64-bit flag
- * per CTA and tile parity, and one 64-bit launch counter per group slot that tags the flags of each
- * launch (kept on the device, so launches replayed from a CUDA graph are tagged afresh too). It has
- * room for 256 co-resident CTAs: 7,356,672 bytes. The caller allocates it once [device], 16-byte aligned, fills it with zeros before
- * its first use and then keeps passing it unchanged (no re-zeroing needed). Calls that may run at
- * the same time on the GPU must not share a workspace. One exception to "no re-zeroing": after a
- * kernel gave up a bounded wait (HC_ERR_DEVICE, a nonzero hc_device_error word), a CTA that started
- * late may have tagged its flags like the next launch; zero the workspace again before reusing it.
- * Host-only, no CUDA call. */
+ * partial sums through it (about 14 KB per CTA per tile, L2-resident) together with one 64-bit
+ * arrival counter per group of CTAs, which counts the blocks published, and the counter's value at
+ * the start of the group's next launch (both kept on the device, so launches replayed from a CUDA
+ * graph wait for their own arrivals too). It has room for 256 co-resident CTAs: 7,344,384 bytes.
+ * The caller allocates it once [device], 16-byte aligned, fills it with zeros before its first use
+ * and then keeps passing it unchanged (no re-zeroing needed). Calls that may run at the same time on
+ * the GPU must not share a workspace. One exception to "no re-zeroing": after a kernel gave up a
+ * bounded wait (HC_ERR_DEVICE, a nonzero hc_device_error word), the counters may no longer match
+ * (a late CTA may add its arrival after the group moved on); zero the workspace again before reusing
+ * it. Host-only, no CUDA call. */
 int hc_workspace_size(size_t* bytes);
 
 /* Reading half of one sublayer ("Source layer, pairs pooled" page, Block.forward excerpt, the
@@ -160,7 +161,7 @@ int hc_post_then_pre_tap(const void* delta, const void* X, const float* post, co
  * engine that owns all device memory and hands it no workspace, a runtime whose memory plan is
  * frozen after start-up, or a program that must not risk an allocation failing mid-run. This
  * entry point takes the same arguments as hc_post_then_pre minus the workspace, and computes the
- * same results: its scratch is a fixed array inside the library's device image, 7,356,672 bytes
+ * same results: its scratch is a fixed array inside the library's device image, 7,344,384 bytes
  * (the hc_workspace_size figure), which every GPU that loads the library keeps until the process
  * exits. It allocates nothing and calls no allocating routine.
  *   - The first call on a device looks up that device's copy of the array (a runtime query, no
@@ -174,8 +175,8 @@ int hc_post_then_pre_tap(const void* delta, const void* X, const float* post, co
  *     could run at the same time on the GPU (other streams, other threads) race on it and produce
  *     wrong results; serialise them, or use hc_post_then_pre with separate workspaces.
  *   - After a kernel gave up a bounded wait (HC_ERR_DEVICE, a nonzero hc_device_error word), the
- *     array's flags may hold stale tags: hc_device_error with `clear` zeroes the array of the
- *     current device too, so the next call starts afresh.
+ *     array's exchange counters may no longer match: hc_device_error with `clear` zeroes the array
+ *     of the current device too, so the next call starts afresh.
  * The pages have no counterpart to this call: it is a packaging of hc_post_then_pre only. */
 int hc_post_then_pre_noalloc(const void* delta, const void* X, const float* post, const float* comb,
                              const float* pre_mix, hc_params_t next, int64_t n, hc_shape_t s,
@@ -306,10 +307,12 @@ int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, int gr
 /* Launch plan of the fused calls for n tokens of stream width d when `ctas` CTAs of the fused
  * kernel can be resident at once (hc_fused_ctas): the CTAs that share one token tile (`group`: 8,
  * 16 or 32, each taking d/group columns; small batches use larger groups, so each CTA has fewer
- * column stages), the tokens per tile (32, 64, 96 or 128; for batches of several waves possibly
- * the height between 96 and 128 that spreads the tiles evenly over the waves; n itself when
- * n < 32) and the number of tiles. Host-only, no CUDA call. Returns HC_ERR_NULL / HC_ERR_SHAPE (n < 0, d not a positive
- * multiple of 256, ctas < 8) on bad arguments. */
+ * column stages), the tokens per tile and the number of tiles. Groups of 8 take tiles of 32, 64, 96
+ * or 128 tokens (for batches of several waves possibly the height between 96 and 128 that spreads
+ * the tiles evenly over the waves; n itself when n < 32). Groups of 16 and 32 take tiles of 32 or 64
+ * tokens (n itself when n < 32) and process two column stages per pass, in the two halves of the
+ * 128-row tensor-core tile. Host-only, no CUDA call. Returns HC_ERR_NULL / HC_ERR_SHAPE (n < 0, d
+ * not a positive multiple of 256, ctas < 8) on bad arguments. */
 int hc_plan_tiles(int64_t n, int d, int ctas, int* group, int* tile_m, int64_t* num_tiles);
 
 /* How many CTAs of the fused kernel can be resident on the current device at once (one per SM on
@@ -317,9 +320,10 @@ int hc_plan_tiles(int64_t n, int d, int ctas, int* group, int* tile_m, int64_t* 
 int hc_fused_ctas(int* ctas);
 
 /* Diagnostic for the bounded waits: one warp waits, exactly as the fused kernel waits for the other
- * CTAs of its group, for the 64-bit flags[0..count-1] [device] (8-byte aligned, count 1..32) to
- * equal `value`, and gives up after limit_ns (0..1e9) nanoseconds: it then sets the exchange bit of
- * the device error word (hc_device_error) and returns, leaving the context usable. The fused kernel
+ * CTAs of its group, for each of the 64-bit counters flags[0..count-1] [device] (8-byte aligned,
+ * count 1..32) to reach at least `value` (the fused kernel waits on one: its group's arrival
+ * counter), and gives up after limit_ns (0..1e9) nanoseconds: it then sets the exchange bit of the
+ * device error word (hc_device_error) and returns, leaving the context usable. The fused kernel
  * gives up after one second on every wait in the same way. No counterpart on the pages. */
 int hc_debug_wait_flag(const unsigned long long* flags, int count, unsigned long long value, int64_t limit_ns,
                        hc_stream_t stream);

@@ -69,9 +69,9 @@ def _expect(status, fn, *args):
 
 
 def test_workspace_size(lib):
-    # partial sums [256 CTAs][2 parities][28][128] fp32, flags [32 group slots][2][32 ranks] u64,
-    # launch counters [32] u64
-    assert hc.hc_workspace_size() == 256 * 2 * 28 * 128 * 4 + 32 * 2 * 32 * 8 + 32 * 8
+    # partial sums [256 CTAs][2 parities][28][128] fp32, an arrival counter per group slot on its own
+    # 128-byte line [32][16] u64, a base per group slot [32] u64
+    assert hc.hc_workspace_size() == 256 * 2 * 28 * 128 * 4 + 32 * 16 * 8 + 32 * 8 == 7344384
 
 
 def test_pre_step_validation(lib):

@@ -1,7 +1,7 @@
 """Failure detection without a GPU fault: every wait in the library's kernels is bounded, and a wait
 that runs out records a bit in the device error word and returns, leaving the context usable. Here
-a wait is made to run out on exchange flags nothing sets (hc_debug_wait_flag runs the fused
-kernel's own bounded flag wait with a short limit); the host reads the bit, and the same context
+a wait is made to run out on exchange counters nothing advances (hc_debug_wait_flag runs the fused
+kernel's own bounded counter wait with a short limit); the host reads the bit, and the same context
 then runs a normal step correctly.
 """
 
@@ -19,7 +19,7 @@ import gpu_util as gu
 
 pytestmark = pytest.mark.gpu
 
-EXCHANGE_BIT = 64  # the device error word's bit for a wait on the group's flags
+EXCHANGE_BIT = 64  # the device error word's bit for a wait on the group's arrival counter
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -46,6 +46,7 @@ def test_flag_wait_runs_out_and_reports():
 def test_flag_wait_that_is_met_reports_nothing():
     flags = torch.full((8,), 5, dtype=torch.int64, device="cuda")
     hc.hc_debug_wait_flag(flags, 8, 5, 20_000_000)
+    hc.hc_debug_wait_flag(flags, 8, 3, 20_000_000)  # a counter past its target also meets it
     assert hc.hc_device_error(clear=True) == 0
 
 

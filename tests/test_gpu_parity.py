@@ -60,6 +60,20 @@ def test_prepare_params_split_is_exact():
     assert np.array_equal(hi, orc.double_to_bf16(prm["hc_fn"].astype(np.float64)))
 
 
+@pytest.mark.parametrize("n,d,group", [(600, 5120, 32), (1200, 5120, 16), (700, 1024, 32), (300, 5120, 8)])
+def test_debug_mixes_forced_group(n, d, group):
+    """The projection with a forced group size over several tiles per CTA (groups of 16 and 32 fold
+    their tiles; 600 tokens over 4 groups of 32 is 3 tiles per CTA), against the oracle."""
+    w = synth.small("step_b1_t64", 1, n, d, seed=150 + n + group)
+    x = synth.tokens(w, T_X, 0)
+    prm = synth.params(w, 0)
+    P = gu.DevParams(prm, d)
+    m_gpu = gu.host_f32(gu.debug_mixes(gu.dev_bf16(x), P, _shape(w), n, group))
+    m_ref, _, S = orc.hc_mixes(x, prm["hc_fn"], w.norm_eps)
+    gu.assert_mixes_close(m_gpu, m_ref, S)
+    gu.device_error_clear()
+
+
 @pytest.mark.parametrize("n,d", [(1, 5120), (3, 5120), (127, 5120), (300, 5120), (129, 1024), (40, 256)])
 def test_debug_mixes_match_oracle(n, d):
     w = synth.small("step_b1_t64", 1, n, d, seed=100 + n)
@@ -150,11 +164,14 @@ def test_many_tiles_per_group_short_rows(d):
     gu.device_error_clear()
 
 
-@pytest.mark.parametrize("n,d,group,waves", [(100, 1024, 32, 1), (257, 5120, 32, 1), (544, 1024, 16, 1),
-                                             (2468, 2048, 16, 3), (2468, 1024, 8, 2)])
+@pytest.mark.parametrize("n,d,group,waves", [(100, 1024, 16, 1), (257, 5120, 16, 1), (544, 1024, 16, 1),
+                                             (1000, 5120, 16, 2), (256, 5120, 32, 1), (129, 5120, 32, 1),
+                                             (64, 5120, 32, 1), (2468, 2048, 8, 2), (2468, 1024, 8, 2)])
 def test_group_sizes(n, d, group, waves):
     """Every group size the launch plan uses (8, 16 or 32 CTAs per token tile), single and multi-wave,
-    with ragged last tiles."""
+    with ragged last tiles. Groups of 16 and 32 fold their tiles (two column stages per pass): an even
+    stage count (d = 1024 over 16 CTAs: 2 stages, one pass), an odd one whose last pass holds one
+    stage (d = 5120 over 32 CTAs: 5 stages, 3 passes), and several tiles per CTA (1000 tokens)."""
     g, tm, nt = hc.hc_plan_tiles(n, d, hc.hc_fused_ctas())
     assert g == group and -(-nt // (hc.hc_fused_ctas() // g)) == waves, (g, tm, nt)
     w = synth.small("step_b1_t64", 1, n, d, seed=900 + n + d)
