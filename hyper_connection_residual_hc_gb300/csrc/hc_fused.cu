@@ -141,7 +141,9 @@ constexpr int kBarFoldFull = kBarExit + 1, kBarFoldEmpty = kBarExit + 2;
 // kBarNormW: the epilogue warps have put norm_w of the CTA's columns in shared memory (one arrival per
 // epilogue warp; only they read it, long after the stage loop has started)
 constexpr int kBarNormW = kBarExit + 3;
-constexpr int kNumBars = kBarExit + 4;
+// folded tiles alternate between two accumulators: the full and empty barriers of the second
+constexpr int kBarAccFull2 = kBarExit + 4, kBarAccEmpty2 = kBarExit + 5;
+constexpr int kNumBars = kBarExit + 6;
 
 // Shared-memory layout of each mode, offsets from a 1024-byte aligned base. A slot holds one column
 // stage (a folded slot two): the stream tiles (four, or the one embedding tile in expand mode), the
@@ -161,17 +163,32 @@ struct Layout {
     static constexpr int kStage = kOffB + 4 * kBTile;
     static constexpr int kStages = kFold ? (kMode == kModeExpand ? 4 : 2)
                                          : (kMode == kModePost ? 3 : kMode == kModePre ? 4 : 6);
-    static constexpr int kOffNormW = kStages * kStage;
+    // folded post and pre modes: a slot of its own for the compact one-stage pass that ends a tile of
+    // an odd stage count: four 64-row X tiles 4 KB apart, the Delta tile, four plane tiles 4,608 B apart
+    static constexpr bool kHasC = kFold && kMode != kModeExpand;
+    static constexpr int kCOffD = 4 * kFoldXHalf;                  // 16384
+    static constexpr int kCOffB = kCOffD + kFoldXHalf;             // 20480
+    static constexpr int kCSlot = kCOffB + 4 * kBTileBytes;        // 38912
+    static constexpr int kOffC = kStages * kStage;
+    static constexpr int kOffNormW = kOffC + (kHasC ? kCSlot : 0);
     static constexpr int kOffYStage = ((kOffNormW + kMaxDSlice * 4 + 1023) / 1024) * 1024;
     static constexpr int kOffFold = kOffYStage + 4 * 2 * kYStageBytes;
-    static constexpr int kOffBar = kOffFold + (kFold ? kFoldScratchBytes : 0);
+    // the split warp's gather scratch: per owned token (at most 16) its 24 mixes and sum of x^2; then
+    // hc_scale and hc_base (27 floats, 32 reserved)
+    static constexpr int kOffSplit = kOffFold + (kFold ? kFoldScratchBytes : 0);
+    static constexpr int kOffSplitPrm = kOffSplit + (kTileMax / 8) * 7 * 16;
+    static constexpr int kOffBar = kOffSplitPrm + 32 * 4;
     static constexpr int kOffTmemPtr = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemPtr + 4;
     static constexpr int kSmemUsed = kOffAbort + 4;
     static constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
     static_assert(kStage % 1024 == 0, "stage buffers keep 1024-byte alignment");
     static_assert(kOffB % 512 == 0 && kBTileBytes % 512 == 0, "B tiles start on 512-byte swizzle atoms");
-    static_assert(kStages <= kMaxStages, "barrier numbering");
+    static_assert(kStages + (kHasC ? 1 : 0) <= kMaxStages, "barrier numbering");
+    static_assert(kCOffB % 512 == 0 && kCSlot % 1024 == 0, "compact slot on swizzle atoms");
+    // the compact slot's MMA reads past its last X tile (into its Delta and plane tiles) and past its
+    // last plane tile (into norm_w and the staging tiles): inside the CTA's shared memory
+    static_assert(!kHasC || kOffC + kCOffB + 3 * kBTileBytes + kUmmaNFold * 64 <= kSmemUsed, "compact overrun");
     static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in shared memory of one CTA");
     // unfolded: the MMA of the last B tile of the last slot reads 8 rows (512 B) past it: into norm_w,
     // inside the CTA (a folded B tile is exactly the 160 rows its MMA reads)
@@ -208,9 +225,10 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0, kYCol = 80;
 constexpr int kRing = 27;
 static_assert(kYCol + kRing * 16 <= kTmemCols, "y ring fits in TMEM");
-// folded tiles: a 144-column accumulator, then 23 ring slots (a tile has at most 10 folded passes)
-constexpr uint32_t kYColFold = 144;
-constexpr int kRingFold = 23;
+// folded tiles: two 144-column accumulators used in turn (the MMA of a pass need not wait for the
+// previous pass's drain), then 13 ring slots (a folded tile has at most 5 passes)
+constexpr uint32_t kYColFold = 2 * 144;
+constexpr int kRingFold = 13;
 static_assert(kYColFold + kRingFold * 16 <= kTmemCols, "folded y ring fits in TMEM");
 static_assert(kBarYFree == kBarYReady + kRing, "one ready and one free barrier per ring slot");
 
@@ -441,7 +459,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kYColN = kFold ? kYColFold : kYCol;
     constexpr int kOffX = Lay::kOffX, kOffD = Lay::kOffD, kOffB = Lay::kOffB, kOffNormW = Lay::kOffNormW;
     constexpr int kOffYStage = Lay::kOffYStage, kOffBar = Lay::kOffBar, kOffTmemPtr = Lay::kOffTmemPtr;
-    constexpr int kOffAbort = Lay::kOffAbort, kOffFold = Lay::kOffFold;
+    constexpr int kOffAbort = Lay::kOffAbort, kOffFold = Lay::kOffFold, kOffSplit = Lay::kOffSplit;
+    constexpr int kOffSplitPrm = Lay::kOffSplitPrm;
+    constexpr int kNumSlots = kStages + (Lay::kHasC ? 1 : 0);
     constexpr bool kPost = kMode == kModePost;
     constexpr bool kExpand = kMode == kModeExpand;
     constexpr bool kWriteX = kPost || kExpand;  // X' goes back to the streams
@@ -468,13 +488,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto compact = [&](int sp) { return kFold && p.combined && 2 * sp + 1 >= S; };
     auto x_pitch = [&](int sp) -> uint32_t { return compact(sp) ? static_cast<uint32_t>(kFoldXHalf) : kXTileBytes; };
     auto b_pitch = [&](int sp) -> uint32_t { return compact(sp) ? static_cast<uint32_t>(kBTileBytes) : kBTile; };
+    // Shared-memory slot of pass sp of the CTA's tile `it` (the same function in every role). With an
+    // odd stage count in post and pre modes the compact last pass takes the slot after the ring, so
+    // that all passes of a tile can be loaded at once; the other passes take the ring in order.
+    const bool use_c = Lay::kHasC && p.combined && (S & 1) != 0;
+    const int nring = use_c ? SP - 1 : SP;
+    struct Slot {
+        int idx;         // barrier index (kStages: the compact slot)
+        uint32_t base;   // shared-memory address
+        long long round; // how many passes used this slot before
+        uint32_t offd, offb;
+    };
+    auto slot_at = [&](long long it, int sp) -> Slot {
+        Slot r;
+        if (use_c && sp == SP - 1) {
+            r.idx = kStages;
+            r.base = sbase + static_cast<uint32_t>(Lay::kOffC);
+            r.round = it;
+            r.offd = static_cast<uint32_t>(Lay::kCOffD);
+            r.offb = static_cast<uint32_t>(Lay::kCOffB);
+        } else {
+            const long long gr = it * nring + sp;
+            r.idx = static_cast<int>(gr % kStages);
+            r.base = sbase + static_cast<uint32_t>(r.idx) * kStageBytes;
+            r.round = gr / kStages;
+            r.offd = static_cast<uint32_t>(kOffD);
+            r.offb = static_cast<uint32_t>(kOffB);
+        }
+        return r;
+    };
 
     auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
     const Waiter W{abort_flag, kWaitLimitNs};
+    // accumulators: one, or two used in turn when folded (pass g uses g % kNAcc)
+    constexpr int kNAcc = kFold ? 2 : 1;
+    auto acc_full = [&](long long g) { return bar((g % kNAcc) ? kBarAccFull2 : kBarAccFull); };
+    auto acc_empty = [&](long long g) { return bar((g % kNAcc) ? kBarAccEmpty2 : kBarAccEmpty); };
+    auto acc_col = [&](long long g) { return kAccCol + static_cast<uint32_t>((g % kNAcc) * kUmmaNFold); };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kNumSlots; ++s) {
             mbar_init(bar(kBarFull + s), 1);
             mbar_init(bar(kBarXReady + s), kComputeWarps);
             mbar_init(bar(kBarEmpty + s), 2);  // MMA completion + X' store done reading
@@ -494,6 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(kBarFoldFull), 4);
         mbar_init(bar(kBarFoldEmpty), 4);
         mbar_init(bar(kBarNormW), 4);
+        mbar_init(bar(kBarAccFull2), 1);
+        mbar_init(bar(kBarAccEmpty2), kComputeWarps);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -502,11 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // bytes of one column stage; a folded pass loads two (rows 64.. of each tile, plane rows 80..)
     const uint32_t stage_bytes =
         static_cast<uint32_t>((kExpand ? 1 : 4) * p.tile_m * 64 + (kPost ? p.tile_m * 64 : 0) + 4 * kBTileBytes);
-    // one thread: the TMA loads of pass s of the tile starting at token t0 into the slot of pass g
-    auto issue_pass = [&](long long g, int s, int t0, uint64_t pol_stream, uint64_t pol_keep) {
-        const int slot = static_cast<int>(g % kStages);
-        const uint32_t sb = sbase + slot * kStageBytes;
-        const uint32_t fb = bar(kBarFull + slot);
+    // one thread: the TMA loads of pass s of the tile starting at token t0 into slot sl
+    auto issue_pass = [&](const Slot& sl, int s, int t0, uint64_t pol_stream, uint64_t pol_keep) {
+        const uint32_t sb = sl.base;
+        const uint32_t fb = bar(kBarFull + sl.idx);
         const int halves = (kFold && 2 * s + 1 < S) ? 2 : 1;
         mbar_arrive_expect_tx(fb, stage_bytes * static_cast<uint32_t>(halves));
         if (kFold && halves == 2 && p.combined) {
@@ -525,8 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(sb + kOffX, &tmD, fb, col, t0, pol_stream);
             else
                 tma_load_3d(sb + kOffX, &tmX3s, fb, col, t0, 0, pol_stream);
-            if (kPost) tma_load_2d(sb + kOffD, &tmD, fb, col, t0, pol_stream);
-            tma_load_3d(sb + kOffB, &tmB3, fb, col, 0, 0, pol_keep);
+            if (kPost) tma_load_2d(sb + sl.offd, &tmD, fb, col, t0, pol_stream);
+            tma_load_3d(sb + sl.offb, &tmB3, fb, col, 0, 0, pol_keep);
             return;
         }
         for (int hf = 0; hf < halves; ++hf) {
@@ -553,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the passes of the first tile that fill the empty slots: issued as soon as the kernel ahead has
     // completed, by the thread that initialised the barriers and before the CTA-wide barrier below
     // (the producer warp skips them)
-    const int early = my_tiles > 0 ? (SP < kStages ? SP : kStages) : 0;
+    auto early = [&](long long it, int sp) { return my_tiles > 0 && it == 0 && sp < nring && sp < kStages; };
     if (warp == kWarpProducer && lane == 0) {
         tma_prefetch_desc(&tmX);
         tma_prefetch_desc(&tmB);
@@ -579,7 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the streamed tiles (X, Delta) keep the normal L2 policy: evict_first dropped the unused
         // half of each 128-byte line and re-read it (356 MB more per prefill step)
         const uint64_t pol_stream = policy_evict_normal(), pol_keep = policy_evict_last();
-        for (int s = 0; s < early; ++s) issue_pass(s, s, static_cast<int>(cid * p.tile_m), pol_stream, pol_keep);
+        for (int s = 0; s < SP; ++s)
+            if (early(0, s)) issue_pass(slot_at(0, s), s, static_cast<int>(cid * p.tile_m), pol_stream, pol_keep);
     }
     tc_fence_before();
     __syncthreads();
@@ -646,11 +702,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // drain pass gd's accumulator (the three planes added back together) into acc; a folded
             // pass with no stage for these rows is waited for and released but not added
             auto drain = [&](long long gd, bool add) {
-                W.wait(bar(kBarAccFull), static_cast<uint32_t>(gd & 1), kErrComputeAcc);
+                W.wait(acc_full(gd), static_cast<uint32_t>((gd / kNAcc) & 1), kErrComputeAcc);
                 tc_fence_after();
                 if (add) {
                     uint32_t v[36];
-                    const uint32_t col = kAccCol + (sub ? static_cast<uint32_t>(kFoldBRow1) : 0u) + 36u * h;
+                    const uint32_t col = acc_col(gd) + (sub ? static_cast<uint32_t>(kFoldBRow1) : 0u) + 36u * h;
                     tmem_ld36_wait(tl + col, tl + col + 32u, v);
                     auto f2 = [&](int i) { return make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])); };
 #pragma unroll
@@ -659,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kBarAccEmpty));
+                if (lane == 0) mbar_arrive(acc_empty(gd));
             };
 
             for (int s = 0; s < SP; ++s, ++g) {
@@ -673,10 +729,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (yround > 0)
                     W.wait(bar(kBarYFree + static_cast<int>(g % kRingN)), static_cast<uint32_t>((yround - 1) & 1),
                            kErrComputeY);
-                const int slot = static_cast<int>(g % kStages);
-                const uint32_t par = static_cast<uint32_t>((g / kStages) & 1);
-                W.wait(bar(kBarFull + slot), par, kErrComputeFull);
-                const uint32_t sb = sbase + slot * kStageBytes;
+                const Slot sl = slot_at(it, s);
+                W.wait(bar(kBarFull + sl.idx), static_cast<uint32_t>(sl.round & 1), kErrComputeFull);
+                const uint32_t sb = sl.base;
+                const uint32_t offd = sl.offd;
                 const bool here = pass_ok(s);  // warp-uniform
                 const uint32_t xp = x_pitch(s);  // bytes between the streams' tiles in this pass
                 uint32_t yb[8];
@@ -699,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (kPost) {
                         // X'_k = post_k * Delta + sum_j comb[j,k] X_j, in this order for every column
                         float2 dl[4], xf[4][4];
-                        unpack4(ld_smem_v4(sb + kOffD + off), dl);
+                        unpack4(ld_smem_v4(sb + offd + off), dl);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) unpack4(xv[j], xf[j]);
 #pragma unroll
@@ -728,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 float2 t = __fadd2_rn(__fadd2_rn(__fadd2_rn(xr[0][e], xr[1][e]), xr[2][e]), xr[3][e]);
                                 o[e] = pack_bf16(__fmul2_rn(t, bcast(0.25f)));
                             }
-                            st_smem_v4(sb + kOffD + off, make_uint4(o[0], o[1], o[2], o[3]));
+                            st_smem_v4(sb + offd + off, make_uint4(o[0], o[1], o[2], o[3]));
                         }
                     } else {
 #pragma unroll
@@ -755,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (kPost) fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kBarXReady + slot));
+                if (lane == 0) mbar_arrive(bar(kBarXReady + sl.idx));
                 // drain the previous pass's accumulator now: its MMA ran while this pass was
                 // computed, so nothing waits here, and the MMA of this pass (which needs the
                 // accumulator empty) is issued right after
@@ -904,49 +960,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             pol_stream = policy_evict_normal();
             pol_keep = policy_evict_last();
         }
-        long long g = 0;
+        long long last_round[kMaxStages];  // the latest pass loaded into each slot
+#pragma unroll
+        for (int i = 0; i < kMaxStages; ++i) last_round[i] = -1;
         for (long long it = 0; it < my_tiles; ++it) {
             const long long tile = cid + it * ncl;
             const int t0 = static_cast<int>(tile * p.tile_m);
-            for (int s = 0; s < SP; ++s, ++g) {
-                if (g < early) continue;  // issued at the start
-                const int slot = static_cast<int>(g % kStages);
-                const long long round = g / kStages;
-                if (round > 0) W.wait(bar(kBarEmpty + slot), static_cast<uint32_t>((round - 1) & 1), kErrProducer);
-                if (lane == 0) issue_pass(g, s, t0, pol_stream, pol_keep);
+            for (int s = 0; s < SP; ++s) {
+                const Slot sl = slot_at(it, s);
+                last_round[sl.idx] = sl.round;
+                if (early(it, s)) continue;  // issued at the start
+                if (sl.round > 0)
+                    W.wait(bar(kBarEmpty + sl.idx), static_cast<uint32_t>((sl.round - 1) & 1), kErrProducer);
+                if (lane == 0) issue_pass(sl, s, t0, pol_stream, pol_keep);
                 __syncwarp();
             }
         }
-        // let every load issued land before the CTA can exit
-        const long long issued = g;
-        for (long long gg = (issued > kStages ? issued - kStages : 0); gg < issued; ++gg)
-            W.drain(bar(kBarFull + static_cast<int>(gg % kStages)), static_cast<uint32_t>((gg / kStages) & 1));
+        // let every load issued land before the CTA can exit (a slot's latest load lands after its
+        // earlier ones, which the compute warps consumed before the slot was reused)
+#pragma unroll
+        for (int i = 0; i < kMaxStages; ++i)
+            if (i < kNumSlots && last_round[i] >= 0) W.drain(bar(kBarFull + i), static_cast<uint32_t>(last_round[i] & 1));
     } else if (warp == kWarpMma) {
         // ================= MMA issuer ===========================================================
         constexpr uint32_t idesc = idesc_bf16_f32(kUmmaM, kFold ? kUmmaNFold : kUmmaN);
         long long g = 0;
         for (long long it = 0; it < my_tiles; ++it) {
             for (int s = 0; s < SP; ++s, ++g) {
-                const int slot = static_cast<int>(g % kStages);
-                // the single accumulator must have been drained (stage g - 1)
-                if (g > 0) W.wait(bar(kBarAccEmpty), static_cast<uint32_t>((g - 1) & 1), kErrMma);
+                const Slot sl = slot_at(it, s);
+                // this pass's accumulator must have been drained (pass g - kNAcc)
+                if (g >= kNAcc) W.wait(acc_empty(g), static_cast<uint32_t>((g / kNAcc - 1) & 1), kErrMma);
                 // post mode multiplies the X' the compute warps wrote; the other modes the loaded tile
-                W.wait(bar((kPost ? kBarXReady : kBarFull) + slot), static_cast<uint32_t>((g / kStages) & 1), kErrMma);
+                W.wait(bar((kPost ? kBarXReady : kBarFull) + sl.idx), static_cast<uint32_t>(sl.round & 1), kErrMma);
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t sb = sbase + slot * kStageBytes;
-                    const uint32_t dcol = tmem + kAccCol;
+                    const uint32_t sb = sl.base;
+                    const uint32_t dcol = tmem + acc_col(g);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             const uint64_t ad = sdesc_kmajor_sw64(sb + kOffX + (kExpand ? 0 : k * x_pitch(s)) + kk * 32);
-                            const uint64_t bd = sdesc_kmajor_sw64(sb + kOffB + k * b_pitch(s) + kk * 32);
+                            const uint64_t bd = sdesc_kmajor_sw64(sb + sl.offb + k * b_pitch(s) + kk * 32);
                             umma_bf16(dcol, ad, bd, idesc, (k | kk) != 0 ? 1u : 0u);
                         }
                     }
-                    umma_commit(bar(kBarEmpty + slot));
-                    umma_commit(bar(kBarAccFull));
+                    umma_commit(bar(kBarEmpty + sl.idx));
+                    umma_commit(acc_full(g));
                 }
                 __syncwarp();
             }
@@ -963,18 +1023,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long tile = cid + it * ncl;
             const int t0 = static_cast<int>(tile * p.tile_m);
             for (int s = 0; s < SP; ++s, ++g) {
-                const int slot = static_cast<int>(g % kStages);
-                W.wait(bar(kBarXReady + slot), static_cast<uint32_t>((g / kStages) & 1), kErrStore);
+                const Slot sl = slot_at(it, s);
+                W.wait(bar(kBarXReady + sl.idx), static_cast<uint32_t>(sl.round & 1), kErrStore);
                 if (kWriteX && lane == 0) {
-                    const uint32_t sb = sbase + slot * kStageBytes;
+                    const uint32_t sb = sl.base;
                     const int halves = (kFold && 2 * s + 1 < S) ? 2 : 1;
                     if (kPost && halves == 2 && p.combined) {
                         // both stages of the four streams in one box, the tap's two in another
                         tma_store_4d(&tmXo4, sb + kOffX, stage_col(2 * s), t0, 0, 0);
-                        if (p.stream_mean) tma_store_3d(&tmM3, sb + kOffD, stage_col(2 * s), t0, 0);
+                        if (p.stream_mean) tma_store_3d(&tmM3, sb + sl.offd, stage_col(2 * s), t0, 0);
                     } else if (kPost && compact(s)) {
                         tma_store_3d(&tmXo3s, sb + kOffX, stage_col(2 * s), t0, 0);  // the compact tiles
-                        if (p.stream_mean) tma_store_2d(&tmM, sb + kOffD, stage_col(2 * s), t0);
+                        if (p.stream_mean) tma_store_2d(&tmM, sb + sl.offd, stage_col(2 * s), t0);
                     } else {
                         for (int hf = 0; hf < halves; ++hf) {
                             const int col = stage_col(kFold ? 2 * s + hf : s);
@@ -982,24 +1042,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
                                 tma_store_3d(&tmXo, sb + kOffX + (kExpand ? 0 : k * kXTileBytes) + xo, col, k, t0);
-                            if (kPost && p.stream_mean) tma_store_2d(&tmM, sb + kOffD + xo, col, t0);  // the tap
+                            if (kPost && p.stream_mean) tma_store_2d(&tmM, sb + sl.offd + xo, col, t0);  // the tap
                         }
                     }
                     bulk_commit();
                     bulk_wait_read<0>();
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kBarEmpty + slot));
+                if (lane == 0) mbar_arrive(bar(kBarEmpty + sl.idx));
             }
         }
         if (lane == 0) bulk_wait<0>();
     } else {  // warp == kWarpSplit
         // ===== group exchange, r_y of every row, split + Sinkhorn for this CTA's share ==========
-        float sc[3], bs[kMix];
-#pragma unroll
-        for (int i = 0; i < 3; ++i) sc[i] = __ldg(p.hc_scale + i);
-#pragma unroll
-        for (int i = 0; i < kMix; ++i) bs[i] = __ldg(p.hc_base + i);
+        // hc_scale and hc_base into shared memory now, read from there by each split (not held in
+        // registers through the gather)
+        float* prm = reinterpret_cast<float*>(smem + kOffSplitPrm);
+        if (lane < 3) prm[lane] = __ldg(p.hc_scale + lane);
+        if (lane < kMix) prm[3 + lane] = __ldg(p.hc_base + lane);
+        __syncwarp();
         // the group's arrival counter and its value when this launch started
         unsigned long long* arrivals = p.ws_flags + static_cast<size_t>(cid) * kCounterStride;
         unsigned long long base = 0;
@@ -1024,67 +1085,77 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long tile = cid + it * ncl;
             const long long t0 = tile * p.tile_m;
             const float* blk = p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kG) * kPartFloats;
-            // the owned tokens t = rank + kG i (i < kT = 128 / kG). The kParts = 32 / kT lanes of token
-            // i (lane = part * kT + i) each sum the token's 24 mixes and sum x^2 over kG / kParts = 4
-            // of the group's blocks (shares part, part + kParts, ...: every load in flight at once);
-            // a reduce-scatter across those lanes then leaves lane `part` with mixes part * kMP ..
-            // part * kMP + kMP - 1 summed over all kG blocks, and an all-reduce gives each the sum x^2
-            constexpr int kT = kTileMax / kG, kParts = 32 / kT, kMP = kMix / kParts;
-            constexpr int kShares = kG / kParts, kLog = kParts == 8 ? 3 : kParts == 4 ? 2 : 1;
-            static_assert(kShares * kParts == kG && (1 << kLog) == kParts, "gather split");
-            const int oi = lane % kT, part = lane / kT;
-            const int r_tok = static_cast<int>(rank) + kG * oi;
-            const bool mine = r_tok < p.tile_m && t0 + r_tok < p.n;
-            float c[kMix];
+            // the owned tokens t = rank + kG i (i < kT = 128 / kG, the first kTv of them in the tile). One
+            // load instruction of the warp covers four shares' rows of one token: lane 4q + j (q < 6)
+            // loads float4 q of the token's 24 mixes and lane 24 + j its two sums of x^2, from shares
+            // j, j + 4, j + 8, ... (about four 128-byte lines per instruction, where one lane per share
+            // and token scattered the loads over 16 to 32 lines). Each lane sums its shares in order, two
+            // shuffle levels add the four phases, and the token's 24 mixes and sum of x^2 go through the
+            // warp's shared-memory scratch to lane i, which runs the token's split. kBatch tokens' loads
+            // are in flight at once (kBatch * kG / 4 = 16 per lane).
+            constexpr int kT = kTileMax / kG, kPhases = 4, kPerPhase = kG / kPhases, kBatch = 64 / kG;
+            static_assert(kBatch * kPerPhase == 16 && kT % kBatch == 0, "gather batches");
+            int kTv = 0;  // owned tokens in this tile
+            for (int i = 0; i < kT; ++i)
+                if (static_cast<int>(rank) + kG * i < p.tile_m && t0 + rank + kG * i < p.n) kTv = i + 1;
+            const int gq = lane >> 2, gj = lane & 3;  // float4 index (6: the sums of x^2), phase
+            float* scr = reinterpret_cast<float*>(smem + kOffSplit);
+            for (int i0 = 0; i0 < kTv; i0 += kBatch) {
+                float4 u[kBatch][kPerPhase];
 #pragma unroll
-            for (int i = 0; i < kMix; ++i) c[i] = 0.f;
+                for (int b = 0; b < kBatch; ++b) {
+                    const int tok_row = static_cast<int>(rank) + kG * (i0 + b);
+#pragma unroll
+                    for (int m = 0; m < kPerPhase; ++m) {
+                        u[b][m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (i0 + b < kTv && lane < 28) {
+                            const float* Pr = blk + static_cast<size_t>(kPhases * m + gj) * kPartFloats;
+                            if (gq < 6) {
+                                u[b][m] = ld_cg_f4(Pr + tok_row * kMix + 4 * gq);
+                            } else {
+                                const float2 v = ld_cg_f2(Pr + kPartSx + 2 * tok_row);
+                                u[b][m] = make_float4(v.x, v.y, 0.f, 0.f);
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                    float4 a = u[b][0];
+#pragma unroll
+                    for (int m = 1; m < kPerPhase; ++m) {
+                        a.x += u[b][m].x; a.y += u[b][m].y; a.z += u[b][m].z; a.w += u[b][m].w;
+                    }
+#pragma unroll
+                    for (int x = 1; x <= 2; x <<= 1) {
+                        a.x += __shfl_xor_sync(0xffffffffu, a.x, x);
+                        a.y += __shfl_xor_sync(0xffffffffu, a.y, x);
+                        a.z += __shfl_xor_sync(0xffffffffu, a.z, x);
+                        a.w += __shfl_xor_sync(0xffffffffu, a.w, x);
+                    }
+                    if (gj == 0 && lane < 28 && i0 + b < kTv)
+                        reinterpret_cast<float4*>(scr)[(i0 + b) * 7 + gq] =
+                            gq < 6 ? a : make_float4(a.x + a.y, 0.f, 0.f, 0.f);
+                }
+            }
+            __syncwarp();
+            const int oi = lane;  // lane i runs the split of owned token i
+            const int r_tok = static_cast<int>(rank) + kG * oi;
+            const bool mine = oi < kTv;
+            float m[kMix];
             float sxt = 0.f;
             if (mine) {
-                float4 u[kShares][kMix / 4];
-                float2 sxr[kShares];
+                const float4* sv = reinterpret_cast<const float4*>(scr) + oi * 7;
 #pragma unroll
-                for (int j = 0; j < kShares; ++j) {
-                    const float* Pr = blk + static_cast<size_t>(part + kParts * j) * kPartFloats;
-#pragma unroll
-                    for (int q = 0; q < kMix / 4; ++q) u[j][q] = ld_cg_f4(Pr + r_tok * kMix + 4 * q);
-                    sxr[j] = ld_cg_f2(Pr + kPartSx + 2 * r_tok);
+                for (int k = 0; k < 6; ++k) {
+                    const float4 v = sv[k];
+                    m[4 * k] = v.x; m[4 * k + 1] = v.y; m[4 * k + 2] = v.z; m[4 * k + 3] = v.w;
                 }
-#pragma unroll
-                for (int j = 0; j < kShares; ++j) {
-#pragma unroll
-                    for (int q = 0; q < kMix / 4; ++q) {
-                        c[4 * q] += u[j][q].x; c[4 * q + 1] += u[j][q].y;
-                        c[4 * q + 2] += u[j][q].z; c[4 * q + 3] += u[j][q].w;
-                    }
-                    sxt += sxr[j].x + sxr[j].y;
-                }
+                sxt = sv[6].x;
             }
-            // reduce-scatter: at level l the lanes split by bit (kLog - 1 - l) of `part`, each keeping
-            // one half of its current span and adding the partner's copy of that half
-#pragma unroll
-            for (int l = 0; l < kLog; ++l) {
-                const int half = (kMix >> l) / 2;
-                const int mask = kT << (kLog - 1 - l);
-                const bool upper = (lane & mask) != 0;
-#pragma unroll
-                for (int i = 0; i < half; ++i) {
-                    const float send = upper ? c[i] : c[i + half];
-                    const float keep = upper ? c[i + half] : c[i];
-                    c[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-                }
-            }
-#pragma unroll
-            for (int l = 0; l < kLog; ++l) sxt += __shfl_xor_sync(0xffffffffu, sxt, kT << l);
-            const float* v = c;  // this lane's kMP mixes
-            float m[kMix];
-#pragma unroll
-            for (int q = 0; q < kParts; ++q)
-#pragma unroll
-                for (int i = 0; i < kMP; ++i) m[q * kMP + i] = __shfl_sync(0xffffffffu, v[i], q * kT + oi);
-            const bool oh = part != 0;
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarSplitDone));  // the blocks of this tile may be reused
-            if (mine && oh == 0) {
+            if (mine) {
                 const long long tok = t0 + r_tok;
                 const float rr = rsqrtf(sxt / static_cast<float>(4 * p.d) + p.norm_eps);  // rsqrt of mean(x^2) + eps
 #pragma unroll
@@ -1096,6 +1167,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (p.pre_out) {
                     float pre[4], post[4], C[16];
+                    float sc[3], bs[kMix];
+#pragma unroll
+                    for (int i = 0; i < 3; ++i) sc[i] = prm[i];
+#pragma unroll
+                    for (int i = 0; i < kMix; ++i) bs[i] = prm[3 + i];
                     split_sinkhorn(m, sc, bs, p.iters, p.hc_eps, pre, post, C);
                     reinterpret_cast<float4*>(p.pre_out)[tok] = make_float4(pre[0], pre[1], pre[2], pre[3]);
                     reinterpret_cast<float4*>(p.post_out)[tok] = make_float4(post[0], post[1], post[2], post[3]);
@@ -1226,18 +1302,18 @@ int prepare_device(int* ctas) {
 // groups run at once; a launch takes ceil(tiles / groups) waves, each of P passes over a tile plus
 // a per-tile cost (group exchange, y_normed epilogue tail). Groups of 8 take tiles of 32, 64, 96 or
 // 128 tokens (or a balanced height of 96..128 for batches of several waves, or n when n < 32) and
-// make one pass per column stage, P = S = d / (32 g). Groups of 16 and 32 fold: tiles of 32 or 64
-// tokens (or n when n < 32), two column stages per pass in the 128 rows of the MMA, P = ceil(S / 2).
-// A pass costs the larger of its latency floor and a fixed part plus a part per row in use; the
-// constants were measured on GB300 (2.1 us per 128-row pass of the prefill step, about 0.8 us for
-// a pass of a small batch, 1.3 us for a folded pass of a decode batch, about 4 us per tile).
+// make one pass per column stage, P = S = d / (32 g). Groups of 16 and 32 fold: tiles of 64 tokens,
+// two column stages per pass in the 128 rows of the MMA, P = ceil(S / 2), every pass loaded with one
+// box per tensor (a folded pass costs the same whatever the tokens of its tile).
+// A pass costs the larger of its latency floor and a fixed part plus a part per row in use (a folded
+// pass uses all 128 rows); the constants were measured on GB300 (2.1 us per 128-row pass of the
+// prefill step, about 0.8 us for a pass of a small batch, about 4 us per tile).
 void plan_tiles(int64_t n, int d, int ctas, int only_group, int* group, int* tile_m, int64_t* num_tiles) {
     *group = 8;
     *tile_m = kTileMax;
     *num_tiles = 0;
     if (n <= 0) return;
-    constexpr double kPassFloorUs = 0.8, kFoldFloorUs = 1.3, kPassFixedUs = 0.5, kPassPerRowUs = 1.6 / kTileMax,
-                     kTileUs = 4.0;
+    constexpr double kPassFloorUs = 0.8, kPassFixedUs = 0.5, kPassPerRowUs = 1.6 / kTileMax, kTileUs = 4.0;
     double best = -1.0;
     const int gs[3] = {8, 16, 32};
     for (int g : gs) {
@@ -1254,14 +1330,15 @@ void plan_tiles(int64_t n, int d, int ctas, int only_group, int* group, int* til
         // stage's time still follows its rows (shorter balanced tiles measured slower)
         const int64_t waves128 = ((n + kTileMax - 1) / kTileMax + groups - 1) / groups;
         const int m_even = static_cast<int>((n + groups * waves128 - 1) / (groups * waves128));
-        const int ms[6] = {fold ? 0 : 128, fold ? 0 : 96, 64, 32, n < 32 ? static_cast<int>(n) : 0,
+        const int ms[6] = {fold ? 0 : 128, fold ? 0 : 96, 64, fold ? 0 : 32, !fold && n < 32 ? static_cast<int>(n) : 0,
                            !fold && waves128 > 1 && m_even >= 96 ? m_even : 0};
         for (int m : ms) {
             if (m < 1) continue;
             const int64_t tiles = (n + m - 1) / m;
             const int64_t waves = (tiles + groups - 1) / groups;
-            const int rows = fold && S > 1 ? 2 * m : m;
-            const double pass = std::max(fold ? kFoldFloorUs : kPassFloorUs, kPassFixedUs + rows * kPassPerRowUs);
+            // a folded pass runs all 128 rows of the tile in every compute warp
+            const int rows = fold ? kTileMax : m;
+            const double pass = std::max(kPassFloorUs, kPassFixedUs + rows * kPassPerRowUs);
             const double cost = static_cast<double>(waves) * (P * pass + kTileUs);
             if (best < 0.0 || cost < best - 1e-9) {
                 best = cost;

@@ -309,9 +309,8 @@ int hc_debug_mixes(const void* X, hc_params_t p, int64_t n, hc_shape_t s, int gr
  * 16 or 32, each taking d/group columns; small batches use larger groups, so each CTA has fewer
  * column stages), the tokens per tile and the number of tiles. Groups of 8 take tiles of 32, 64, 96
  * or 128 tokens (for batches of several waves possibly the height between 96 and 128 that spreads
- * the tiles evenly over the waves; n itself when n < 32). Groups of 16 and 32 take tiles of 32 or 64
- * tokens (n itself when n < 32) and process two column stages per pass, in the two halves of the
- * 128-row tensor-core tile. Host-only, no CUDA call. Returns HC_ERR_NULL / HC_ERR_SHAPE (n < 0, d
+ * the tiles evenly over the waves; n itself when n < 32). Groups of 16 and 32 take tiles of 64 tokens
+ * and process two column stages per pass, in the two halves of the 128-row tensor-core tile. Host-only, no CUDA call. Returns HC_ERR_NULL / HC_ERR_SHAPE (n < 0, d
  * not a positive multiple of 256, ctas < 8) on bad arguments. */
 int hc_plan_tiles(int64_t n, int d, int ctas, int* group, int* tile_m, int64_t* num_tiles);
 
