@@ -77,7 +77,13 @@ typedef struct {
 
 /* One sublayer's HC parameters ("Source layer, pairs pooled" page, Block.__init__ excerpt:
  * hc_fn [mix_hc, hc*d], hc_base [mix_hc], hc_scale [3], mix_hc = (2+hc)*hc; the sublayer's
- * RMSNorm weight [d]). All [device]. */
+ * RMSNorm weight [d]). All [device].
+ * The projection weights come as the planes hc_prepare_params makes from the fp32 hc_fn, not as
+ * hc_fn itself: the split is done once per parameter set instead of in every call, and the planes
+ * are laid out for the kernel's loads. The caller guarantees that the planes were prepared with
+ * the (hc, d) of the call's hc_shape_t and from the hc_fn in use. A device buffer carries neither
+ * its size nor its source, so the library cannot check this: planes of another shape are read out
+ * of bounds, and planes of an older hc_fn give that hc_fn's mixes. */
 typedef struct {
     const void* hc_fn_planes; /* bf16 [3*mix_hc, hc*d]: hc_fn split by hc_prepare_params. Required. */
     const float* hc_scale;    /* fp32 [3] */
