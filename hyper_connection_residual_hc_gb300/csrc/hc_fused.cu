@@ -662,13 +662,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarYReady + static_cast<int>(gy % kRingN)));
         };
-        for (long long it = 0; it < my_tiles; ++it) {
-            const long long tile = cid + it * ncl;
-            const long long t0 = tile * p.tile_m;
-            const long long tok = t0 + trow;
+        // this token's coefficients of the current tile, each broadcast to both lanes of a float2
+        float2 cpost[4], ccomb[16], pm[4];
+        auto load_coefs = [&](long long it) {
+            const long long tok = (cid + it * ncl) * p.tile_m + trow;
             const bool valid = (trow < p.tile_m) && (tok < p.n);
-            // this token's coefficients, each broadcast to both lanes of a float2
-            float2 cpost[4], ccomb[16], pm[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) cpost[i] = pm[i] = bcast(0.f);
 #pragma unroll
@@ -691,6 +689,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+        };
+        if (my_tiles > 0) load_coefs(0);
+        for (long long it = 0; it < my_tiles; ++it) {
             float2 acc[6];  // the 12 mixes of this thread's column half, in pairs
 #pragma unroll
             for (int i = 0; i < 6; ++i) acc[i] = bcast(0.f);
@@ -819,6 +820,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             drain(g - 1, pass_ok(SP - 1));
             y_ready(g - 1);
+            // the next tile's coefficients, loaded now (this tile's are no longer read) so that their
+            // latency passes while the partial sums below are written and published: the publishing
+            // arrive waits for this thread's stores, and the next tile's first pass would wait for
+            // these loads
+            if (it + 1 < my_tiles) load_coefs(it + 1);
 
             // publish this CTA's partial sums of the tile to the group; the split warp collects them.
             // The block of tile it reuses that of tile it - 2, which the other CTAs of the group may
