@@ -143,7 +143,10 @@ constexpr int kBarFoldFull = kBarExit + 1, kBarFoldEmpty = kBarExit + 2;
 constexpr int kBarNormW = kBarExit + 3;
 // folded tiles alternate between two accumulators: the full and empty barriers of the second
 constexpr int kBarAccFull2 = kBarExit + 4, kBarAccEmpty2 = kBarExit + 5;
-constexpr int kNumBars = kBarExit + 6;
+// kBarPartEmpty: the split warp has copied a tile's partial sums out of their shared-memory block
+// (unfolded post and expand modes, one arrival per tile)
+constexpr int kBarPartEmpty = kBarExit + 6;
+constexpr int kNumBars = kBarExit + 7;
 
 // Shared-memory layout of each mode, offsets from a 1024-byte aligned base. A slot holds one column
 // stage (a folded slot two): the stream tiles (four, or the one embedding tile in expand mode), the
@@ -177,7 +180,13 @@ struct Layout {
     // hc_scale and hc_base (27 floats, 32 reserved)
     static constexpr int kOffSplit = kOffFold + (kFold ? kFoldScratchBytes : 0);
     static constexpr int kOffSplitPrm = kOffSplit + (kTileMax / 8) * 7 * 16;
-    static constexpr int kOffBar = kOffSplitPrm + 32 * 4;
+    // unfolded post and expand tiles hand their partial sums to the split warp in a shared-memory block
+    // (the split warp writes them to the workspace). Pre mode has no room for the block; holding the
+    // tile's last slot for it instead measured slower (152 -> 154 us at the prefill batch), as did
+    // publishing a tile one pass late, so its compute warps write the workspace themselves
+    static constexpr bool kPartInSmem = !kFold && kMode != kModePre;
+    static constexpr int kOffPart = kOffSplitPrm + 32 * 4;
+    static constexpr int kOffBar = kOffPart + (kPartInSmem ? kPartFloats * 4 : 0);
     static constexpr int kOffTmemPtr = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemPtr + 4;
     static constexpr int kSmemUsed = kOffAbort + 4;
@@ -195,6 +204,7 @@ struct Layout {
     static_assert(kOffB + 3 * kBTile + (kFold ? kUmmaNFold : kUmmaN) * 64 + (kStages - 1) * kStage <= kSmemUsed,
                   "B overrun");
     static_assert(kFoldXHalf % 512 == 0 && (kFoldBRow1 * 64) % 512 == 0, "second stage on swizzle atoms");
+    static_assert(kOffPart % 16 == 0, "partial-sum block: 16-byte aligned");
 };
 
 // global workspace: partial sums [group][tile parity][rank][28][128] fp32 (a block per CTA and
@@ -460,7 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kOffX = Lay::kOffX, kOffD = Lay::kOffD, kOffB = Lay::kOffB, kOffNormW = Lay::kOffNormW;
     constexpr int kOffYStage = Lay::kOffYStage, kOffBar = Lay::kOffBar, kOffTmemPtr = Lay::kOffTmemPtr;
     constexpr int kOffAbort = Lay::kOffAbort, kOffFold = Lay::kOffFold, kOffSplit = Lay::kOffSplit;
-    constexpr int kOffSplitPrm = Lay::kOffSplitPrm;
+    constexpr int kOffSplitPrm = Lay::kOffSplitPrm, kOffPart = Lay::kOffPart;
+    constexpr bool kPartInSmem = Lay::kPartInSmem;
     constexpr int kNumSlots = kStages + (Lay::kHasC ? 1 : 0);
     constexpr bool kPost = kMode == kModePost;
     constexpr bool kExpand = kMode == kModeExpand;
@@ -550,6 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(kBarNormW), 4);
         mbar_init(bar(kBarAccFull2), 1);
         mbar_init(bar(kBarAccEmpty2), kComputeWarps);
+        mbar_init(bar(kBarPartEmpty), 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -863,9 +875,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarFoldEmpty));
             }
-            if (it > 0) W.wait(bar(kBarSplitDone), static_cast<uint32_t>((it - 1) & 1), kErrExchange);
-            const int buf = static_cast<int>(it & 1);
-            float* P = p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kG + rank) * kPartFloats;
+            float* P;
+            if constexpr (kPartInSmem) {
+                // into shared memory; the split warp writes the block to the workspace, so the arrive
+                // below has no global stores to wait for (a memory round trip per tile otherwise)
+                if (it > 0) W.wait(bar(kBarPartEmpty), static_cast<uint32_t>((it - 1) & 1), kErrComputeAcc);
+                P = reinterpret_cast<float*>(smem + kOffPart);
+            } else {
+                if (it > 0) W.wait(bar(kBarSplitDone), static_cast<uint32_t>((it - 1) & 1), kErrExchange);
+                P = p.ws_part + (static_cast<size_t>(cid * 2 + static_cast<int>(it & 1)) * kG + rank) * kPartFloats;
+            }
             {
                 float4* pm4 = reinterpret_cast<float4*>(P + trow * kMix + 12 * h);
                 pm4[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
@@ -1081,8 +1100,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             // tile (whose buffer the group reuses after this tile): the split warp read them in its
             // last iteration, the epilogue warps read the sums of y^2
             if (it >= 1) W.wait(bar(kBarEpiRead), static_cast<uint32_t>((it - 1) & 1), kErrSplit);
-            // the compute warps' block writes happen before the add (the publish mbarrier orders them
-            // within the CTA, the add's release orders them at GPU scope)
+            if constexpr (kPartInSmem) {
+                // the CTA's block from shared memory to its place in the workspace. That place held tile
+                // it - 2, which every CTA of the group had read before it added its arrival of tile
+                // it - 1, which this warp has seen. Each store consumes its load, so when the last store
+                // has issued the block may be reused (a relaxed arrival: the stores need not complete)
+                const float4* src = reinterpret_cast<const float4*>(smem + kOffPart);
+                float4* dst = reinterpret_cast<float4*>(p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kG + rank) * kPartFloats);
+                constexpr int kPer = kPartFloats / 4 / 32, kChunkV = 7;  // 28 float4 per lane, 7 at a time
+                static_assert(kPer % kChunkV == 0, "copy chunks");
+#pragma unroll
+                for (int c0 = 0; c0 < kPer; c0 += kChunkV) {
+                    float4 v[kChunkV];
+#pragma unroll
+                    for (int c = 0; c < kChunkV; ++c) v[c] = src[lane + 32 * (c0 + c)];
+#pragma unroll
+                    for (int c = 0; c < kChunkV; ++c) dst[lane + 32 * (c0 + c)] = v[c];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_relaxed(bar(kBarPartEmpty), 1u);
+            }
+            // the block's writes happen before the add (the publish mbarrier, or this warp's own stores
+            // and __syncwarp, order them within the CTA; the add's release orders them at GPU scope)
             if (lane == 0) red_release_gpu_add_u64(arrivals, 1ull);
             const unsigned long long target = base + static_cast<unsigned long long>(kG) * static_cast<unsigned long long>(it + 1);
             W.wait_count(arrivals, target, lane, 1, kErrExchange);
