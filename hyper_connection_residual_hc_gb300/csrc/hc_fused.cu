@@ -113,10 +113,6 @@ constexpr int kFoldXHalf = kFoldRows * kChunk * 2;            // 4096: the secon
 constexpr int kUmmaNFold = 144;
 constexpr int kFoldBRow1 = kBRows;                            // first plane row of the second stage
 constexpr int kBTileBytesFold = kUmmaNFold * kChunk * 2;      // 9216
-// per token row and column half: 12 mixes, sum x^2, sum y^2 (+ 2 pad), handed from the warps of
-// rows 64..127 to those of rows 0..63 at the end of a folded tile
-constexpr int kFoldScratchFloats = 16;
-constexpr int kFoldScratchBytes = kFoldRows * 2 * kFoldScratchFloats * 4;   // 8192
 // One CTA's partial sums for one tile: mixes [128 tokens][24] (token-major), then
 // sum x^2 [128 tokens][2 column halves], then sum y^2 [128][2] (a token's two halves adjacent).
 constexpr int kPartRows = 28;
@@ -135,18 +131,15 @@ constexpr int kBarSplitDone = 21, kBarFlagsSeen = 22, kBarEpiRead = 24, kBarYRea
 // this kernel, whose warps spend most of their time in mbarrier waits, a block-wide bar.sync at
 // the end was measured releasing warp 0 while other warps had not reached it; mbarriers hold.
 constexpr int kBarPublish = 25 + 2 * 27, kBarExit = kBarPublish + 1;
-// folded tiles: the warps of rows 64..127 have put their partial sums of a tile in the scratch
-// (one arrival per warp), and the warps of rows 0..63 have taken them (one arrival per warp)
-constexpr int kBarFoldFull = kBarExit + 1, kBarFoldEmpty = kBarExit + 2;
 // kBarNormW: the epilogue warps have put norm_w of the CTA's columns in shared memory (one arrival per
 // epilogue warp; only they read it, long after the stage loop has started)
-constexpr int kBarNormW = kBarExit + 3;
+constexpr int kBarNormW = kBarExit + 1;
 // folded tiles alternate between two accumulators: the full and empty barriers of the second
-constexpr int kBarAccFull2 = kBarExit + 4, kBarAccEmpty2 = kBarExit + 5;
+constexpr int kBarAccFull2 = kBarExit + 2, kBarAccEmpty2 = kBarExit + 3;
 // kBarPartEmpty: the split warp has copied a tile's partial sums out of their shared-memory block
-// (unfolded post and expand modes, one arrival per tile)
-constexpr int kBarPartEmpty = kBarExit + 6;
-constexpr int kNumBars = kBarExit + 7;
+// (every mode but unfolded pre, one arrival per tile)
+constexpr int kBarPartEmpty = kBarExit + 4;
+constexpr int kNumBars = kBarExit + 5;
 
 // Shared-memory layout of each mode, offsets from a 1024-byte aligned base. A slot holds one column
 // stage (a folded slot two): the stream tiles (four, or the one embedding tile in expand mode), the
@@ -175,18 +168,20 @@ struct Layout {
     static constexpr int kOffC = kStages * kStage;
     static constexpr int kOffNormW = kOffC + (kHasC ? kCSlot : 0);
     static constexpr int kOffYStage = ((kOffNormW + kMaxDSlice * 4 + 1023) / 1024) * 1024;
-    static constexpr int kOffFold = kOffYStage + 4 * 2 * kYStageBytes;
+    // Tiles hand their partial sums to the split warp in a shared-memory block, which the split warp
+    // writes to the workspace. Folded tiles have it here: rows 64..127 (the same tokens at the odd
+    // stages) are added to rows 0..63 as it is copied. Unfolded post and expand tiles have it after
+    // the split warp's scratch. Unfolded pre mode has no room for it, so its compute warps write the
+    // workspace themselves. Holding the tile's last slot for the block instead measured slower
+    // (152 -> 154 us at the prefill batch), as did publishing a tile one pass late.
+    static constexpr bool kPartInSmem = kFold || kMode != kModePre;
+    static constexpr int kOffFoldPart = kOffYStage + 4 * 2 * kYStageBytes;
     // the split warp's gather scratch: per owned token (at most 16) its 24 mixes and sum of x^2; then
     // hc_scale and hc_base (27 floats, 32 reserved)
-    static constexpr int kOffSplit = kOffFold + (kFold ? kFoldScratchBytes : 0);
+    static constexpr int kOffSplit = kOffFoldPart + (kFold ? kPartFloats * 4 : 0);
     static constexpr int kOffSplitPrm = kOffSplit + (kTileMax / 8) * 7 * 16;
-    // unfolded post and expand tiles hand their partial sums to the split warp in a shared-memory block
-    // (the split warp writes them to the workspace). Pre mode has no room for the block; holding the
-    // tile's last slot for it instead measured slower (152 -> 154 us at the prefill batch), as did
-    // publishing a tile one pass late, so its compute warps write the workspace themselves
-    static constexpr bool kPartInSmem = !kFold && kMode != kModePre;
-    static constexpr int kOffPart = kOffSplitPrm + 32 * 4;
-    static constexpr int kOffBar = kOffPart + (kPartInSmem ? kPartFloats * 4 : 0);
+    static constexpr int kOffPart = kFold ? kOffFoldPart : kOffSplitPrm + 32 * 4;
+    static constexpr int kOffBar = kOffSplitPrm + 32 * 4 + ((kPartInSmem && !kFold) ? kPartFloats * 4 : 0);
     static constexpr int kOffTmemPtr = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemPtr + 4;
     static constexpr int kSmemUsed = kOffAbort + 4;
@@ -469,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kYColN = kFold ? kYColFold : kYCol;
     constexpr int kOffX = Lay::kOffX, kOffD = Lay::kOffD, kOffB = Lay::kOffB, kOffNormW = Lay::kOffNormW;
     constexpr int kOffYStage = Lay::kOffYStage, kOffBar = Lay::kOffBar, kOffTmemPtr = Lay::kOffTmemPtr;
-    constexpr int kOffAbort = Lay::kOffAbort, kOffFold = Lay::kOffFold, kOffSplit = Lay::kOffSplit;
+    constexpr int kOffAbort = Lay::kOffAbort, kOffSplit = Lay::kOffSplit;
     constexpr int kOffSplitPrm = Lay::kOffSplitPrm, kOffPart = Lay::kOffPart;
     constexpr bool kPartInSmem = Lay::kPartInSmem;
     constexpr int kNumSlots = kStages + (Lay::kHasC ? 1 : 0);
@@ -556,8 +551,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(kBarPublish), kComputeWarps);
         mbar_init(bar(kBarExit), kThreads / 32);
-        mbar_init(bar(kBarFoldFull), 4);
-        mbar_init(bar(kBarFoldEmpty), 4);
         mbar_init(bar(kBarNormW), 4);
         mbar_init(bar(kBarAccFull2), 1);
         mbar_init(bar(kBarAccEmpty2), kComputeWarps);
@@ -846,53 +839,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 sxx = __fadd2_rn(__fadd2_rn(sx[0], sx[1]), __fadd2_rn(sx[2], sx[3]));
             const float2 syy = __fadd2_rn(sy[0], sy[1]);
             float sxs = sxx.x + sxx.y, sys = syy.x + syy.y;
-            if (kFold) {
-                // the same tokens' sums of the odd stages (rows 64..127) join those of the even ones
-                float4* fs = reinterpret_cast<float4*>(smem + kOffFold) + (trow * 2 + h) * (kFoldScratchFloats / 4);
-                if (sub) {
-                    if (it > 0) W.wait(bar(kBarFoldEmpty), static_cast<uint32_t>((it - 1) & 1), kErrComputeAcc);
-                    fs[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
-                    fs[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
-                    fs[2] = make_float4(acc[4].x, acc[4].y, acc[5].x, acc[5].y);
-                    fs[3] = make_float4(sxs, sys, 0.f, 0.f);
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(bar(kBarFoldFull));
-                        mbar_arrive(bar(kBarPublish));  // the block is written by the warp of rows 0..63
-                    }
-                    continue;
-                }
-                W.wait(bar(kBarFoldFull), static_cast<uint32_t>(it & 1), kErrComputeAcc);
-                const float4 f0 = fs[0], f1 = fs[1], f2v = fs[2], f3 = fs[3];
-                acc[0] = __fadd2_rn(acc[0], make_float2(f0.x, f0.y));
-                acc[1] = __fadd2_rn(acc[1], make_float2(f0.z, f0.w));
-                acc[2] = __fadd2_rn(acc[2], make_float2(f1.x, f1.y));
-                acc[3] = __fadd2_rn(acc[3], make_float2(f1.z, f1.w));
-                acc[4] = __fadd2_rn(acc[4], make_float2(f2v.x, f2v.y));
-                acc[5] = __fadd2_rn(acc[5], make_float2(f2v.z, f2v.w));
-                sxs += f3.x;
-                sys += f3.y;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kBarFoldEmpty));
-            }
             float* P;
+            int prow = trow;  // the block's row of this thread's sums
             if constexpr (kPartInSmem) {
                 // into shared memory; the split warp writes the block to the workspace, so the arrive
-                // below has no global stores to wait for (a memory round trip per tile otherwise)
+                // below has no global stores to wait for (a memory round trip per tile otherwise).
+                // Folded, rows 64..127 keep their own row: the split warp adds them to rows 0..63
                 if (it > 0) W.wait(bar(kBarPartEmpty), static_cast<uint32_t>((it - 1) & 1), kErrComputeAcc);
                 P = reinterpret_cast<float*>(smem + kOffPart);
+                prow = row;
             } else {
                 if (it > 0) W.wait(bar(kBarSplitDone), static_cast<uint32_t>((it - 1) & 1), kErrExchange);
                 P = p.ws_part + (static_cast<size_t>(cid * 2 + static_cast<int>(it & 1)) * kG + rank) * kPartFloats;
             }
             {
-                float4* pm4 = reinterpret_cast<float4*>(P + trow * kMix + 12 * h);
+                float4* pm4 = reinterpret_cast<float4*>(P + prow * kMix + 12 * h);
                 pm4[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
                 pm4[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
                 pm4[2] = make_float4(acc[4].x, acc[4].y, acc[5].x, acc[5].y);
             }
-            P[kPartSx + 2 * trow + h] = sxs;
-            P[kPartSy + 2 * trow + h] = sys;
+            P[kPartSx + 2 * prow + h] = sxs;
+            P[kPartSy + 2 * prow + h] = sys;
             // hand the block to the split warp, which publishes it; no waiting here
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarPublish));
@@ -1107,15 +1074,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // has issued the block may be reused (a relaxed arrival: the stores need not complete)
                 const float4* src = reinterpret_cast<const float4*>(smem + kOffPart);
                 float4* dst = reinterpret_cast<float4*>(p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kG + rank) * kPartFloats);
-                constexpr int kPer = kPartFloats / 4 / 32, kChunkV = 7;  // 28 float4 per lane, 7 at a time
-                static_assert(kPer % kChunkV == 0, "copy chunks");
+                if constexpr (kFold) {
+                    // rows 0..63 (each pass's first stage) plus rows 64..127 (the same tokens at its
+                    // second stage), in that order: the mixes are float4 i < 384 (row i / 6) with the
+                    // partner 384 further on; the sums of x^2 and of y^2 are 32 float4 each (two rows'
+                    // halves per float4) with the partner 32 further on. Rows 64..127 of the workspace
+                    // block are not read.
+                    constexpr int kMixV = kFoldRows * kMix / 4, kSumV = kFoldRows * 2 / 4;
+                    static_assert((kMixV + 2 * kSumV) % 32 == 0, "whole warps");
+#pragma unroll 2
+                    for (int i = lane; i < kMixV + 2 * kSumV; i += 32) {
+                        const int a = i < kMixV ? i
+                                      : i < kMixV + kSumV ? kPartSx / 4 + (i - kMixV)
+                                                           : kPartSy / 4 + (i - kMixV - kSumV);
+                        const int b = a + (i < kMixV ? kMixV : kSumV);
+                        const float4 u = src[a], v = src[b];
+                        dst[a] = make_float4(u.x + v.x, u.y + v.y, u.z + v.z, u.w + v.w);
+                    }
+                } else {
+                    constexpr int kPer = kPartFloats / 4 / 32, kChunkV = 7;  // 28 float4 per lane, 7 at a time
+                    static_assert(kPer % kChunkV == 0, "copy chunks");
 #pragma unroll
-                for (int c0 = 0; c0 < kPer; c0 += kChunkV) {
-                    float4 v[kChunkV];
+                    for (int c0 = 0; c0 < kPer; c0 += kChunkV) {
+                        float4 v[kChunkV];
 #pragma unroll
-                    for (int c = 0; c < kChunkV; ++c) v[c] = src[lane + 32 * (c0 + c)];
+                        for (int c = 0; c < kChunkV; ++c) v[c] = src[lane + 32 * (c0 + c)];
 #pragma unroll
-                    for (int c = 0; c < kChunkV; ++c) dst[lane + 32 * (c0 + c)] = v[c];
+                        for (int c = 0; c < kChunkV; ++c) dst[lane + 32 * (c0 + c)] = v[c];
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive_relaxed(bar(kBarPartEmpty), 1u);
