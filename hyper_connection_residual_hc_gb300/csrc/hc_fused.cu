@@ -735,6 +735,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (yround > 0)
                     W.wait(bar(kBarYFree + static_cast<int>(g % kRingN)), static_cast<uint32_t>((yround - 1) & 1),
                            kErrComputeY);
+                // three passes before the tile ends (the first, in a shorter tile), the next tile's
+                // coefficient lines into L2: loaded from DRAM at the tile's end, under the stream's
+                // load, they took 1.3-2.2 us to land, which the next tile's first pass waited for
+                if (kPost && h == 0 && s == (SP > 3 ? SP - 3 : 0) && it + 1 < my_tiles) {
+                    const long long ntok = (cid + (it + 1) * ncl) * p.tile_m + trow;
+                    if (trow < p.tile_m && ntok < p.n) {
+                        prefetch_l2_evict_last(p.post + ntok * 4);
+                        prefetch_l2_evict_last(p.comb + ntok * 16);
+                        if (p.pre_mix) prefetch_l2_evict_last(p.pre_mix + ntok * 4);
+                    }
+                }
                 const Slot sl = slot_at(it, s);
                 W.wait(bar(kBarFull + sl.idx), static_cast<uint32_t>(sl.round & 1), kErrComputeFull);
                 const uint32_t sb = sl.base;

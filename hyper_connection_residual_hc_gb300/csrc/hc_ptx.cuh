@@ -63,6 +63,11 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 }
 
 // Fetch one tile of a tensor map into L2 only (no shared memory, no completion to wait for).
+// One line of global memory into L2, marked to be evicted last.
+__device__ __forceinline__ void prefetch_l2_evict_last(const void* p) {
+    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
                  "r"(x), "r"(y)
