@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -29,7 +30,7 @@ __device__ __forceinline__ uint32_t pk(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__global__ void __launch_bounds__(256) hc_post_kernel(const uint4* __restrict__ X, const uint4* __restrict__ delta,
+__global__ void __launch_bounds__(256, 3) hc_post_kernel(const uint4* __restrict__ X, const uint4* __restrict__ delta,
                                                       const float4* __restrict__ post, const float4* __restrict__ comb,
                                                       uint4* X_out, long long n, int dv) {
     const long long total = n * dv;
@@ -106,6 +107,27 @@ int grid_for(long long work, int per_block) {
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     return static_cast<int>(blocks);
+}
+
+// Blocks of hc_post_kernel resident at once on the current device (SMs x blocks per SM), found once
+// per device: its grid-stride loop then runs as a single wave (at 3 blocks per SM, the earlier cap of
+// 8 blocks per SM left a partial last wave)
+int post_grid(long long work) {
+    static std::atomic<int> resident[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return grid_for(work, 256);
+    int r = resident[dev].load(std::memory_order_relaxed);
+    if (r == 0) {
+        int sms = 0, per_sm = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hc_post_kernel, 256, 0) != cudaSuccess ||
+            sms < 1 || per_sm < 1)
+            return grid_for(work, 256);
+        r = sms * per_sm;
+        resident[dev].store(r, std::memory_order_relaxed);
+    }
+    const long long blocks = (work + 255) / 256;
+    return static_cast<int>(blocks < r ? (blocks < 1 ? 1 : blocks) : r);
 }
 
 // ---- validation ---------------------------------------------------------------------------------
@@ -315,7 +337,7 @@ int hc_post(const void* delta, const void* X, const float* post, const float* co
     const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     if (s.hc != kHC) return launch_status(launch_generic_post(X, delta, post, comb, X_out, nullptr, n, s.hc, s.d, cs));
     const int dv = s.d / 8;
-    hc_post_kernel<<<grid_for(n * dv, 256), 256, 0, cs>>>(
+    hc_post_kernel<<<post_grid(n * dv), 256, 0, cs>>>(
         static_cast<const uint4*>(X), static_cast<const uint4*>(delta), reinterpret_cast<const float4*>(post),
         reinterpret_cast<const float4*>(comb), static_cast<uint4*>(X_out), n, dv);
     return cuda_status(cudaGetLastError());
