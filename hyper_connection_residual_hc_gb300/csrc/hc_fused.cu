@@ -1093,7 +1093,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // block are not read.
                     constexpr int kMixV = kFoldRows * kMix / 4, kSumV = kFoldRows * 2 / 4;
                     static_assert((kMixV + 2 * kSumV) % 32 == 0, "whole warps");
-#pragma unroll 2
+#pragma unroll 7
                     for (int i = lane; i < kMixV + 2 * kSumV; i += 32) {
                         const int a = i < kMixV ? i
                                       : i < kMixV + kSumV ? kPartSx / 4 + (i - kMixV)
