@@ -369,28 +369,10 @@ __device__ __forceinline__ float2 rcp2_refined(float2 x) {
     return __ffma2_rn(r, e, r);
 }
 
-__device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const float (&sc)[3], const float (&b)[kMix],
-                                               int iters, float eps, float (&pre)[4], float (&post)[4],
-                                               float (&C)[16]) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) pre[j] = sigmoidf_(m[j] * sc[0] + b[j]) + eps;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) post[j] = 2.0f * sigmoidf_(m[4 + j] * sc[1] + b[4 + j]);
-    float2 C2[8];
+// The Sinkhorn rounds on the softmax matrix C2 (row j: C2[2j] holds columns 0 and 1, C2[2j + 1]
+// columns 2 and 3): one column normalisation, then iters - 1 times a row and a column one.
+__device__ __forceinline__ void sinkhorn_rounds(float2 (&C2)[8], int iters, float eps) {
     const float2 e2 = make_float2(eps, eps);
-    // softmax over each row (max subtracted), then + eps
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        float l[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) l[k] = m[8 + 4 * j + k] * sc[2] + b[8 + 4 * j + k];
-        const float mx = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
-        const float2 x01 = make_float2(expf(l[0] - mx), expf(l[1] - mx));
-        const float2 x23 = make_float2(expf(l[2] - mx), expf(l[3] - mx));
-        const float inv = rcp_refined((x01.x + x01.y) + (x23.x + x23.y));
-        C2[2 * j] = __ffma2_rn(x01, make_float2(inv, inv), e2);
-        C2[2 * j + 1] = __ffma2_rn(x23, make_float2(inv, inv), e2);
-    }
     auto col_norm = [&]() {
         const float2 s01 = __fadd2_rn(__fadd2_rn(C2[0], C2[2]), __fadd2_rn(C2[4], C2[6]));
         const float2 s23 = __fadd2_rn(__fadd2_rn(C2[1], C2[3]), __fadd2_rn(C2[5], C2[7]));
@@ -424,6 +406,31 @@ __device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const flo
         row_norm();
         col_norm();
     }
+}
+
+__device__ __forceinline__ void split_sinkhorn(const float (&m)[kMix], const float (&sc)[3], const float (&b)[kMix],
+                                               int iters, float eps, float (&pre)[4], float (&post)[4],
+                                               float (&C)[16]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pre[j] = sigmoidf_(fmaf(m[j], sc[0], b[j])) + eps;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) post[j] = 2.0f * sigmoidf_(fmaf(m[4 + j], sc[1], b[4 + j]));
+    float2 C2[8];
+    const float2 e2 = make_float2(eps, eps);
+    // softmax over each row (max subtracted), then + eps
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float l[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) l[k] = fmaf(m[8 + 4 * j + k], sc[2], b[8 + 4 * j + k]);
+        const float mx = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
+        const float2 x01 = make_float2(expf(l[0] - mx), expf(l[1] - mx));
+        const float2 x23 = make_float2(expf(l[2] - mx), expf(l[3] - mx));
+        const float inv = rcp_refined((x01.x + x01.y) + (x23.x + x23.y));
+        C2[2 * j] = __ffma2_rn(x01, make_float2(inv, inv), e2);
+        C2[2 * j + 1] = __ffma2_rn(x23, make_float2(inv, inv), e2);
+    }
+    sinkhorn_rounds(C2, iters, eps);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         C[4 * j] = C2[2 * j].x;
@@ -1181,45 +1188,114 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             __syncwarp();
-            const int oi = lane;  // lane i runs the split of owned token i
-            const int r_tok = static_cast<int>(rank) + kG * oi;
-            const bool mine = oi < kTv;
-            float m[kMix];
-            float sxt = 0.f;
-            if (mine) {
-                const float4* sv = reinterpret_cast<const float4*>(scr) + oi * 7;
+            if constexpr (kFold) {
+                // At most 64 / kG = 4 owned tokens. The steps of the split before its Sinkhorn rounds
+                // (logits, sigmoids, row softmax) run with one lane per mix (lanes 0..23), each value
+                // by the same operations as in split_sinkhorn: the row max and sum combine the four
+                // lanes of a row as (0,1),(2,3) then the two pairs, as split_sinkhorn does. On one lane
+                // those 24 exponentials and 8 divisions took about 1,600 of its 4,900 cycles. Token i's
+                // rounds then run on lane i, which gathers its 16 softmax values by shuffles.
+                constexpr int kOwn = kFoldRows / kG;
+                static_assert(kOwn >= 1 && kOwn <= 4, "owned tokens of a folded tile");
+                float mv[kOwn];  // lane k < 24: mix k of each owned token
 #pragma unroll
-                for (int k = 0; k < 6; ++k) {
-                    const float4 v = sv[k];
-                    m[4 * k] = v.x; m[4 * k + 1] = v.y; m[4 * k + 2] = v.z; m[4 * k + 3] = v.w;
+                for (int i = 0; i < kOwn; ++i) {
+                    mv[i] = 0.f;
+                    if (i < kTv && lane < kMix) {
+                        const float rr = rsqrtf(scr[i * 28 + 24] / static_cast<float>(4 * p.d) + p.norm_eps);
+                        mv[i] = scr[i * 28 + lane] * rr;
+                    }
                 }
-                sxt = sv[6].x;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarSplitDone));  // the blocks of this tile may be reused
-            if (mine) {
-                const long long tok = t0 + r_tok;
-                const float rr = rsqrtf(sxt / static_cast<float>(4 * p.d) + p.norm_eps);  // rsqrt of mean(x^2) + eps
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarSplitDone));  // the blocks of this tile may be reused
+                if (p.mixes_out && lane < kMix) {
 #pragma unroll
-                for (int i = 0; i < kMix; ++i) m[i] *= rr;
-                if (p.mixes_out) {
-                    float4* mo = reinterpret_cast<float4*>(p.mixes_out + tok * kMix);
-#pragma unroll
-                    for (int i = 0; i < kMix / 4; ++i) mo[i] = make_float4(m[4 * i], m[4 * i + 1], m[4 * i + 2], m[4 * i + 3]);
+                    for (int i = 0; i < kOwn; ++i)
+                        if (i < kTv) p.mixes_out[(t0 + static_cast<int>(rank) + kG * i) * kMix + lane] = mv[i];
                 }
                 if (p.pre_out) {
-                    float pre[4], post[4], C[16];
-                    float sc[3], bs[kMix];
+                    const float bk = lane < kMix ? prm[3 + lane] : 0.f;
+                    const float sck = prm[lane < 4 ? 0 : lane < 8 ? 1 : 2];
+                    float cv[kOwn];  // lanes 8..23: entry lane - 8 of each token's softmax, + eps
 #pragma unroll
-                    for (int i = 0; i < 3; ++i) sc[i] = prm[i];
+                    for (int i = 0; i < kOwn; ++i) {
+                        const float l = fmaf(mv[i], sck, bk);
+                        float mx = fmaxf(l, __shfl_xor_sync(0xffffffffu, l, 1));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                        const float x = expf(l - mx);
+                        float sm = x + __shfl_xor_sync(0xffffffffu, x, 1);
+                        sm = sm + __shfl_xor_sync(0xffffffffu, sm, 2);
+                        cv[i] = fmaf(x, rcp_refined(sm), p.hc_eps);
+                        if (i < kTv && lane < 8) {
+                            const long long tok = t0 + static_cast<int>(rank) + kG * i;
+                            if (lane < 4)
+                                p.pre_out[tok * 4 + lane] = sigmoidf_(l) + p.hc_eps;
+                            else
+                                p.post_out[tok * 4 + (lane - 4)] = 2.0f * sigmoidf_(l);
+                        }
+                    }
+                    float2 C2[8];
 #pragma unroll
-                    for (int i = 0; i < kMix; ++i) bs[i] = prm[3 + i];
-                    split_sinkhorn(m, sc, bs, p.iters, p.hc_eps, pre, post, C);
-                    reinterpret_cast<float4*>(p.pre_out)[tok] = make_float4(pre[0], pre[1], pre[2], pre[3]);
-                    reinterpret_cast<float4*>(p.post_out)[tok] = make_float4(post[0], post[1], post[2], post[3]);
-                    float4* co = reinterpret_cast<float4*>(p.comb_out) + tok * 4;
+                    for (int q = 0; q < 8; ++q) {
+                        float a = 0.f, b = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) co[j] = make_float4(C[4 * j], C[4 * j + 1], C[4 * j + 2], C[4 * j + 3]);
+                        for (int i = 0; i < kOwn; ++i) {
+                            const float va = __shfl_sync(0xffffffffu, cv[i], 8 + 2 * q);
+                            const float vb = __shfl_sync(0xffffffffu, cv[i], 9 + 2 * q);
+                            if (lane == i) { a = va; b = vb; }
+                        }
+                        C2[q] = make_float2(a, b);
+                    }
+                    if (lane < kTv) {
+                        sinkhorn_rounds(C2, p.iters, p.hc_eps);
+                        const long long tok = t0 + static_cast<int>(rank) + kG * lane;
+                        float4* co = reinterpret_cast<float4*>(p.comb_out) + tok * 4;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            co[j] = make_float4(C2[2 * j].x, C2[2 * j].y, C2[2 * j + 1].x, C2[2 * j + 1].y);
+                    }
+                }
+            } else {
+                const int oi = lane;  // lane i runs the split of owned token i
+                const int r_tok = static_cast<int>(rank) + kG * oi;
+                const bool mine = oi < kTv;
+                float m[kMix];
+                float sxt = 0.f;
+                if (mine) {
+                    const float4* sv = reinterpret_cast<const float4*>(scr) + oi * 7;
+    #pragma unroll
+                    for (int k = 0; k < 6; ++k) {
+                        const float4 v = sv[k];
+                        m[4 * k] = v.x; m[4 * k + 1] = v.y; m[4 * k + 2] = v.z; m[4 * k + 3] = v.w;
+                    }
+                    sxt = sv[6].x;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarSplitDone));  // the blocks of this tile may be reused
+                if (mine) {
+                    const long long tok = t0 + r_tok;
+                    const float rr = rsqrtf(sxt / static_cast<float>(4 * p.d) + p.norm_eps);  // rsqrt of mean(x^2) + eps
+    #pragma unroll
+                    for (int i = 0; i < kMix; ++i) m[i] *= rr;
+                    if (p.mixes_out) {
+                        float4* mo = reinterpret_cast<float4*>(p.mixes_out + tok * kMix);
+    #pragma unroll
+                        for (int i = 0; i < kMix / 4; ++i) mo[i] = make_float4(m[4 * i], m[4 * i + 1], m[4 * i + 2], m[4 * i + 3]);
+                    }
+                    if (p.pre_out) {
+                        float pre[4], post[4], C[16];
+                        float sc[3], bs[kMix];
+    #pragma unroll
+                        for (int i = 0; i < 3; ++i) sc[i] = prm[i];
+    #pragma unroll
+                        for (int i = 0; i < kMix; ++i) bs[i] = prm[3 + i];
+                        split_sinkhorn(m, sc, bs, p.iters, p.hc_eps, pre, post, C);
+                        reinterpret_cast<float4*>(p.pre_out)[tok] = make_float4(pre[0], pre[1], pre[2], pre[3]);
+                        reinterpret_cast<float4*>(p.post_out)[tok] = make_float4(post[0], post[1], post[2], post[3]);
+                        float4* co = reinterpret_cast<float4*>(p.comb_out) + tok * 4;
+    #pragma unroll
+                        for (int j = 0; j < 4; ++j) co[j] = make_float4(C[4 * j], C[4 * j + 1], C[4 * j + 2], C[4 * j + 3]);
+                    }
                 }
             }
             __syncwarp();
