@@ -845,11 +845,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // these loads
             if (it + 1 < my_tiles) load_coefs(it + 1);
 
-            // publish this CTA's partial sums of the tile to the group; the split warp collects them.
-            // The block of tile it reuses that of tile it - 2, which the other CTAs of the group may
-            // still be reading; each of them publishes tile it - 1 only after it has read tile it - 2,
-            // and this CTA's split warp signals split_done(it - 1) only after it has seen all those
-            // flags (and read tile it - 1 itself).
+            // this CTA's partial sums of the tile, for the split warp to publish to the group. The
+            // workspace block of tile it reuses that of tile it - 2, which the other CTAs of the group
+            // may still be reading; each of them publishes tile it - 1 only after it has read tile
+            // it - 2, and this CTA's split warp signals split_done(it - 1) only after it has seen all
+            // those arrivals (and read tile it - 1 itself). Compute warps that write the workspace
+            // therefore wait for split_done(it - 1); where the split warp writes it, its own order
+            // gives the same.
             const float2 sxx = __fadd2_rn(__fadd2_rn(sx[0], sx[1]), __fadd2_rn(sx[2], sx[3]));
             const float2 syy = __fadd2_rn(sy[0], sy[1]);
             float sxs = sxx.x + sxx.y, sys = syy.x + syy.y;
@@ -874,7 +876,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             P[kPartSx + 2 * prow + h] = sxs;
             P[kPartSy + 2 * prow + h] = sys;
-            // hand the block to the split warp, which publishes it; no waiting here
+            // hand the block to the split warp, which publishes it (the arrive is a release: in
+            // unfolded pre mode it waits for this warp's workspace stores)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarPublish));
         }
