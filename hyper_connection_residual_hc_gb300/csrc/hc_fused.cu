@@ -260,7 +260,7 @@ struct FusedParams {
     void* stream_mean;              // bf16 [n, d] mean of the 4 new streams, or null
     void* y_normed;
     float* ws_part;                 // workspace partial-sum blocks
-    unsigned long long* ws_flags;   // workspace flags
+    unsigned long long* ws_arrivals;  // workspace arrival counters, one per group slot
     unsigned long long* ws_launch;  // workspace launch counters, one per group
     long long n;
     long long num_tiles;
@@ -903,7 +903,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (long long it = 0; it < my_tiles; ++it) {
             const int buf = static_cast<int>(it & 1);
             // r_y of this thread's row from the group's sums of y^2 (2 halves of each of the kG
-            // column shares), once the split warp has seen all their flags
+            // column shares), once the split warp has seen the group's arrivals for the tile
             W.wait(bar(kBarFlagsSeen + buf), static_cast<uint32_t>((it >> 1) & 1), kErrEpilogue);
             const float* blk =
                 p.ws_part + (static_cast<size_t>(cid * 2 + buf) * kG) * kPartFloats + kPartSy + 2 * trow;
@@ -1071,7 +1071,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < kMix) prm[3 + lane] = __ldg(p.hc_base + lane);
         __syncwarp();
         // the group's arrival counter and its value when this launch started
-        unsigned long long* arrivals = p.ws_flags + static_cast<size_t>(cid) * kCounterStride;
+        unsigned long long* arrivals = p.ws_arrivals + static_cast<size_t>(cid) * kCounterStride;
         unsigned long long base = 0;
         if (lane == 0) base = ld_acquire_gpu_u64(p.ws_launch + cid);
         base = __shfl_sync(0xffffffffu, base, 0);
@@ -1576,7 +1576,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream) {
     p.stream_mean = a.stream_mean;
     p.y_normed = a.y_normed;
     p.ws_part = reinterpret_cast<float*>(a.workspace);
-    p.ws_flags = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(a.workspace) + kWsPartBytes);
+    p.ws_arrivals = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(a.workspace) + kWsPartBytes);
     p.ws_launch =
         reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(a.workspace) + kWsPartBytes + kWsFlagBytes);
     p.n = a.n;
@@ -1638,7 +1638,7 @@ static __device__ __align__(256) unsigned char g_noalloc_workspace[kWorkspaceByt
 // sized to kWorkspaceBytes, so no call is ever refused for want of room in the array.
 static_assert(sizeof(g_noalloc_workspace) >= kWorkspaceBytes && kWorkspaceBytes >= kWsPartBytes &&
                   kWsPartBytes == static_cast<size_t>(kMaxCtas) * 2 * kPartFloats * 4,
-              "the fixed scratch holds the partial sums of kMaxCtas CTAs, their flags and counters");
+              "the fixed scratch holds the partial sums of kMaxCtas CTAs and the groups' counters");
 
 namespace {
 void* g_noalloc_ptr[kMaxDevices] = {};
@@ -1677,10 +1677,11 @@ int read_device_error(unsigned int* word, int clear, cudaStream_t stream) {
         if (cudaMemcpyToSymbolAsync(g_hc_error, &z, sizeof(z), 0, cudaMemcpyHostToDevice, stream) != cudaSuccess)
             return -7;
         if (v != 0) {
-            // A kernel gave up a wait: a CTA of its group that had not yet read the group's launch
-            // counter when the counter advanced would tag its flags like the group's next launch. The
-            // library's fixed scratch (hc_post_then_pre_noalloc) therefore starts afresh from zero; a
-            // memset is not an allocation. Caller workspaces are the caller's to zero (hc.h).
+            // A kernel gave up a wait: a CTA of its group may still add arrivals to the group's
+            // counter after the group's base has moved on, and the group's next launch would count
+            // them as its own. The library's fixed scratch (hc_post_then_pre_noalloc) therefore
+            // starts afresh from zero; a memset is not an allocation. Caller workspaces are the
+            // caller's to zero (hc.h).
             int dev = 0;
             if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -7;
             void* scratch = nullptr;
