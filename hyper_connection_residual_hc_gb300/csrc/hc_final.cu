@@ -32,16 +32,19 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // a -> low half
     return *reinterpret_cast<uint32_t*>(&v);
 }
-__device__ __forceinline__ void unpack(const uint4& v, float (&f)[8]) {
-    f[0] = flo(v.x); f[1] = fhi(v.x); f[2] = flo(v.y); f[3] = fhi(v.y);
-    f[4] = flo(v.z); f[5] = fhi(v.z); f[6] = flo(v.w); f[7] = fhi(v.w);
+// 8 bf16 columns as column pairs: f[m] = columns 2m, 2m + 1
+__device__ __forceinline__ void unpack(const uint4& v, float2 (&f)[4]) {
+    f[0] = make_float2(flo(v.x), fhi(v.x)); f[1] = make_float2(flo(v.y), fhi(v.y));
+    f[2] = make_float2(flo(v.z), fhi(v.z)); f[3] = make_float2(flo(v.w), fhi(v.w));
 }
-__device__ __forceinline__ uint4 pack8(const float (&o)[8]) {
-    return make_uint4(pack2(o[0], o[1]), pack2(o[2], o[3]), pack2(o[4], o[5]), pack2(o[6], o[7]));
+__device__ __forceinline__ uint4 pack8(const float2 (&o)[4]) {
+    return make_uint4(pack2(o[0].x, o[0].y), pack2(o[1].x, o[1].y), pack2(o[2].x, o[2].y), pack2(o[3].x, o[3].y));
 }
+__device__ __forceinline__ float2 bcast2(float a) { return make_float2(a, a); }
 
+// X' without its store is held to 128 registers (4 blocks per SM): left free it took 130 and 3 blocks
 template <bool kPost, bool kStoreX>
-__global__ void __launch_bounds__(kFinalThreads) hc_final_kernel(
+__global__ void __launch_bounds__(kFinalThreads, (kPost && !kStoreX) ? 4 : 0) hc_final_kernel(
     const uint4* __restrict__ X, const uint4* __restrict__ delta, const float4* __restrict__ post,
     const float4* __restrict__ comb, const float4* __restrict__ pre_mix, const float* __restrict__ norm_w,
     uint4* __restrict__ X_out, uint4* __restrict__ z, int dv, float inv_d, float eps) {
@@ -75,31 +78,33 @@ __global__ void __launch_bounds__(kFinalThreads) hc_final_kernel(
         }
     }
 
-    // pass 1: X' (post), y rounded to bf16, sum of y^2
+    // pass 1: X' (post), y rounded to bf16, sum of y^2. Column pairs go through the packed fp32
+    // instructions (two IEEE operations each, rounded per lane as the scalar ones), in the order
+    // of the formulas above.
     uint32_t yb[kFinalVec][4];
     float ss = 0.f;
 #pragma unroll
     for (int v = 0; v < kFinalVec; ++v) {
         const int i = tid + v * kFinalThreads;
         if (i < dv) {
-            float x[4][8];
+            float2 x[4][4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) unpack(xs[v][j], x[j]);
             if (kPost) {
-                float dl[8];
+                float2 dl[4];
                 unpack(ds[v], dl);
-                float xp[4][8];
+                float2 xp[4][4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    float o[8];
+                    float2 o[4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        float s = pv[k] * dl[e];
-                        s = fmaf(c[0 * 4 + k], x[0][e], s);
-                        s = fmaf(c[1 * 4 + k], x[1][e], s);
-                        s = fmaf(c[2 * 4 + k], x[2][e], s);
-                        s = fmaf(c[3 * 4 + k], x[3][e], s);
-                        o[e] = s;
+                    for (int m = 0; m < 4; ++m) {
+                        float2 s = __fmul2_rn(bcast2(pv[k]), dl[m]);
+                        s = __ffma2_rn(bcast2(c[0 * 4 + k]), x[0][m], s);
+                        s = __ffma2_rn(bcast2(c[1 * 4 + k]), x[1][m], s);
+                        s = __ffma2_rn(bcast2(c[2 * 4 + k]), x[2][m], s);
+                        s = __ffma2_rn(bcast2(c[3 * 4 + k]), x[3][m], s);
+                        o[m] = s;
                     }
                     const uint4 ov = pack8(o);
                     if (kStoreX) __stcs(X_out + (t * 4 + k) * dv + i, ov);
@@ -108,21 +113,16 @@ __global__ void __launch_bounds__(kFinalThreads) hc_final_kernel(
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x[k][e] = xp[k][e];
-            }
-            float y[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                float s = pm[0] * x[0][e];
-                s = fmaf(pm[1], x[1][e], s);
-                s = fmaf(pm[2], x[2][e], s);
-                s = fmaf(pm[3], x[3][e], s);
-                y[e] = s;
+                    for (int m = 0; m < 4; ++m) x[k][m] = xp[k][m];
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t u = pack2(y[2 * e], y[2 * e + 1]);
-                yb[v][e] = u;
+            for (int m = 0; m < 4; ++m) {
+                float2 s = __fmul2_rn(bcast2(pm[0]), x[0][m]);
+                s = __ffma2_rn(bcast2(pm[1]), x[1][m], s);
+                s = __ffma2_rn(bcast2(pm[2]), x[2][m], s);
+                s = __ffma2_rn(bcast2(pm[3]), x[3][m], s);
+                const uint32_t u = pack2(s.x, s.y);
+                yb[v][m] = u;
                 const float a0 = flo(u), a1 = fhi(u);
                 ss = fmaf(a0, a0, ss);
                 ss = fmaf(a1, a1, ss);
@@ -146,12 +146,11 @@ __global__ void __launch_bounds__(kFinalThreads) hc_final_kernel(
             const float4 w0 = __ldg(reinterpret_cast<const float4*>(norm_w) + 2 * i);
             const float4 w1 = __ldg(reinterpret_cast<const float4*>(norm_w) + 2 * i + 1);
             const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            float o[8];
+            float2 o[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                o[2 * e] = w[2 * e] * (flo(yb[v][e]) * r);
-                o[2 * e + 1] = w[2 * e + 1] * (fhi(yb[v][e]) * r);
-            }
+            for (int e = 0; e < 4; ++e)
+                o[e] = __fmul2_rn(make_float2(w[2 * e], w[2 * e + 1]),
+                                  __fmul2_rn(make_float2(flo(yb[v][e]), fhi(yb[v][e])), bcast2(r)));
             __stcs(z + t * dv + i, pack8(o));
         }
     }
