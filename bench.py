@@ -40,9 +40,25 @@ BYTES_PER_TOKEN = 102592      # read X 40960 + delta 10240 + post 16 + comb 64 +
                               # write X' 40960 + y_normed 10240 + pre/post/comb 96
 PARAM_BYTES = 1986668         # hc_fn fp32 1966080 + norm_w 20480 + hc_base 96 + hc_scale 12
 FINAL_EPS = 1e-20             # the final RMSNorm's eps ("Final RMSNorm" page)
+
+
+def step_bytes_per_token(hc: int, d: int) -> int:
+    """hc_post_then_pre's bytes per token for hc streams of width d: read X, Delta, post, comb and
+    pre_mix; write X', y_normed and pre, post, comb (BYTES_PER_TOKEN at hc = 4, d = 5120)."""
+    coefs = 4 * (2 * hc + hc * hc)  # post, comb, pre_mix in; pre, post, comb out: the same count
+    return 2 * (hc * d * 2 + d * 2 + coefs)
+
+
+def step_param_bytes(hc: int, d: int) -> int:
+    """Bytes of one parameter set: hc_fn fp32 [(2 + hc) hc, hc d], norm_w, hc_base, hc_scale
+    (PARAM_BYTES at hc = 4, d = 5120)."""
+    M = (2 + hc) * hc
+    return M * hc * d * 4 + d * 4 + M * 4 + 3 * 4
 CSRC = "hyper_connection_residual_hc_gb300/csrc/"
 FUSED_SOURCES = [CSRC + "hc_fused.cu", CSRC + "hc_ptx.cuh"]
 FINAL_SOURCES = [CSRC + "hc_final.cu"]
+GENERIC_SOURCES = [CSRC + "hc_generic.cu"]
+GENERIC_KERNELS = "gen_post_kernel, gen_proj_kernel, gen_tail_kernel"
 
 # Per op: algorithmic bytes per token and per call (parameters), the kernel it launches, the sources
 # that kernel is built from, and the ncu summary of that kernel on this workload; `call` is the entry
@@ -78,6 +94,23 @@ OPS = {
     "long_prefill_b1_t65536": dict(bytes_per_token=BYTES_PER_TOKEN, param_bytes=PARAM_BYTES,
                                    kernel="hc_fused_kernel<1>", sources=FUSED_SOURCES, traffic=None,
                                    call="post_then_pre", workload="long_prefill_b1_t65536_4steps"),
+    # the step on the prefill batch at other shapes: 8 or 2 streams, or d = 7168, on the CUDA-core
+    # kernels (the writing half, then per chunk of tokens the projection and the split + norm); d = 2048
+    # on the fused kernel
+    "post_then_pre_hc8": dict(bytes_per_token=step_bytes_per_token(8, 5120), param_bytes=step_param_bytes(8, 5120),
+                              kernel=GENERIC_KERNELS, sources=GENERIC_SOURCES, traffic=None, call="post_then_pre",
+                              workload="prefill_b4_t4096_hc8"),
+    "post_then_pre_hc2": dict(bytes_per_token=step_bytes_per_token(2, 5120), param_bytes=step_param_bytes(2, 5120),
+                              kernel=GENERIC_KERNELS, sources=GENERIC_SOURCES, traffic=None, call="post_then_pre",
+                              workload="prefill_b4_t4096_hc2"),
+    "post_then_pre_d7168": dict(bytes_per_token=step_bytes_per_token(4, 7168),
+                                param_bytes=step_param_bytes(4, 7168), kernel=GENERIC_KERNELS,
+                                sources=GENERIC_SOURCES, traffic=None, call="post_then_pre",
+                                workload="prefill_b4_t4096_d7168"),
+    "post_then_pre_d2048": dict(bytes_per_token=step_bytes_per_token(4, 2048),
+                                param_bytes=step_param_bytes(4, 2048), kernel="hc_fused_kernel<1>",
+                                sources=FUSED_SOURCES, traffic=None, call="post_then_pre",
+                                workload="prefill_b4_t4096_d2048"),
 }
 
 
@@ -108,6 +141,10 @@ def _metric(op):
         return "HC step latency and tokens/s, single step B=1 T=64"
     if op == "long_prefill_b1_t65536":
         return "HC step tokens/s and achieved HBM GB/s vs peak, long prefill B=1 T=65536"
+    if _workload_name(op) != WORKLOAD:  # the prefill batch at another shape
+        from hyper_connection_residual_hc_gb300 import synth
+        w = synth.WORKLOADS[_workload_name(op)]
+        return "HC step tokens/s and achieved HBM GB/s vs peak, prefill B=4 T=4096, hc=%d d=%d" % (w.hc, w.d)
     return "HC %s tokens/s and achieved HBM GB/s vs peak, prefill B=4 T=4096" % op
 
 
@@ -337,7 +374,7 @@ def run_ours(args):
     hc.load()
 
     w = rank_workload(synth.WORKLOADS[_workload_name(op)], rank)
-    n, d = w.n, w.d
+    n, d, hcn = w.n, w.d, w.hc
     prm = synth.params(w, 0)
 
     def bf(a):
@@ -357,29 +394,29 @@ def run_ours(args):
     host = {k: draw[k]() for k in names}
     dev = {k: v.cuda() for k, v in host.items()}
     hc_fn = f32(prm["hc_fn"]).cuda()
-    planes = torch.empty(hc.hc_prepare_params_size(4, d) // 2, dtype=torch.bfloat16, device="cuda")
-    hc.hc_prepare_params(hc_fn, 4, d, planes)
+    planes = torch.empty(hc.hc_prepare_params_size(hcn, d) // 2, dtype=torch.bfloat16, device="cuda")
+    hc.hc_prepare_params(hc_fn, hcn, d, planes)
     scale, base, nw = f32(prm["hc_scale"]).cuda(), f32(prm["hc_base"]).cuda(), f32(prm["norm_w"]).cuda()
     P = hc.params(planes, scale, base, nw)
-    s = hc.shape(d=d, sinkhorn_iters=w.iters, hc_eps=w.hc_eps, norm_eps=w.norm_eps)
-    sf = hc.shape(d=d, norm_eps=FINAL_EPS)
+    s = hc.shape(d=d, sinkhorn_iters=w.iters, hc_eps=w.hc_eps, norm_eps=w.norm_eps, hc=hcn)
+    sf = hc.shape(d=d, norm_eps=FINAL_EPS, hc=hcn)
     fw = f32(synth.final_norm_w(w)).cuda()
 
     def empty(*shape, dt=torch.bfloat16):
         return torch.empty(shape, dtype=dt, device="cuda")
 
-    coef = lambda: dict(pre=empty(n, 4, dt=torch.float32), post=empty(n, 4, dt=torch.float32),  # noqa: E731
-                        comb=empty(n, 4, 4, dt=torch.float32))
+    coef = lambda: dict(pre=empty(n, hcn, dt=torch.float32), post=empty(n, hcn, dt=torch.float32),  # noqa: E731
+                        comb=empty(n, hcn, hcn, dt=torch.float32))
     if call in ("post_then_pre", "expand_pre_step"):
-        out = dict(X_out=empty(n, 4, d), y_normed=empty(n, d), **coef())
+        out = dict(X_out=empty(n, hcn, d), y_normed=empty(n, d), **coef())
     elif call == "post_then_pre_tap":
-        out = dict(X_out=empty(n, 4, d), y_normed=empty(n, d), stream_mean=empty(n, d), **coef())
+        out = dict(X_out=empty(n, hcn, d), y_normed=empty(n, d), stream_mean=empty(n, d), **coef())
     elif call == "pre_step":
         out = dict(y_normed=empty(n, d), **coef())
     elif call in ("post_then_final", "final"):
         out = dict(z=empty(n, d))
     else:
-        out = dict(X_out=empty(n, 4, d))
+        out = dict(X_out=empty(n, hcn, d))
     stream = torch.cuda.current_stream()
     ws = hc.new_workspace()
 
@@ -416,9 +453,9 @@ def run_ours(args):
     barrier()
     werr = hc.hc_device_error(clear=True)
 
-    # timed region: one fused launch per step, CUDA events on the launching stream around each launch;
-    # with flush_l2, a 256 MB write before every launch (outside its events), and the steps' time is
-    # the sum of the launches' own times
+    # timed region: one call per step (one fused launch; the CUDA-core path's launches for other
+    # shapes), CUDA events on the launching stream around each call; with flush_l2, a 256 MB write
+    # before every call (outside its events), and the steps' time is the sum of the calls' own times
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if spec.get("flush_l2") else None
     clocks = ClockSampler(local)
     clocks.start()
@@ -453,7 +490,7 @@ def run_ours(args):
     if call == "post_then_pre":
         # the library's host-buffer executor: chunks of tokens copied in, stepped and copied out on
         # overlapping streams, all behind one C-ABI call on host arrays
-        pipe = hc.HostPipeline(4, d, args.e2e_chunk)
+        pipe = hc.HostPipeline(hcn, d, args.e2e_chunk)
         e2e_path = "hc_host_post_then_pre, chunks of %d tokens" % pipe.chunk_tokens
     else:
         e2e_path = "copies in, hc_%s, copies out, one after another" % op
@@ -489,7 +526,16 @@ def run_ours(args):
     achieved = alg_bytes / (kern_ms / 1e3) / 1e9
     med_ms = statistics.median(per_launch)
     ctas = hc.hc_fused_ctas()
-    group, tile_m, tiles = hc.hc_plan_tiles(n, d, ctas)
+    if spec["kernel"] == GENERIC_KERNELS:
+        # the writing half in one launch, then per chunk of tokens (as many as the workspace holds raw
+        # mixes and sums of squares for) a projection launch and a split + norm launch
+        chunk = hc.hc_workspace_size() // (((2 + hcn) * hcn + 1) * 4)
+        launches = 1 + 2 * -(-n // chunk)
+        plan = {"path": "CUDA-core kernels", "chunk_tokens": chunk, "launches_per_step": launches}
+    else:
+        group, tile_m, tiles = hc.hc_plan_tiles(n, d, ctas)
+        launches = 1
+        plan = {"tile_tokens": tile_m, "tiles": tiles, "ctas_per_tile": group, "resident_ctas": ctas}
     prof = _profile(op)
 
     cpu = None
@@ -509,7 +555,7 @@ def run_ours(args):
             "warmup": max(3, args.warmup), "ms_per_step": el_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": workload_config(w, op),
-            "plan": {"tile_tokens": tile_m, "tiles": tiles, "ctas_per_tile": group, "resident_ctas": ctas},
+            "plan": plan,
             "latency_us": {"median": 1e3 * med_ms, "best": 1e3 * per_launch[0], "mean": 1e3 * kern_ms,
                            "launches": args.steps},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -526,7 +572,7 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h, "path": e2e_path},
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
-            "gpu_launches": args.steps,
+            "gpu_launches": launches * args.steps,
             "device_error": werr | derr,
         }
         print(json.dumps(line), flush=True)

@@ -10,7 +10,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libhc.so")
-SOURCES = ["hc_fused.cu", "hc_api.cu", "hc_final.cu", "hc_generic.cu", "hc_host.cu"]
+SOURCES = ["hc_fused.cu", "hc_api.cu", "hc_final.cu", "hc_generic.cu", "hc_proj.cu", "hc_host.cu"]
 HEADERS = ["hc_ptx.cuh", "hc_internal.h"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -579,7 +579,11 @@ int hc_debug_wait_flag(const unsigned long long* flags, int count, unsigned long
 
 int hc_device_error(unsigned int* word, int clear, hc_stream_t stream) {
     if (!word) return HC_ERR_NULL;
-    return read_device_error(word, clear, reinterpret_cast<cudaStream_t>(stream)) == 0 ? HC_OK : HC_ERR_CUDA;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    unsigned int fused = 0, proj = 0;
+    if (read_device_error(&fused, clear, cs) != 0 || read_proj_error(&proj, clear, cs) != 0) return HC_ERR_CUDA;
+    *word = fused | proj;
+    return HC_OK;
 }
 
 }  // extern "C"

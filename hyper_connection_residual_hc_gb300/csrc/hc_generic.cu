@@ -6,8 +6,8 @@
 //
 //   writing half   gen_post_kernel      X' = bf16(post_k * Delta + sum_j comb[j,k] X_j) (+ stream mean)
 //   head           gen_expand_kernel    X' = the embedding in every stream
-//   projection     gen_proj_kernel      raw mixes sum_c X'_c w_mc and sum_c X'_c^2, 16 tokens per CTA,
-//                                       columns staged through shared memory
+//   projection     gen_proj_tc_kernel   raw mixes sum_c X'_c w_mc and sum_c X'_c^2 on the tensor cores
+//                                       (csrc/hc_proj.cu), 128 tokens per CTA
 //   rest           gen_tail_kernel      r, split + Sinkhorn, y = bf16(sum_j pre_mix_j X'_j), RMSNorm
 //   tail           gen_final_kernel     [hc_post], collapse, final RMSNorm
 // The weights come from the bf16 planes of hc_prepare_params: w = hi + (mid + lo) is exact in fp32.
@@ -99,76 +99,6 @@ __global__ void __launch_bounds__(256) gen_expand_kernel(const uint4* __restrict
         const long long t = idx / dv, i = idx - (idx / dv) * dv;
         const uint4 v = __ldcs(h + t * dv + i);
         for (int j = 0; j < hc; ++j) __stcs(X_out + (t * hc + j) * dv + i, v);
-    }
-}
-
-// ---- projection: raw[t][m] = sum_c X_c w_mc, ssx[t] = sum_c X_c^2 ---------------------------------
-constexpr int kPTok = 16;     // tokens per CTA
-constexpr int kPCols = 64;    // columns of the flattened hc*d row per shared-memory stage
-constexpr int kPThreads = 256;
-
-__global__ void __launch_bounds__(kPThreads) gen_proj_kernel(const uint16_t* __restrict__ X,
-                                                             const uint16_t* __restrict__ planes, long long n,
-                                                             int hc, int d, float* __restrict__ raw,
-                                                             float* __restrict__ ssx) {
-    __shared__ float xs[kPTok][kPCols + 1];
-    __shared__ float ws[kGMaxMix][kPCols + 1];
-    const int M = (2 + hc) * hc;
-    const long long D = static_cast<long long>(hc) * d;
-    const long long t0 = static_cast<long long>(blockIdx.x) * kPTok;
-    const int tid = threadIdx.x;
-    const int tt = tid % kPTok, grp = tid / kPTok;       // token of this thread, mix group
-    constexpr int kGroups = kPThreads / kPTok;           // 16: mixes grp, grp + 16, ...
-    float acc[(kGMaxMix + kGroups - 1) / kGroups];
-#pragma unroll
-    for (int q = 0; q < (kGMaxMix + kGroups - 1) / kGroups; ++q) acc[q] = 0.f;
-    float sq = 0.f;
-    for (long long c0 = 0; c0 < D; c0 += kPCols) {
-        const int cw = static_cast<int>(D - c0 < kPCols ? D - c0 : kPCols);
-        for (int e = tid; e < kPTok * kPCols; e += kPThreads) {
-            const int r = e / kPCols, c = e % kPCols;
-            const long long t = t0 + r;
-            xs[r][c] = (t < n && c < cw) ? bf16f(X, t * D + c0 + c) : 0.f;
-        }
-        for (int e = tid; e < M * kPCols; e += kPThreads) {
-            const int m = e / kPCols, c = e % kPCols;
-            float w = 0.f;
-            if (c < cw) {
-                const float hi = bf16f(planes, static_cast<long long>(plane_row(hc, M, 0, m)) * D + c0 + c);
-                const float mid = bf16f(planes, static_cast<long long>(plane_row(hc, M, 1, m)) * D + c0 + c);
-                const float lo = bf16f(planes, static_cast<long long>(plane_row(hc, M, 2, m)) * D + c0 + c);
-                w = hi + (mid + lo);  // exact: the planes split w exactly
-            }
-            ws[m][c] = w;
-        }
-        __syncthreads();
-        // two-level sums: each chunk of columns on its own, then the chunk's sum into the total, so
-        // that rounding grows with the chunk and chunk counts rather than with all hc*d terms
-        float part[(kGMaxMix + kGroups - 1) / kGroups], psq = 0.f;
-#pragma unroll
-        for (int q = 0; q < (kGMaxMix + kGroups - 1) / kGroups; ++q) part[q] = 0.f;
-        for (int c = 0; c < cw; ++c) {
-            const float x = xs[tt][c];
-            if (grp == 0) psq = fmaf(x, x, psq);
-#pragma unroll
-            for (int q = 0; q < (kGMaxMix + kGroups - 1) / kGroups; ++q) {
-                const int m = grp + kGroups * q;
-                if (m < M) part[q] = fmaf(x, ws[m][c], part[q]);
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < (kGMaxMix + kGroups - 1) / kGroups; ++q) acc[q] += part[q];
-        sq += psq;
-        __syncthreads();
-    }
-    const long long t = t0 + tt;
-    if (t < n) {
-#pragma unroll
-        for (int q = 0; q < (kGMaxMix + kGroups - 1) / kGroups; ++q) {
-            const int m = grp + kGroups * q;
-            if (m < M) raw[t * M + m] = acc[q];
-        }
-        if (grp == 0) ssx[t] = sq;
     }
 }
 
@@ -374,9 +304,8 @@ int launch_generic_reading(const GenericArgs& a, cudaStream_t stream) {
     for (int64_t t0 = 0; t0 < a.n; t0 += chunk) {
         const int64_t m = a.n - t0 < chunk ? a.n - t0 : chunk;
         const uint16_t* Xc = static_cast<const uint16_t*>(a.X) + t0 * D;
-        gen_proj_kernel<<<static_cast<unsigned>((m + kPTok - 1) / kPTok), kPThreads, 0, stream>>>(
-            Xc, static_cast<const uint16_t*>(a.planes), m, a.hc, a.d, raw, ssx);
-        if (cudaGetLastError() != cudaSuccess) return -7;
+        const int st = launch_proj_tc(Xc, a.planes, m, a.hc, a.d, raw, ssx, stream);
+        if (st != 0) return st;
         gen_tail_kernel<<<static_cast<unsigned>(m), kTThreads, 0, stream>>>(
             Xc, a.pre_mix ? a.pre_mix + t0 * a.hc : nullptr, a.identity, a.hc_scale, a.hc_base, a.norm_w, raw, ssx,
             a.hc, a.d, a.iters, a.hc_eps, a.norm_eps,

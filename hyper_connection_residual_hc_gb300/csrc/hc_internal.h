@@ -107,6 +107,12 @@ int launch_generic_post(const void* X, const void* delta, const float* post, con
                         void* mean_out, int64_t n, int hc, int d, cudaStream_t stream);
 int launch_generic_expand(const void* h, void* X_out, int64_t n, int hc, int d, cudaStream_t stream);
 int launch_generic_reading(const GenericArgs& a, cudaStream_t stream);
+// The generic path's projection on the tensor cores (csrc/hc_proj.cu): raw [m, M] and ssx [m] of the
+// m tokens of X (bf16 [m, hc * d]) against the prepared planes; returns 0, -2 (shape) or -7 (CUDA).
+int launch_proj_tc(const void* X, const void* planes, int64_t m, int hc, int d, float* raw, float* ssx,
+                   cudaStream_t stream);
+// The projection kernel's device error word (read, and cleared if asked); returns 0 or -7.
+int read_proj_error(unsigned int* word, int clear, cudaStream_t stream);
 int launch_generic_final(const void* X, const void* delta, const float* post, const float* comb,
                          const float* pre_mix, const float* norm_w, void* X_out, void* z, int64_t n, int hc, int d,
                          float eps, cudaStream_t stream);

@@ -76,6 +76,11 @@ WORKLOADS = {
         Workload("long_prefill_b1_t65536_4steps", seed=3000, B=1, T=65536, steps=4, chain="fresh"),
         Workload("stress_b2_t8192_80steps", seed=4000, B=2, T=8192, steps=80, chain="stress", iters=50,
                  x_dist="t3x4", delta_sd=4.0, scale_lo=5.0, scale_hi=10.0, base_sd=3.0),
+        # the prefill batch at other stream counts and widths (the formulas hold for any hc and d)
+        Workload("prefill_b4_t4096_hc8", seed=2100, B=4, T=4096, hc=8),
+        Workload("prefill_b4_t4096_hc2", seed=2200, B=4, T=4096, hc=2),
+        Workload("prefill_b4_t4096_d7168", seed=2300, B=4, T=4096, d=7168),
+        Workload("prefill_b4_t4096_d2048", seed=2400, B=4, T=4096, d=2048),
     ]
 }
 

@@ -67,8 +67,9 @@ enum {
  * hc = 4 (hc_mult), d = 5120 (dim), sinkhorn_iters = 20, hc_eps = 1e-6, norm_eps = 1e-20. */
 typedef struct {
     int hc;             /* streams, 1..8. hc = 4 with d a multiple of 256 up to 5120 (the model's shape)
-                           runs on the fused tensor-core kernel; every other shape on plain CUDA-core
-                           kernels with the same results (slower) */
+                           runs on the fused tensor-core kernel; every other shape on the generic
+                           kernels (the projection on the tensor cores, the other steps on CUDA cores),
+                           within the same tolerances (slower) */
     int d;              /* width of one stream: a multiple of 8, at most 65536 */
     int sinkhorn_iters; /* >= 1: one softmax + column normalisation, then iters-1 row+column rounds */
     float hc_eps;       /* >= 0, finite: the eps of pre and of the Sinkhorn normalisations */
@@ -334,7 +335,8 @@ int hc_debug_wait_flag(const unsigned long long* flags, int count, unsigned long
                        hc_stream_t stream);
 
 /* Read the device-side error word of the current device: nonzero when a kernel gave up a
- * bounded wait (it then returned early and its outputs are not valid). Synchronises `stream`.
+ * bounded wait (it then returned early and its outputs are not valid); bits 0-15 are the fused
+ * kernel's waits, bits 16-19 those of the generic path's projection. Synchronises `stream`.
  * If `clear` is nonzero the word is reset to 0, and, when it was nonzero, the library's own fixed
  * scratch of hc_post_then_pre_noalloc on this device is zeroed as well (on `stream`; no call using it
  * may still be running). Returns HC_OK, HC_ERR_NULL or HC_ERR_CUDA. */

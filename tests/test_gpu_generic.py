@@ -144,3 +144,28 @@ def test_generic_uniform_logits_closed_form_hc8():
         assert np.allclose(gu.host_f32(out["pre"]), 0.5 + np.float32(eps), rtol=1e-6)
         assert np.array_equal(gu.host_f32(out["post"]), np.ones((n, hcn)))
         assert np.allclose(gu.host_f32(out["comb"]), v, rtol=1e-5)
+
+
+@pytest.mark.parametrize("name", ["prefill_b4_t4096_hc8", "prefill_b4_t4096_hc2", "prefill_b4_t4096_d7168",
+                                  "prefill_b4_t4096_d2048"])
+def test_prefill_batch_at_other_shapes(name):
+    """The 16,384-token prefill batch at 8 or 2 streams, or at d = 7168 (the CUDA-core kernels) or
+    d = 2048 (the fused kernel), in the call bench.py times: one hc_post_then_pre on all tokens,
+    checked against the oracle on the first and last tokens, tile edges and 128 random tokens."""
+    gu.COEF_STATS.clear()
+    w = synth.WORKLOADS[name]
+    prm = synth.params(w, 0)
+    P = gu.DevParams(prm, w.d, w.hc)
+    inp = dict(X=synth.tokens(w, T_X, 0), delta=synth.tokens(w, T_DELTA, 0), post=synth.tokens(w, T_POST, 0),
+               comb=synth.tokens(w, T_COMB, 0), pre_mix=synth.tokens(w, T_PREMIX, 0))
+    dev = {k: (gu.dev_bf16(v) if v.dtype == np.uint16 else gu.dev_f32(v)) for k, v in inp.items()}
+    del inp
+    out = gu.run_post_then_pre(dev["delta"], dev["X"], dev["post"], dev["comb"], dev["pre_mix"], P, gu.shape_of(w),
+                               w.n)
+    idx = gu.sample_tokens(w.n, 128, np.random.default_rng(3))
+    gu.check_sampled(w, 0, dev, out, prm, idx, True, name)
+    assert torch.isfinite(out["y_normed"].float()).all()
+    assert float((out["comb"].sum(dim=1) - 1).abs().max()) < 1e-4
+    gu.check_guards()
+    gu.device_error_clear()
+    print("%s: coefficients beyond the flat rel 1e-5 / abs 1e-6\n%s" % (name, gu.coef_stats_report()))
