@@ -7,18 +7,22 @@
 //
 // The weights are the three bf16 planes of hc_prepare_params, a [3M, hc*d] matrix with
 // w = hi + mid + lo exactly (plane_row gives each plane's row). One CTA takes 128 tokens of a chunk
-// and streams the hc*d columns in stages of 32: a TMA load of the X' tile [128 x 32] and of all 3M
-// plane rows [N x 32] (N = 3M rounded up to 16; rows past 3M and columns past hc*d read as zeros),
-// both with the 64-byte swizzle, then two tcgen05.mma kind::f16 (K = 16 each) into a TMEM
-// accumulator of N fp32 columns, one per plane row. Each product of two bf16 values is exact in
-// fp32, so the projection has the accuracy of an fp32 dot product.
+// and streams the hc*d columns in stages of 32: a TMA load of the X' tile [128 x 32] and of the plane
+// rows [N x 32], both with the 64-byte swizzle, then two tcgen05.mma kind::f16 (K = 16 each) into a
+// TMEM accumulator of N fp32 columns. The planes are loaded through a 3-D view (4-D for the grouping
+// the fused kernel uses at hc = 4) whose strides put the three planes of a mix side by side, so that
+// accumulator column 3 i + pl holds plane pl of mix slot i; the mix slots are the M mixes padded to a
+// multiple of 16 (N = 3 * that), and rows past the planes and columns past hc*d read as zeros. Each
+// product of two bf16 values is exact in fp32, so the projection has the accuracy of an fp32 dot
+// product.
 //
-// Two accumulators take blocks of 8 stages in turn. While the tensor cores fill one, the four row
-// warps (warp q: TMEM lanes and tile rows 32q..32q+31) add the other's columns into their rows'
-// running fp32 sums per mix in shared memory: a sum of 256-column partial sums, as the fused kernel
-// sums its stages. Between drains they sum the squares of their rows from the same shared tiles.
-// Warp 4 issues the loads and warp 5 the MMAs. Every wait is bounded: on expiry the kernel sets a
-// bit in its device error word, stops waiting, lets its copies land and frees its tensor memory.
+// Two accumulators take blocks of 8 stages in turn. While the tensor cores fill one, four drain
+// warps (warp 4 + q: TMEM lanes and tile rows 32q..32q+31) add the other's (hi + mid) + lo of every
+// mix into running fp32 sums held in registers: a sum of 256-column partial sums, as the fused
+// kernel sums its stages. Four square warps sum the squares of the rows from the shared tiles and
+// release the slots, so a drain never holds up the loads. Warp 8 issues the loads, warp 9 the MMAs.
+// Every wait is bounded: on expiry the kernel sets a bit in its device error word, stops waiting,
+// lets its copies land and frees its tensor memory.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -38,8 +42,8 @@ constexpr int kPjRows = 128;                     // tokens per CTA: the MMA's M
 constexpr int kPjCols = 32;                      // columns per stage: one 64-byte row per token
 constexpr int kPjATile = kPjRows * kPjCols * 2;  // 8 KB
 constexpr int kPjBlock = 8;                      // stages per accumulator block (256 columns)
-constexpr int kPjThreads = 192;                  // warps 0-3 rows, 4 loads, 5 MMAs
-constexpr int kPjWarpLoad = 4, kPjWarpMma = 5;
+constexpr int kPjThreads = 320;                  // warps 0-3 squares, 4-7 drains, 8 loads, 9 MMAs
+constexpr int kPjWarpDrain = 4, kPjWarpLoad = 8, kPjWarpMma = 9;
 constexpr int kPjMaxSlots = 8;
 constexpr int kPjSmemBudget = 200 * 1024;
 constexpr uint64_t kPjWaitNs = 1000000000ull;  // 1 s
@@ -55,7 +59,7 @@ struct ProjParams {
     long long m;      // tokens of the chunk
     int hc;
     int M;            // (2 + hc) * hc
-    int N;            // accumulator columns: 3M rounded up to 16
+    int N;            // accumulator columns: 3 per mix slot (M rounded up to 16 slots)
     int stages;       // ceil(hc * d / 32)
     int slots;        // load ring depth
     int tmem_cols;    // allocated TMEM columns (a power of two >= 2N)
@@ -63,11 +67,10 @@ struct ProjParams {
 
 // shared-memory layout, the same on host and device
 struct ProjLayout {
-    int slot_bytes, off_sums, off_bars, bytes;
-    __host__ __device__ ProjLayout(int N, int M, int slots) {
+    int slot_bytes, off_bars, bytes;
+    __host__ __device__ ProjLayout(int N, int slots) {
         slot_bytes = kPjATile + N * kPjCols * 2;
-        off_sums = slots * slot_bytes;
-        off_bars = (off_sums + M * kPjRows * 4 + 7) & ~7;
+        off_bars = slots * slot_bytes;
         bytes = off_bars + (2 * slots + 5) * 8 + 8;  // full, empty, 2 acc full, 2 acc empty, mma done; tmem + abort
     }
 };
@@ -100,11 +103,15 @@ struct PjWait {
     }
 };
 
-// the mix whose plane sits in plane row j (the inverse of plane_row)
-__device__ __forceinline__ int mix_of_row(int hc, int M, int j) {
-    return hc == 4 ? 12 * (j / 36) + (j % 36) % 12 : j % M;
+// the mix in mix slot i of the accumulator, or -1 for a padding slot: the slots follow the mixes,
+// except at hc = 4, where each half of the 24 mixes fills 12 of 16 slots
+__device__ __forceinline__ int mix_of_slot(int hc, int M, int i) {
+    if (hc == 4) return i % 16 < 12 ? 12 * (i / 16) + i % 16 : -1;
+    return i < M ? i : -1;
 }
 
+// kMC: mix slots / 16 (the drain warps' running sums, 16 per chunk, live in registers)
+template <int kMC>
 __global__ void __launch_bounds__(kPjThreads, 1) gen_proj_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                                     const __grid_constant__ CUtensorMap tmB,
                                                                     const ProjParams p) {
@@ -112,8 +119,7 @@ __global__ void __launch_bounds__(kPjThreads, 1) gen_proj_tc_kernel(const __grid
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
-    const ProjLayout L(p.N, p.M, p.slots);
-    float* sums = reinterpret_cast<float*>(smem + L.off_sums);  // [M][128]: mix-major, a row per lane
+    const ProjLayout L(p.N, p.slots);
     const uint32_t bars = sbase + static_cast<uint32_t>(L.off_bars);
     auto full = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
     auto empty = [&](int i) { return bars + 8u * static_cast<uint32_t>(p.slots + i); };
@@ -130,11 +136,11 @@ __global__ void __launch_bounds__(kPjThreads, 1) gen_proj_tc_kernel(const __grid
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.slots; ++i) {
             mbar_init(full(i), 1);
-            mbar_init(empty(i), 1 + 4);  // the MMAs' completion + the four row warps' squares
+            mbar_init(empty(i), 1 + 4);  // the MMAs' completion + the four square warps
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full(b), 1);
-            mbar_init(acc_empty(b), 4);
+            mbar_init(acc_empty(b), 4);  // the four drain warps
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0u;
@@ -148,14 +154,13 @@ __global__ void __launch_bounds__(kPjThreads, 1) gen_proj_tc_kernel(const __grid
         tmem_alloc(smem_u32(tmem_ptr), static_cast<uint32_t>(p.tmem_cols));
         tmem_relinquish();
     }
-    for (int i = static_cast<int>(threadIdx.x); i < p.M * kPjRows; i += kPjThreads) sums[i] = 0.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_ptr);
 
     if (warp == kPjWarpLoad) {
-        // ===== TMA: stage s into slot s % slots, once the MMAs and the row warps are done with it ====
+        // ===== TMA: stage s into slot s % slots, once the MMAs and the square warps are done with it =
         if (lane == 0) {
             const uint64_t pol_stream = policy_evict_normal(), pol_keep = policy_evict_last();
             for (int s = 0; s < S; ++s) {
@@ -164,7 +169,10 @@ __global__ void __launch_bounds__(kPjThreads, 1) gen_proj_tc_kernel(const __grid
                 const uint32_t a = sbase + static_cast<uint32_t>(i * L.slot_bytes);
                 mbar_arrive_expect_tx(full(i), static_cast<uint32_t>(L.slot_bytes));
                 tma_load_2d(a, &tmA, full(i), kPjCols * s, row0, pol_stream);
-                tma_load_2d(a + kPjATile, &tmB, full(i), kPjCols * s, 0, pol_keep);
+                if (p.hc == 4)
+                    tma_load_4d(a + kPjATile, &tmB, full(i), kPjCols * s, 0, 0, 0, pol_keep);
+                else
+                    tma_load_3d(a + kPjATile, &tmB, full(i), kPjCols * s, 0, 0, pol_keep);
             }
             // every load lands before the CTA may exit (a slot's last load lands after its earlier ones)
             for (int s = S - p.slots > 0 ? S - p.slots : 0; s < S; ++s)
@@ -172,12 +180,12 @@ __global__ void __launch_bounds__(kPjThreads, 1) gen_proj_tc_kernel(const __grid
         }
         __syncwarp();
     } else if (warp == kPjWarpMma) {
-        // ===== MMA: block b of 16 stages into accumulator b % 2 ======================================
+        // ===== MMA: block b of 8 stages into accumulator b % 2 =======================================
         const uint32_t idesc = idesc_bf16_f32(kPjRows, p.N);
         for (int s = 0; s < S; ++s) {
             const int i = s % p.slots, round = s / p.slots;
             const int b = s / kPjBlock, buf = b & 1;
-            // the accumulator's previous block (b - 2) must have been drained by the row warps
+            // the accumulator's previous block (b - 2) must have been drained
             if (s % kPjBlock == 0 && b >= 2) W.wait(acc_empty(buf), static_cast<uint32_t>(((b >> 1) - 1) & 1), kPjErrMma);
             W.wait(full(i), static_cast<uint32_t>(round & 1), kPjErrMma);
             tc_fence_after();
@@ -198,29 +206,47 @@ __global__ void __launch_bounds__(kPjThreads, 1) gen_proj_tc_kernel(const __grid
             W.drain(mma_done, 0u);
         }
         __syncwarp();
-    } else {
-        // ===== row warps: squares of the rows, and the accumulator blocks into the running sums =====
-        const int r = 32 * warp + lane;
-        const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
-        float sq = 0.f;
-        int drained = 0;
-        auto drain_block = [&](int b) {
+    } else if (warp >= kPjWarpDrain) {
+        // ===== drain warps: each block's (hi + mid) + lo of every mix into the running sums ==========
+        const int q = warp - kPjWarpDrain;
+        const int r = 32 * q + lane;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        float acc[kMC * 16];
+#pragma unroll
+        for (int i = 0; i < kMC * 16; ++i) acc[i] = 0.f;
+        for (int b = 0; b < nblocks; ++b) {
             const int buf = b & 1;
             W.wait(acc_full(buf), static_cast<uint32_t>((b >> 1) & 1), kPjErrRows);
             tc_fence_after();
-            for (int c0 = 0; c0 < p.N; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld16_wait(tl + static_cast<uint32_t>(buf * p.N + c0), v);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int j = c0 + e;
-                    if (j < 3 * p.M) sums[mix_of_row(p.hc, p.M, j) * kPjRows + r] += __uint_as_float(v[e]);
-                }
+            for (int c = 0; c < kMC; ++c) {
+                // mix slots 16c .. 16c + 15: accumulator columns 48c .. 48c + 47, three planes each
+                uint32_t v0[16], v1[16], v2[16];
+                const uint32_t col = tl + static_cast<uint32_t>(buf * p.N + 48 * c);
+                tmem_ld16_wait(col, v0);
+                tmem_ld16_wait(col + 16u, v1);
+                tmem_ld16_wait(col + 32u, v2);
+                // column k of the 48 (a compile-time index once unrolled)
+                auto at = [&](int k) { return __uint_as_float(k < 16 ? v0[k & 15] : k < 32 ? v1[k & 15] : v2[k & 15]); };
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[16 * c + i] += (at(3 * i) + at(3 * i + 1)) + at(3 * i + 2);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty(buf));
-        };
+        }
+        const long long t = static_cast<long long>(row0) + r;
+        if (t < p.m) {
+#pragma unroll
+            for (int i = 0; i < kMC * 16; ++i) {
+                const int mm = mix_of_slot(p.hc, p.M, i);
+                if (mm >= 0) p.raw[t * p.M + mm] = acc[i];
+            }
+        }
+    } else {
+        // ===== square warps: the squares of the rows, then the slot goes back to the loads ==========
+        const int r = 32 * warp + lane;
+        float sq = 0.f;
         for (int s = 0; s < S; ++s) {
             const int i = s % p.slots, round = s / p.slots;
             W.wait(full(i), static_cast<uint32_t>(round & 1), kPjErrRows);
@@ -241,15 +267,9 @@ __global__ void __launch_bounds__(kPjThreads, 1) gen_proj_tc_kernel(const __grid
             sq += part;
             __syncwarp();
             if (lane == 0) mbar_arrive(empty(i));
-            // block b is drained half a block after it ends, when its MMAs have long completed
-            if (s % kPjBlock == kPjBlock / 2 && s >= kPjBlock) drain_block(drained++);
         }
-        while (drained < nblocks) drain_block(drained++);
         const long long t = static_cast<long long>(row0) + r;
-        if (t < p.m) {
-            for (int mm = 0; mm < p.M; ++mm) p.raw[t * p.M + mm] = sums[mm * kPjRows + r];
-            p.ssx[t] = sq;
-        }
+        if (t < p.m) p.ssx[t] = sq;
     }
     tc_fence_before();
     __syncthreads();
@@ -273,17 +293,44 @@ PFN_cuTensorMapEncodeTiled_v12000 proj_encode_fn() {
     return fn;
 }
 
-// a 2-D bf16 tensor map [rows, cols] (row stride cols * 2 bytes) with boxes of box_rows x 32 columns
-bool encode_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+// a bf16 tensor map of `rank` dimensions (dims[0] = columns, the other strides in bytes) whose box is
+// 32 columns by box[1..]
+bool encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                const uint32_t* box_rest) {
     auto fn = proj_encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kPjCols), box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+    cuuint64_t gd[4], gs[3];
+    cuuint32_t bx[4], es[4];
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bx[i] = i == 0 ? static_cast<cuuint32_t>(kPjCols) : box_rest[i - 1];
+        es[i] = 1;
+        if (i > 0) gs[i - 1] = strides[i - 1];
+    }
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base), gd, gs, bx,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int kMC>
+int launch_mc(const CUtensorMap& tmA, const CUtensorMap& tmB, const ProjParams& p, unsigned grid, int smem,
+              cudaStream_t stream) {
+    // the kernel's shared-memory limit, once per device
+    static std::mutex mu;
+    static bool done[kPjMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kPjMaxDevices) return -7;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!done[dev]) {
+            if (cudaFuncSetAttribute(gen_proj_tc_kernel<kMC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kPjSmemBudget) != cudaSuccess)
+                return -7;
+            done[dev] = true;
+        }
+    }
+    gen_proj_tc_kernel<kMC><<<grid, kPjThreads, static_cast<size_t>(smem), stream>>>(tmA, tmB, p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -7;
 }
 
 }  // namespace
@@ -291,18 +338,36 @@ bool encode_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
 int launch_proj_tc(const void* X, const void* planes, int64_t m, int hc, int d, float* raw, float* ssx,
                    cudaStream_t stream) {
     if (m <= 0) return 0;
+    if (hc < 1 || hc > 8 || d % 8 != 0) return -2;
     const int M = (2 + hc) * hc;
-    const int N = (3 * M + 15) / 16 * 16;
-    if (hc < 1 || N > 256 || d % 8 != 0) return -2;
+    const int slots_mix = hc == 4 ? 32 : (M + 15) / 16 * 16;  // mix slots, a multiple of 16
+    const int N = 3 * slots_mix;                               // at most 240
     const uint64_t D = static_cast<uint64_t>(hc) * static_cast<uint64_t>(d);
     int slots = kPjMaxSlots;
-    while (slots > 2 && ProjLayout(N, M, slots).bytes + 1024 > kPjSmemBudget) --slots;
-    const int smem = ProjLayout(N, M, slots).bytes + 1024;
+    while (slots > 2 && ProjLayout(N, slots).bytes + 1024 > kPjSmemBudget) --slots;
+    const int smem = ProjLayout(N, slots).bytes + 1024;
     int tcols = 32;
     while (tcols < 2 * N) tcols *= 2;
     CUtensorMap tmA, tmB;
-    if (!encode_rows(&tmA, X, D, static_cast<uint64_t>(m), kPjRows)) return -7;
-    if (!encode_rows(&tmB, planes, D, static_cast<uint64_t>(3 * M), static_cast<uint32_t>(N))) return -7;
+    {
+        const uint64_t dims[2] = {D, static_cast<uint64_t>(m)};
+        const uint64_t str[1] = {D * 2};
+        const uint32_t box[1] = {static_cast<uint32_t>(kPjRows)};
+        if (!encode_map(&tmA, X, 2, dims, str, box)) return -7;
+    }
+    if (hc == 4) {
+        // plane rows 36 h + 12 pl + i (mix 12 h + i): [h][i][pl] with i padded to 16
+        const uint64_t dims[4] = {D, 3, 12, 2};
+        const uint64_t str[3] = {12 * D * 2, D * 2, 36 * D * 2};
+        const uint32_t box[3] = {3, 16, 2};
+        if (!encode_map(&tmB, planes, 4, dims, str, box)) return -7;
+    } else {
+        // plane rows pl * M + m: [m][pl], m padded to the mix slots
+        const uint64_t dims[3] = {D, 3, static_cast<uint64_t>(M)};
+        const uint64_t str[2] = {static_cast<uint64_t>(M) * D * 2, D * 2};
+        const uint32_t box[2] = {3, static_cast<uint32_t>(slots_mix)};
+        if (!encode_map(&tmB, planes, 3, dims, str, box)) return -7;
+    }
     ProjParams p;
     p.raw = raw;
     p.ssx = ssx;
@@ -313,23 +378,15 @@ int launch_proj_tc(const void* X, const void* planes, int64_t m, int hc, int d, 
     p.stages = static_cast<int>((D + kPjCols - 1) / kPjCols);
     p.slots = slots;
     p.tmem_cols = tcols;
-    {
-        // the kernel's shared-memory limit, once per device
-        static std::mutex mu;
-        static bool done[kPjMaxDevices] = {};
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kPjMaxDevices) return -7;
-        std::lock_guard<std::mutex> lk(mu);
-        if (!done[dev]) {
-            if (cudaFuncSetAttribute(gen_proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPjSmemBudget) !=
-                cudaSuccess)
-                return -7;
-            done[dev] = true;
-        }
-    }
     const unsigned grid = static_cast<unsigned>((m + kPjRows - 1) / kPjRows);
-    gen_proj_tc_kernel<<<grid, kPjThreads, static_cast<size_t>(smem), stream>>>(tmA, tmB, p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -7;
+    switch (slots_mix / 16) {
+        case 1: return launch_mc<1>(tmA, tmB, p, grid, smem, stream);
+        case 2: return launch_mc<2>(tmA, tmB, p, grid, smem, stream);
+        case 3: return launch_mc<3>(tmA, tmB, p, grid, smem, stream);
+        case 4: return launch_mc<4>(tmA, tmB, p, grid, smem, stream);
+        case 5: return launch_mc<5>(tmA, tmB, p, grid, smem, stream);
+        default: return -2;
+    }
 }
 
 int read_proj_error(unsigned int* word, int clear, cudaStream_t stream) {
