@@ -57,8 +57,8 @@ def step_param_bytes(hc: int, d: int) -> int:
 CSRC = "hyper_connection_residual_hc_gb300/csrc/"
 FUSED_SOURCES = [CSRC + "hc_fused.cu", CSRC + "hc_ptx.cuh"]
 FINAL_SOURCES = [CSRC + "hc_final.cu"]
-GENERIC_SOURCES = [CSRC + "hc_generic.cu"]
-GENERIC_KERNELS = "gen_post_kernel, gen_proj_kernel, gen_tail_kernel"
+GENERIC_SOURCES = [CSRC + "hc_generic.cu", CSRC + "hc_proj.cu"]
+GENERIC_KERNELS = "gen_post_kernel, gen_proj_tc_kernel, gen_tail_kernel"
 
 # Per op: algorithmic bytes per token and per call (parameters), the kernel it launches, the sources
 # that kernel is built from, and the ncu summary of that kernel on this workload; `call` is the entry
@@ -94,9 +94,9 @@ OPS = {
     "long_prefill_b1_t65536": dict(bytes_per_token=BYTES_PER_TOKEN, param_bytes=PARAM_BYTES,
                                    kernel="hc_fused_kernel<1>", sources=FUSED_SOURCES, traffic=None,
                                    call="post_then_pre", workload="long_prefill_b1_t65536_4steps"),
-    # the step on the prefill batch at other shapes: 8 or 2 streams, or d = 7168, on the CUDA-core
-    # kernels (the writing half, then per chunk of tokens the projection and the split + norm); d = 2048
-    # on the fused kernel
+    # the step on the prefill batch at other shapes: 8 or 2 streams, or d = 7168, on the generic kernels
+    # (the writing half, then per chunk of tokens the tensor-core projection and the split + norm);
+    # d = 2048 on the fused kernel
     "post_then_pre_hc8": dict(bytes_per_token=step_bytes_per_token(8, 5120), param_bytes=step_param_bytes(8, 5120),
                               kernel=GENERIC_KERNELS, sources=GENERIC_SOURCES, traffic=None, call="post_then_pre",
                               workload="prefill_b4_t4096_hc8"),
@@ -531,7 +531,8 @@ def run_ours(args):
         # mixes and sums of squares for) a projection launch and a split + norm launch
         chunk = hc.hc_workspace_size() // (((2 + hcn) * hcn + 1) * 4)
         launches = 1 + 2 * -(-n // chunk)
-        plan = {"path": "CUDA-core kernels", "chunk_tokens": chunk, "launches_per_step": launches}
+        plan = {"path": "generic kernels (projection on tcgen05)", "chunk_tokens": chunk,
+                "launches_per_step": launches}
     else:
         group, tile_m, tiles = hc.hc_plan_tiles(n, d, ctas)
         launches = 1

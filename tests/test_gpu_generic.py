@@ -1,8 +1,9 @@
-"""The generic path (plain CUDA-core kernels) against the oracle: any number of streams hc in 1..8
-and any stream width d that is a multiple of 8, through every entry point. hc = 4 at widths the
-fused kernel does not take (not a multiple of 256, or above 5120) runs here too. The formulas are
-the model's for any hc ("Source layer, pairs pooled" page, Block excerpts; "Reading weights" page,
-hc_split_sinkhorn; "Write the streams" and "Final RMSNorm" pages); tolerances as in gpu_util.
+"""The generic path (the projection on the tensor cores, the other steps on CUDA cores) against the
+oracle: any number of streams hc in 1..8 and any stream width d that is a multiple of 8, through
+every entry point. hc = 4 at widths the fused kernel does not take (not a multiple of 256, or above
+5120) runs here too. The formulas are the model's for any hc ("Source layer, pairs pooled" page,
+Block excerpts; "Reading weights" page, hc_split_sinkhorn; "Write the streams" and "Final RMSNorm"
+pages); tolerances as in gpu_util.
 """
 
 import numpy as np
@@ -149,7 +150,7 @@ def test_generic_uniform_logits_closed_form_hc8():
 @pytest.mark.parametrize("name", ["prefill_b4_t4096_hc8", "prefill_b4_t4096_hc2", "prefill_b4_t4096_d7168",
                                   "prefill_b4_t4096_d2048"])
 def test_prefill_batch_at_other_shapes(name):
-    """The 16,384-token prefill batch at 8 or 2 streams, or at d = 7168 (the CUDA-core kernels) or
+    """The 16,384-token prefill batch at 8 or 2 streams, or at d = 7168 (the generic kernels) or
     d = 2048 (the fused kernel), in the call bench.py times: one hc_post_then_pre on all tokens,
     checked against the oracle on the first and last tokens, tile edges and 128 random tokens."""
     gu.COEF_STATS.clear()
