@@ -97,10 +97,11 @@ typedef struct {
 int hc_prepare_params_size(int hc, int d, size_t* bytes);
 
 /* Split an fp32 hc_fn [(2+hc)*hc, hc*d] [device] into three bf16 planes hi + mid + lo whose sum
- * equals every fp32 weight exactly, laid out for the fused kernels' tensor-core projection,
- * into `planes` [device] (hc_prepare_params_size bytes, 16-byte aligned). Run it once per
- * parameter set (weights are static); the planes stay valid while hc_fn is unchanged.
- * No counterpart on the pages: it is this library's weight packing. hc in 1..8. */
+ * equals every fp32 weight exactly, laid out for the tensor-core projections, into `planes`
+ * [device] (hc_prepare_params_size bytes, 16-byte aligned): [3*mix_hc, hc*d] rows, at hc = 4 row
+ * 36h + 12p + i holding plane p of mix 12h + i, at any other hc row p*mix_hc + m holding plane p
+ * of mix m. Run it once per parameter set (weights are static); the planes stay valid while hc_fn
+ * is unchanged. No counterpart on the pages: it is this library's weight packing. hc in 1..8. */
 int hc_prepare_params(const float* hc_fn, int hc, int d, void* planes, hc_stream_t stream);
 
 /* Size in bytes of the workspace the fused calls (hc_pre_step, hc_post_then_pre,
