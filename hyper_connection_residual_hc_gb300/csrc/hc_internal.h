@@ -108,7 +108,8 @@ int launch_generic_post(const void* X, const void* delta, const float* post, con
 int launch_generic_expand(const void* h, void* X_out, int64_t n, int hc, int d, cudaStream_t stream);
 int launch_generic_reading(const GenericArgs& a, cudaStream_t stream);
 // The generic path's projection on the tensor cores (csrc/hc_proj.cu): raw [m, M] and ssx [m] of the
-// m tokens of X (bf16 [m, hc * d]) against the prepared planes; returns 0, -2 (shape) or -7 (CUDA).
+// m tokens of X (bf16 [m, hc * d]) against the prepared planes; returns 0, -3 (a shape it does not
+// take: hc outside 1..8 or d not a multiple of 8) or -7 (CUDA).
 int launch_proj_tc(const void* X, const void* planes, int64_t m, int hc, int d, float* raw, float* ssx,
                    cudaStream_t stream);
 // The projection kernel's device error word (read, and cleared if asked); returns 0 or -7.

@@ -338,7 +338,7 @@ int launch_mc(const CUtensorMap& tmA, const CUtensorMap& tmB, const ProjParams& 
 int launch_proj_tc(const void* X, const void* planes, int64_t m, int hc, int d, float* raw, float* ssx,
                    cudaStream_t stream) {
     if (m <= 0) return 0;
-    if (hc < 1 || hc > 8 || d % 8 != 0) return -2;
+    if (hc < 1 || hc > 8 || d % 8 != 0) return -3;
     const int M = (2 + hc) * hc;
     const int slots_mix = hc == 4 ? 32 : (M + 15) / 16 * 16;  // mix slots, a multiple of 16
     const int N = 3 * slots_mix;                               // at most 240
@@ -385,7 +385,7 @@ int launch_proj_tc(const void* X, const void* planes, int64_t m, int hc, int d, 
         case 3: return launch_mc<3>(tmA, tmB, p, grid, smem, stream);
         case 4: return launch_mc<4>(tmA, tmB, p, grid, smem, stream);
         case 5: return launch_mc<5>(tmA, tmB, p, grid, smem, stream);
-        default: return -2;
+        default: return -3;
     }
 }
 
